@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for jagged attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it and it
+never calls the CUDA library: the two share no code.
+
+The arithmetic lives in ``jfa_oracle.c`` (plain C, fp64, one thread per
+(sequence, head) unit); this module compiles it with gcc on first use and wraps
+it with ctypes.  Arrays are float64 numpy arrays in [rows, heads, dim] layout;
+offsets are int32 with offsets[0] == 0 (the packed-sequence convention of the
+jagged-attention pages: sequence b is rows offsets[b] .. offsets[b+1]-1).
+
+Functions
+---------
+attn_fwd   exact softmax(scale Q K^T) V per sequence and head, plus the natural-log
+           log-sum-exp per row; self-attention or broadcast-Q (nq > 0).
+attn_bwd   dQ, dK, dV for the loss sum(O * dO); broadcast-Q sums the shared-Q
+           gradient over all sequences.
+block_fwd  / block_bwd: the same inside fixed blocks of ``block`` tokens.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "jfa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libjfa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no -ffast-math: IEEE fp64 throughout)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", _SRC,
+                               "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            bp = ctypes.c_void_p
+            i, d = ctypes.c_int, ctypes.c_double
+            lib.oracle_attn_fwd.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, i, bp, dp, dp, i]
+            lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, i, i, d, i, bp, dp, dp, dp, i]
+            lib.oracle_block_fwd.argtypes = [dp, dp, dp, ip, i, i, i, d, i, bp, dp, i]
+            lib.oracle_block_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, d, i, bp, dp, dp, dp, i]
+            for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_block_fwd, lib.oracle_block_bwd):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _offs(offsets) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
+
+
+def _sel(sel, batch, H):
+    if sel is None:
+        return None, None
+    s = np.ascontiguousarray(np.asarray(sel, dtype=np.uint8).reshape(batch * H))
+    return s, s.ctypes.data_as(ctypes.c_void_p)
+
+
+def attn_fwd(q, k, v, offsets, *, scale: float, causal: bool = False, nq: int = 0,
+             sel=None, nthreads: int = 0, out=None):
+    """Returns (o, lse, threads_used).
+
+    Self mode (nq == 0): q [T,H,D], k/v [T,Hkv,D] -> o [T,H,D], lse [H,T].
+    Broadcast (nq > 0): q [nq,H,D] -> o [B*nq,H,D], lse [H,B*nq].
+    Units not selected by ``sel`` ([B,H] bool) are left as NaN.
+    """
+    lib = _load()
+    q, k, v, offsets = _f64(q), _f64(k), _f64(v), _offs(offsets)
+    B = offsets.shape[0] - 1
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    rows = B * nq if nq > 0 else int(offsets[-1])
+    o = np.full((rows, H, D), np.nan)
+    lse = np.full((H, rows), np.nan)
+    s_arr, s_ptr = _sel(sel, B, H)
+    used = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                               B, nq, H, Hkv, D, float(scale), int(bool(causal)), s_ptr, _ptr(o), _ptr(lse),
+                               int(nthreads))
+    if used < 0:
+        raise ValueError(f"oracle_attn_fwd rejected its arguments ({used})")
+    return o, lse, used
+
+
+def attn_bwd(q, k, v, dout, offsets, *, scale: float, causal: bool = False, nq: int = 0,
+             sel=None, nthreads: int = 0):
+    """Returns (dq, dk, dv, threads_used) for the loss sum(O * dout)."""
+    lib = _load()
+    q, k, v, dout, offsets = _f64(q), _f64(k), _f64(v), _f64(dout), _offs(offsets)
+    B = offsets.shape[0] - 1
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    s_arr, s_ptr = _sel(sel, B, H)
+    used = lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                               offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, nq, H, Hkv, D,
+                               float(scale), int(bool(causal)), s_ptr, _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    if used < 0:
+        raise ValueError(f"oracle_attn_bwd rejected its arguments ({used})")
+    return dq, dk, dv, used
+
+
+def block_fwd(q, k, v, offsets, *, scale: float, block: int = 64, sel=None, nthreads: int = 0):
+    """Block-diagonal forward; returns (o, threads_used)."""
+    lib = _load()
+    q, k, v, offsets = _f64(q), _f64(k), _f64(v), _offs(offsets)
+    B = offsets.shape[0] - 1
+    H, D = q.shape[1], q.shape[2]
+    o = np.full_like(q, np.nan)
+    s_arr, s_ptr = _sel(sel, B, H)
+    used = lib.oracle_block_fwd(_ptr(q), _ptr(k), _ptr(v), offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                B, H, D, float(scale), int(block), s_ptr, _ptr(o), int(nthreads))
+    if used < 0:
+        raise ValueError(f"oracle_block_fwd rejected its arguments ({used})")
+    return o, used
+
+
+def block_bwd(q, k, v, dout, offsets, *, scale: float, block: int = 64, sel=None, nthreads: int = 0):
+    """Block-diagonal backward; returns (dq, dk, dv, threads_used)."""
+    lib = _load()
+    q, k, v, dout, offsets = _f64(q), _f64(k), _f64(v), _f64(dout), _offs(offsets)
+    B = offsets.shape[0] - 1
+    H, D = q.shape[1], q.shape[2]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    s_arr, s_ptr = _sel(sel, B, H)
+    used = lib.oracle_block_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, H, D, float(scale),
+                                int(block), s_ptr, _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    if used < 0:
+        raise ValueError(f"oracle_block_bwd rejected its arguments ({used})")
+    return dq, dk, dv, used

@@ -1,0 +1,291 @@
+"""Pins for the fp64 oracle: it is checked against things other than itself.
+
+- the offsets worked example printed on the pages (tests/golden/),
+- textbook dense attention in matrix form (scipy softmax / logsumexp),
+- closed forms (zero queries, equal values, single tokens),
+- structural equalities (packed == per-piece, broadcast dQ == sum over pieces,
+  block mode == jagged attention over 64-token pieces),
+- central finite differences of the forward for every gradient,
+- invariants (softmax rows sum to 1, keys' gradients sum to zero).
+Each check is chosen so that a dropped term, a wrong sign or index, or a
+transposed operand in the oracle fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.dense_ref import packed_dense
+from variable_length_attention_gb300.workloads import offsets_from_lengths
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [int(x) for x in rest]
+    return vals
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _problem(rng, lengths, H, Hkv, D, nq=0):
+    offs = offsets_from_lengths(lengths)
+    T = int(offs[-1])
+    q = _rand(rng, nq if nq else T, H, D)
+    k = _rand(rng, T, Hkv, D)
+    v = _rand(rng, T, Hkv, D)
+    rows = len(lengths) * nq if nq else T
+    do = _rand(rng, rows, H, D)
+    return offs, q, k, v, do
+
+
+# --------------------------------------------------------------------------- offsets
+@pytest.mark.parametrize("name", ["offsets_worked_example.txt", "offsets_tiny_workload.txt"])
+def test_offsets_golden(name):
+    g = _read_golden(name)
+    offs = offsets_from_lengths(g["lengths"])
+    assert offs.tolist() == g["offsets"]
+    if "padded_slots" in g:
+        assert len(g["lengths"]) * max(g["lengths"]) == g["padded_slots"][0]
+        assert int(offs[-1]) == g["valid_tokens"][0]
+
+
+# --------------------------------------------------------------------------- dense brute force
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv,D", [(2, 2, 4), (4, 2, 8), (4, 1, 8)])
+def test_forward_matches_textbook_dense(causal, H, Hkv, D):
+    rng = np.random.default_rng(11 + H + 7 * Hkv + D + int(causal))
+    lengths = [3, 1, 9, 0, 6]
+    offs, q, k, v, _ = _problem(rng, lengths, H, Hkv, D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=scale, causal=causal)
+    o_ref, lse_ref = packed_dense(q, k, v, offs, scale, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_broadcast_forward_matches_textbook_dense():
+    rng = np.random.default_rng(5)
+    lengths = [4, 0, 7, 1]
+    offs, q, k, v, _ = _problem(rng, lengths, 2, 2, 8, nq=5)
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.3, nq=5)
+    o_ref, lse_ref = packed_dense(q, k, v, offs, 0.3, nq=5)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isinf(lse), np.isinf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=0, atol=1e-12)
+    # empty sequence: zero output rows, log-sum-exp of nothing is -inf
+    assert np.all(o[5:10] == 0.0) and np.all(lse[:, 5:10] == -np.inf)
+
+
+# --------------------------------------------------------------------------- invariants / closed forms
+def test_softmax_rows_sum_to_one():
+    # With V = identity (D >= L) the output row is the softmax row itself.
+    rng = np.random.default_rng(3)
+    L, D = 7, 8
+    offs = offsets_from_lengths([L])
+    q = _rand(rng, L, 1, D) * 3
+    k = _rand(rng, L, 1, D) * 3
+    v = np.zeros((L, 1, D))
+    v[np.arange(L), 0, np.arange(L)] = 1.0
+    for causal in (False, True):
+        o, _, _ = oracle.attn_fwd(q, k, v, offs, scale=0.5, causal=causal)
+        p = o[:, 0, :L]
+        assert np.all(p >= 0)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        if causal:
+            assert np.all(np.triu(p, 1) == 0.0)
+
+
+def test_zero_queries_average_values():
+    rng = np.random.default_rng(4)
+    lengths = [5, 3]
+    offs, q, k, v, _ = _problem(rng, lengths, 2, 2, 4)
+    q[:] = 0.0
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=1.0)
+    for b, (a, e) in enumerate(zip(offs[:-1], offs[1:])):
+        np.testing.assert_allclose(o[a:e], np.broadcast_to(v[a:e].mean(axis=0), o[a:e].shape), atol=1e-14)
+        np.testing.assert_allclose(lse[:, a:e], math.log(e - a), atol=1e-14)
+    oc, lsec, _ = oracle.attn_fwd(q, k, v, offs, scale=1.0, causal=True)
+    for a, e in zip(offs[:-1], offs[1:]):
+        for i in range(e - a):
+            np.testing.assert_allclose(oc[a + i], v[a:a + i + 1].mean(axis=0), atol=1e-14)
+            np.testing.assert_allclose(lsec[:, a + i], math.log(i + 1), atol=1e-14)
+
+
+def test_single_token_sequences():
+    rng = np.random.default_rng(6)
+    offs, q, k, v, do = _problem(rng, [1, 1, 1], 2, 2, 8)
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.7)
+    np.testing.assert_array_equal(o, v)
+    np.testing.assert_allclose(lse, 0.7 * np.einsum("thd,thd->ht", q, k), atol=1e-14)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.7)
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_array_equal(dv, do)
+
+
+def test_equal_values_rows():
+    # All V rows equal c: O = c whatever P is, so dQ = dK = 0 and sum_j dV_j = sum_i dO_i.
+    rng = np.random.default_rng(7)
+    offs, q, k, v, do = _problem(rng, [6, 4], 2, 2, 4)
+    c = rng.standard_normal(4)
+    v[:] = c
+    o, _, _ = oracle.attn_fwd(q, k, v, offs, scale=0.5)
+    np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), atol=1e-14)
+    for causal in (False, True):
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.5, causal=causal)
+        np.testing.assert_allclose(dq, 0, atol=1e-13)
+        np.testing.assert_allclose(dk, 0, atol=1e-13)
+        for a, e in zip(offs[:-1], offs[1:]):
+            np.testing.assert_allclose(dv[a:e].sum(axis=0), do[a:e].sum(axis=0), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_gradients_sum_to_zero(causal):
+    # Shifting every key of a sequence by the same vector leaves the softmax
+    # unchanged, so the key gradients of each (sequence, kv head) sum to zero.
+    rng = np.random.default_rng(8)
+    offs, q, k, v, do = _problem(rng, [5, 9, 2], 4, 2, 8)
+    _, dk, _, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.4, causal=causal)
+    for a, e in zip(offs[:-1], offs[1:]):
+        np.testing.assert_allclose(dk[a:e].sum(axis=0), 0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- structure
+def test_packed_equals_pieces():
+    rng = np.random.default_rng(9)
+    lengths = [3, 8, 5]
+    offs, q, k, v, do = _problem(rng, lengths, 2, 1, 8)
+    for causal in (False, True):
+        o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.3, causal=causal)
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.3, causal=causal)
+        for a, e in zip(offs[:-1], offs[1:]):
+            one = np.array([0, e - a], dtype=np.int32)
+            o1, l1, _ = oracle.attn_fwd(q[a:e], k[a:e], v[a:e], one, scale=0.3, causal=causal)
+            g1 = oracle.attn_bwd(q[a:e], k[a:e], v[a:e], do[a:e], one, scale=0.3, causal=causal)
+            np.testing.assert_array_equal(o[a:e], o1)
+            np.testing.assert_array_equal(lse[:, a:e], l1)
+            for full, piece in zip((dq, dk, dv), g1[:3]):
+                np.testing.assert_array_equal(full[a:e], piece)
+
+
+def test_broadcast_dq_is_sum_over_sequences():
+    rng = np.random.default_rng(10)
+    lengths = [6, 0, 3, 11]
+    nq = 4
+    offs, q, k, v, do = _problem(rng, lengths, 2, 2, 8, nq=nq)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.35, nq=nq)
+    dq_sum = np.zeros_like(dq)
+    for b, (a, e) in enumerate(zip(offs[:-1], offs[1:])):
+        one = np.array([0, e - a], dtype=np.int32)
+        g = oracle.attn_bwd(q, k[a:e], v[a:e], do[b * nq:(b + 1) * nq], one, scale=0.35, nq=nq)
+        dq_sum += g[0]
+        np.testing.assert_allclose(dk[a:e], g[1], atol=1e-14)
+        np.testing.assert_allclose(dv[a:e], g[2], atol=1e-14)
+    np.testing.assert_allclose(dq, dq_sum, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("lengths", [[64, 128, 192], [130, 64, 7]])
+def test_block_mode_equals_jagged_over_blocks(lengths):
+    rng = np.random.default_rng(12)
+    offs, q, k, v, do = _problem(rng, lengths, 2, 2, 4)
+    pieces = []
+    for L in lengths:
+        pieces += [64] * (L // 64) + ([L % 64] if L % 64 else [])
+    offs64 = offsets_from_lengths(pieces)
+    o_b, _ = oracle.block_fwd(q, k, v, offs, scale=0.5)
+    o_j, _, _ = oracle.attn_fwd(q, k, v, offs64, scale=0.5)
+    np.testing.assert_array_equal(o_b, o_j)
+    g_b = oracle.block_bwd(q, k, v, do, offs, scale=0.5)
+    g_j = oracle.attn_bwd(q, k, v, do, offs64, scale=0.5)
+    for a, b in zip(g_b[:3], g_j[:3]):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    # and against the textbook form over the same pieces
+    o_ref, _ = packed_dense(q, k, v, offs64, 0.5)
+    np.testing.assert_allclose(o_b, o_ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- finite differences
+def _loss(fwd, x_name, x, base, h_idx, eps, dout):
+    args = dict(base)
+    xp = x.copy()
+    xp[h_idx] += eps
+    args[x_name] = xp
+    op = fwd(**args)
+    xm = x.copy()
+    xm[h_idx] -= eps
+    args[x_name] = xm
+    om = fwd(**args)
+    return float(np.sum((op - om) * dout)) / (2 * eps)
+
+
+def _check_fd(fwd, bwd_grads, base, dout, rng, n_probe=12, eps=1e-5):
+    for name, g in zip(("q", "k", "v"), bwd_grads):
+        x = base[name]
+        for _ in range(n_probe):
+            idx = tuple(int(rng.integers(0, s)) for s in x.shape)
+            fd = _loss(fwd, name, x, base, idx, eps, dout)
+            assert abs(fd - g[idx]) <= 1e-7 + 1e-6 * abs(fd), (name, idx, fd, g[idx])
+
+
+@pytest.mark.parametrize("causal,H,Hkv", [(False, 2, 2), (True, 2, 2), (False, 4, 2), (True, 4, 1)])
+def test_gradients_finite_differences(causal, H, Hkv):
+    rng = np.random.default_rng(20 + H + Hkv + int(causal))
+    offs, q, k, v, do = _problem(rng, [4, 7, 1], H, Hkv, 4)
+    scale = 0.6
+
+    def fwd(q, k, v):
+        return oracle.attn_fwd(q, k, v, offs, scale=scale, causal=causal)[0]
+
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=scale, causal=causal)
+    _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng)
+
+
+def test_broadcast_gradients_finite_differences():
+    rng = np.random.default_rng(30)
+    nq = 3
+    offs, q, k, v, do = _problem(rng, [4, 2, 5], 2, 2, 4, nq=nq)
+
+    def fwd(q, k, v):
+        return oracle.attn_fwd(q, k, v, offs, scale=0.5, nq=nq)[0]
+
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.5, nq=nq)
+    _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng)
+
+
+def test_block_gradients_finite_differences():
+    rng = np.random.default_rng(31)
+    offs, q, k, v, do = _problem(rng, [70, 5], 1, 1, 4)
+
+    def fwd(q, k, v):
+        return oracle.block_fwd(q, k, v, offs, scale=0.5)[0]
+
+    dq, dk, dv, _ = oracle.block_bwd(q, k, v, do, offs, scale=0.5)
+    _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng, n_probe=20)
+
+
+def test_unit_selection_and_threads():
+    rng = np.random.default_rng(40)
+    offs, q, k, v, do = _problem(rng, [9, 4, 12], 2, 2, 8)
+    sel = np.zeros((3, 2), dtype=bool)
+    sel[1, 0] = sel[2, 1] = True
+    o_all, lse_all, _ = oracle.attn_fwd(q, k, v, offs, scale=0.4, nthreads=1)
+    o_sel, lse_sel, _ = oracle.attn_fwd(q, k, v, offs, scale=0.4, sel=sel, nthreads=3)
+    for b in range(3):
+        a, e = offs[b], offs[b + 1]
+        for h in range(2):
+            if sel[b, h]:
+                np.testing.assert_array_equal(o_sel[a:e, h], o_all[a:e, h])
+            else:
+                assert np.all(np.isnan(o_sel[a:e, h]))
