@@ -1,0 +1,177 @@
+/*
+ * jfa.h -- C ABI of libjfa: Jagged Flash Attention on GB300 (sm_103a).
+ *
+ * Exact attention O = softmax(scale * Q K^T) V, forward and backward, computed
+ * directly on packed variable-length sequences.  Sources (four web pages on the
+ * subject):
+ *   [C]  "Optimizing Jagged Flash Attention with TLX" (commentary page):
+ *        sections "why unequal lengths change the problem", "architecture",
+ *        "load balancing", "performance and feature scope".
+ *   [N]  n1n.ai page on JFA with TLX: the padded-tensor cost and the jagged
+ *        layout example (offsets [0, 128, 4224, 4736, 6784]).
+ *   [B]  "TLX Block Attention" (translation of the PyTorch blog): sections 2.1
+ *        (the fixed-block simplifications), 3 (warp-specialised pipeline),
+ *        4 (backward without a log-sum-exp tensor), 5 (variable-length scheduling).
+ *   [R]  aixai.ru summary of the JFA-TLX work: "What is JFA", "Framework",
+ *        "Tile balancing and Cluster Launch Control", "dQ epilogue",
+ *        "Loop peeling", "Paired CTAs".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Packed ("jagged") layout [C, N]: the tokens of all sequences are stored
+ *    back to back; offsets[b] .. offsets[b+1]-1 are the rows of sequence b,
+ *    offsets[0] = 0, offsets has batch+1 int32 entries.
+ *  - Tensors are contiguous row-major [rows, heads, head_dim] bf16: element
+ *    (t, h, d) is at t*heads*head_dim + h*head_dim + d.  K and V (and dK, dV)
+ *    have num_kv_heads heads; query head h reads key/value head
+ *    h / (num_heads / num_kv_heads).
+ *  - Self-attention (broadcast_q == 0): q, o, dO, dq have offsets[batch] rows.
+ *  - Broadcast-Q (broadcast_q != 0) [C "unequal lengths"; R "What is JFA"]:
+ *    q and dq have nq_broadcast rows shared by every sequence; o and dO have
+ *    batch * nq_broadcast rows (sequence-major: rows b*nq .. b*nq+nq-1 belong to
+ *    sequence b); dq is the sum over all sequences.
+ *  - lse is fp32 [num_heads, rows of o]: the natural-log log-sum-exp of each
+ *    score row, L = m + log(l) [B 2.1, Listing 1].  An empty sequence in
+ *    broadcast mode yields o rows of 0 and lse = -inf.
+ *  - Causal masking (key j visible to query i iff j <= i inside a sequence) is
+ *    supported for self-attention only.
+ *  - head_dim must be 64 or 128 (the pages allow up to 128 [C "feature scope"];
+ *    this library builds those two).  GQA is forward-only: the backward needs
+ *    num_kv_heads == num_heads [C "feature scope"].
+ *  - offsets_dev is the device copy of the offsets; offsets_host the host copy,
+ *    from which all scheduling is planned on the CPU with no device sync
+ *    [B 5].  Both must hold the same values; only offsets_host is validated.
+ *  - Ownership: the caller owns every buffer, including `workspace` (device
+ *    memory of at least jfa_workspace_size() bytes, any contents).  The library
+ *    allocates no device memory and keeps no state across calls except cached
+ *    device properties and kernel attributes.
+ *  - Streams: all device work is enqueued on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  Calls return once the work is enqueued.
+ *    The host-side offsets are read before the call returns.
+ *  - Errors: every call returns a jfa_status; nothing is thrown across the ABI.
+ *    Argument errors are detected before any work is enqueued.  A kernel whose
+ *    internal wait times out records JFA_ERR_DEVICE_TIMEOUT in the workspace,
+ *    which jfa_device_status() reports.
+ */
+#ifndef JFA_H_
+#define JFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned pointer */
+  JFA_ERR_UNSUPPORTED = 2,          /* head_dim not 64/128, GQA backward, causal+broadcast,
+                                       num_heads % num_kv_heads != 0 */
+  JFA_ERR_BAD_OFFSETS = 3,          /* offsets[0] != 0, decreasing, or a length > max_len */
+  JFA_ERR_WORKSPACE_TOO_SMALL = 4,
+  JFA_ERR_ARCH = 5,                 /* current device is not compute capability 10.x */
+  JFA_ERR_CUDA = 6,                 /* a CUDA runtime call or launch failed */
+  JFA_ERR_DEVICE_TIMEOUT = 7        /* a kernel wait ran out (see jfa_device_status) */
+} jfa_status;
+
+typedef enum { JFA_OP_FWD = 0, JFA_OP_BWD = 1, JFA_OP_BLOCK_FWD = 2, JFA_OP_BLOCK_BWD = 3 } jfa_op;
+
+/*
+ * jfa_fwd -- jagged flash-attention forward [C "architecture"; R "Framework";
+ * B 2.1 Listing 1 for the online-softmax recurrence; N for the layout].
+ *   o   = softmax(scale * q k^T) v per sequence and head (bf16 out),
+ *   lse = log-sum-exp per row (fp32, may be NULL to skip writing it).
+ * Work is planned on the host: 256-row query units sorted by K/V length and
+ * dealt to one persistent CTA per SM in snake (zigzag) order [R "Tile
+ * balancing"].
+ */
+int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+            const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
+            int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/*
+ * jfa_bwd -- jagged flash-attention backward [B 4 for the gradient algebra;
+ * R "Paired CTAs" (five GEMMs per K/V block), "dQ epilogue"; C "load balancing"].
+ * Inputs are the forward's q, k, v, o, lse and the output gradient dO; outputs
+ * dq (bf16, like q), dk and dv (bf16, like k):
+ *   P = exp(scale q k^T - lse), dV = P^T dO, dP = dO V^T, Di = rowsum(dO o O),
+ *   dS = P o (dP - Di), dQ = scale dS K, dK = scale dS^T Q.
+ * Requires num_kv_heads == num_heads.  In broadcast-Q mode dq is summed over all
+ * sequences.  Valid 128-key blocks are dealt round-robin to the CTAs.
+ */
+int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+            int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale, int causal,
+            int broadcast_q, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * block_attn_fwd -- fixed 64-token block-diagonal self-attention [B 1, 2.1, 3].
+ * Each sequence is cut into blocks of 64 tokens (the last one may be shorter)
+ * and every block attends only within itself: one score GEMM and one PV GEMM per
+ * block, no running-max correction, no log-sum-exp output.  num_kv_heads is
+ * num_heads.  Programs get balanced contiguous ranges of (block pair, head)
+ * tiles computed on the host in closed form [B 5].
+ */
+int block_attn_fwd(const void* q, const void* k, const void* v, void* o, const int32_t* offsets_dev,
+                   const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * block_attn_bwd -- backward of block_attn_fwd [B 4]: P is recomputed from q and
+ * k (no log-sum-exp tensor), Di is formed inline, and each block owns its own
+ * dq, dk, dv rows, so no atomics are needed.  `o` is accepted for interface
+ * symmetry; the kernel forms Di = rowsum(P o dP), which equals rowsum(dO o O).
+ */
+int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,
+                   void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                   int max_len, int num_heads, int head_dim, float scale, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * jfa_workspace_size -- device workspace in bytes that `op` needs for this
+ * problem (plans, per-row Di, the fp32 dQ accumulator, an error word).
+ * Returns 0 on invalid arguments.  Queries the current device's SM count.
+ */
+size_t jfa_workspace_size(int op, const int32_t* offsets_host, int batch, int nq_broadcast, int num_heads,
+                          int head_dim, int causal, int broadcast_q);
+
+/* Human-readable name of a jfa_status value (static string). */
+const char* jfa_status_string(int status);
+
+/*
+ * jfa_device_status -- synchronises `stream` and returns JFA_OK or the error a
+ * kernel recorded in `workspace` since the last call that used it.
+ */
+int jfa_device_status(const void* workspace, void* stream);
+
+/*
+ * Host planners, exported so tests can compare them bit for bit with a naive
+ * restatement [R "Tile balancing and Cluster Launch Control"; B 5].
+ * Entries are int32 quadruples (b, h, tile, cost), CTA-major, with cta_start
+ * [n_cta+1] giving each CTA's slice.  Pass NULL buffers to only count.
+ * Return the number of units (>= 0) or -jfa_status.
+ *
+ *   jfa_plan_fwd: unit = 256 query rows (b, h, m); cost = 128-key blocks
+ *     visited; stable sort by cost descending; snake deal over n_cta.
+ *   jfa_plan_bwd: unit = one valid 128-key block (b, h, n), enumerated b, h, n
+ *     (n innermost), dealt round-robin; cost = 128-row query tiles visited.
+ */
+int jfa_plan_fwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal, int n_cta,
+                 int32_t* units, int32_t* cta_start);
+int jfa_plan_bwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal, int n_cta,
+                 int32_t* units, int32_t* cta_start);
+/*
+ *   block_plan: block_per_batch [batch+1] = exclusive prefix sum of ceil(L/64);
+ *     tiles are pairs of consecutive global blocks per head (id = pair*H + h);
+ *     prog_start [P+1] with P = min(n_sm, tiles) from closed-form divmod.
+ *     Either buffer may be NULL.  Returns P (>= 0) or -jfa_status.
+ */
+int block_plan(const int32_t* offsets_host, int batch, int num_heads, int n_sm, int32_t* block_per_batch,
+               int32_t* prog_start);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JFA_H_ */

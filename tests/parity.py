@@ -1,0 +1,84 @@
+"""Helpers shared by the GPU parity tests: run a workload through the CUDA
+library and the fp64 oracle on the same seeded bf16 inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import variable_length_attention_gb300 as V
+
+# Tolerances (bf16 inputs, fp32 accumulation, bf16 outputs):
+O_MAX_ABS = 1e-2       # output, max |gpu - oracle|
+O_REL_L2 = 5e-3        # output, ||gpu - oracle|| / ||oracle||
+LSE_MAX_ABS = 2e-3     # log-sum-exp, max abs
+GRAD_REL_L2 = 2e-2     # dQ, dK, dV relative L2
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b.ravel())
+    return float(np.linalg.norm((a - b).ravel()) / (den if den > 0 else 1.0))
+
+
+def to64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def sample_units(batch, H, n, seed=0):
+    """A [batch, H] selection of about n (sequence, head) units, always including
+    the longest and the shortest sequences' units of head 0."""
+    rng = np.random.default_rng(seed)
+    sel = np.zeros((batch, H), dtype=bool)
+    flat = rng.choice(batch * H, size=min(n, batch * H), replace=False)
+    sel.reshape(-1)[flat] = True
+    return sel
+
+
+def rows_of(offsets, sel, H, nq=0):
+    """Boolean [rows, H] mask of output rows covered by a unit selection."""
+    B = len(offsets) - 1
+    rows = B * nq if nq else int(offsets[-1])
+    mask = np.zeros((rows, H), dtype=bool)
+    for b in range(B):
+        a, e = (b * nq, (b + 1) * nq) if nq else (int(offsets[b]), int(offsets[b + 1]))
+        mask[a:e] = sel[b][None, :]
+    return mask
+
+
+def gpu_inputs(w, device="cuda"):
+    q, k, v, do = w.tensors("cpu")
+    offs = torch.from_numpy(w.offsets).to(device)
+    return [t.to(device) for t in (q, k, v, do)], offs, (q, k, v, do)
+
+
+def check_fwd(w, sel=None, nthreads=0):
+    """Runs jfa_fwd and compares O and LSE with the oracle.  Returns a dict of errors."""
+    (q, k, v, do), offs, cpu = gpu_inputs(w)
+    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref, _ = oracle.attn_fwd(to64(cpu[0]), to64(cpu[1]), to64(cpu[2]), w.offsets, scale=w.scale,
+                                        causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads)
+    o_g, lse_g = to64(o), to64(lse)
+    if sel is not None:
+        m = rows_of(w.offsets, sel, w.num_heads, w.nq)
+        o_g, o_ref = o_g[m], o_ref[m]
+        lse_g, lse_ref = lse_g.T[m], lse_ref.T[m]
+    fin = np.isfinite(lse_ref)
+    res = {
+        "o_max_abs": float(np.max(np.abs(o_g - o_ref))) if o_g.size else 0.0,
+        "o_rel_l2": rel_l2(o_g, o_ref),
+        "lse_max_abs": float(np.max(np.abs(lse_g[fin] - lse_ref[fin]))) if fin.any() else 0.0,
+        "lse_inf_match": bool(np.all(np.isneginf(lse_g[~fin]))) if (~fin).any() else True,
+        "finite": bool(np.all(np.isfinite(o_g))),
+    }
+    return res, (o, lse)
+
+
+def assert_fwd_ok(res):
+    assert res["finite"], res
+    assert res["o_max_abs"] <= O_MAX_ABS, res
+    assert res["o_rel_l2"] <= O_REL_L2, res
+    assert res["lse_max_abs"] <= LSE_MAX_ABS, res
+    assert res["lse_inf_match"], res

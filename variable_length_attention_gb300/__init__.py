@@ -1,0 +1,8 @@
+"""Jagged Flash Attention for GB300 (sm_103a).
+
+The compute path is libjfa.so (hand-written CUDA; C ABI in include/jfa.h);
+``jfa`` is its thin ctypes binding and ``workloads`` draws seeded inputs.
+"""
+from . import workloads  # noqa: F401
+from .jfa import (block_attn_bwd, block_attn_fwd, block_plan, jfa_bwd, jfa_device_status, jfa_fwd,  # noqa: F401
+                  jfa_plan_bwd, jfa_plan_fwd, jfa_status_string, jfa_workspace_size)

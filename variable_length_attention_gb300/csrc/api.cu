@@ -1,0 +1,301 @@
+// api.cu -- the C ABI of libjfa: argument validation, host planning, workspace
+// layout and kernel launches.  The public contract is in include/jfa.h.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/jfa.h"
+#include "host.h"
+#include "plan.h"
+
+namespace jfa {
+
+// ---------------------------------------------------------------- device info
+int current_device(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return JFA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  DeviceInfo& d = cache[dev];
+  if (d.device != dev) {
+    DeviceInfo n;
+    n.device = dev;
+    if (cudaDeviceGetAttribute(&n.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return JFA_ERR_CUDA;
+    d = n;
+  }
+  *out = d;
+  return (d.cc_major == 10) ? JFA_OK : JFA_ERR_ARCH;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return JFA_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_INVALID_ARG;
+}
+
+// ---------------------------------------------------------------- pinned staging
+// Plans are built on the host every call.  They reach the device through a small
+// ring of pinned host buffers so the copy never forces a host-device sync; each
+// slot is reused only after the event recorded behind its previous copy has fired.
+namespace {
+struct Slot {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+  int device = -1;
+};
+constexpr int kSlots = 8;
+std::mutex g_stage_mu;
+Slot g_slots[kSlots];
+int g_next_slot = 0;
+}  // namespace
+
+static int stage_to_device(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (bytes == 0) return JFA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_stage_mu);
+  Slot& s = g_slots[g_next_slot];
+  g_next_slot = (g_next_slot + 1) % kSlots;
+  if (s.done != nullptr && cudaEventSynchronize(s.done) != cudaSuccess) return JFA_ERR_CUDA;
+  if (s.done != nullptr && s.device != dev) {
+    cudaEventDestroy(s.done);
+    s.done = nullptr;
+  }
+  if (s.cap < bytes) {
+    if (s.host) cudaFreeHost(s.host);
+    s.host = nullptr;
+    s.cap = 0;
+    size_t cap = 1 << 16;
+    while (cap < bytes) cap *= 2;
+    if (cudaHostAlloc(&s.host, cap, cudaHostAllocPortable) != cudaSuccess) return JFA_ERR_CUDA;
+    s.cap = cap;
+  }
+  if (s.done == nullptr) {
+    if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) return JFA_ERR_CUDA;
+    s.device = dev;
+  }
+  std::memcpy(s.host, src, bytes);
+  if (cudaMemcpyAsync(dst, s.host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (cudaEventRecord(s.done, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  return JFA_OK;
+}
+
+// ---------------------------------------------------------------- workspace layout
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct FwdLayout {
+  size_t err = 0, units = 0, cta = 0, empty = 0, total = 0;
+};
+static FwdLayout fwd_layout(int n_units, int n_cta, int batch) {
+  FwdLayout l;
+  l.err = 0;
+  l.units = 256;
+  l.cta = l.units + align256(static_cast<size_t>(n_units) * 16);
+  l.empty = l.cta + align256(static_cast<size_t>(n_cta + 1) * 4);
+  l.total = l.empty + align256(static_cast<size_t>(batch) * 4);
+  return l;
+}
+
+__global__ void fill_empty_broadcast_kernel(const int32_t* empty_seq, int n_empty, int nq, int H, int D,
+                                            int o_rows, __nv_bfloat16* o, float* lse) {
+  // one block row per (empty sequence, query row); threads over H*D
+  const int r = blockIdx.x;
+  if (r >= n_empty * nq) return;
+  const int b = empty_seq[r / nq];
+  const int row = b * nq + r % nq;
+  for (int i = threadIdx.x; i < H * D; i += blockDim.x) o[static_cast<size_t>(row) * H * D + i] = __float2bfloat16(0.f);
+  if (lse)
+    for (int h = threadIdx.x; h < H; h += blockDim.x) lse[static_cast<size_t>(h) * o_rows + row] = -INFINITY;
+}
+
+struct Common {
+  DeviceInfo dev;
+  int q_rows = 0, kv_rows = 0, o_rows = 0;
+};
+
+static int validate_common(const void* q, const void* k, const void* v, const void* o, const int32_t* offsets_dev,
+                           const int32_t* offsets_host, int batch, int max_len, int nq, int H, int Hkv, int D,
+                           float scale, int causal, int broadcast_q, Common* c) {
+  if (batch < 0 || H <= 0 || Hkv <= 0 || max_len < 0) return JFA_ERR_INVALID_ARG;
+  if (offsets_host == nullptr || offsets_dev == nullptr) return JFA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+  if (H % Hkv != 0) return JFA_ERR_UNSUPPORTED;
+  if (broadcast_q && causal) return JFA_ERR_UNSUPPORTED;
+  if (broadcast_q && nq <= 0) return JFA_ERR_INVALID_ARG;
+  const int st = check_offsets(offsets_host, batch, max_len);
+  if (st != JFA_OK) return st;
+  c->kv_rows = offsets_host[batch];
+  c->q_rows = broadcast_q ? nq : c->kv_rows;
+  c->o_rows = broadcast_q ? batch * nq : c->kv_rows;
+  if (c->o_rows > 0 && (q == nullptr || o == nullptr)) return JFA_ERR_INVALID_ARG;
+  if (c->kv_rows > 0 && (k == nullptr || v == nullptr)) return JFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JFA_ERR_INVALID_ARG;
+  return current_device(&c->dev);
+}
+
+static int plan_ctas(const DeviceInfo& dev, int n_units) { return n_units < dev.num_sms ? n_units : dev.num_sms; }
+
+}  // namespace jfa
+
+using namespace jfa;
+
+extern "C" const char* jfa_status_string(int status) {
+  switch (status) {
+    case JFA_OK: return "ok";
+    case JFA_ERR_INVALID_ARG: return "invalid argument";
+    case JFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case JFA_ERR_BAD_OFFSETS: return "bad offsets";
+    case JFA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case JFA_ERR_ARCH: return "device is not compute capability 10.x";
+    case JFA_ERR_CUDA: return "CUDA error";
+    case JFA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int batch, int nq_broadcast, int num_heads,
+                                     int head_dim, int causal, int broadcast_q) {
+  if (offsets_host == nullptr || batch < 0 || num_heads <= 0) return 0;
+  if (check_offsets(offsets_host, batch, -1) != JFA_OK) return 0;
+  DeviceInfo dev;
+  if (current_device(&dev) != JFA_OK) return 0;
+  const int nq = broadcast_q ? nq_broadcast : 0;
+  if (op == JFA_OP_FWD) {
+    const int n = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+    return fwd_layout(n, plan_ctas(dev, n), batch).total;
+  }
+  (void)head_dim;
+  return 0;
+}
+
+extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+                       const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
+                       int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* workspace,
+                       size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Common c;
+  const int nq = broadcast_q ? nq_broadcast : 0;
+  int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
+                           head_dim, scale, causal, broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  if (workspace == nullptr && workspace_bytes > 0) return JFA_ERR_INVALID_ARG;
+
+  std::vector<int32_t> units, cta_start;
+  const int n_probe = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+  const int n_cta = plan_ctas(c.dev, n_probe);
+  int n = 0;
+  if (n_cta > 0) n = plan_fwd(offsets_host, batch, num_heads, nq, causal, n_cta, &units, &cta_start);
+  std::vector<int32_t> empty;
+  if (broadcast_q)
+    for (int b = 0; b < batch; ++b)
+      if (offsets_host[b + 1] == offsets_host[b]) empty.push_back(b);
+  const FwdLayout lay = fwd_layout(n, n_cta, batch);
+  if (workspace_bytes < lay.total || workspace == nullptr) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
+
+  if (!empty.empty()) {
+    // one staging copy for the list of empty sequences, then a fill kernel
+    st = stage_to_device(ws + lay.empty, empty.data(), empty.size() * 4, stream);
+    if (st != JFA_OK) return st;
+    const int blocks = static_cast<int>(empty.size()) * nq;
+    fill_empty_broadcast_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const int32_t*>(ws + lay.empty),
+                                                             static_cast<int>(empty.size()), nq, num_heads,
+                                                             head_dim, c.o_rows, static_cast<__nv_bfloat16*>(o), lse);
+    if (cudaGetLastError() != cudaSuccess) return JFA_ERR_CUDA;
+  }
+  if (n == 0) return JFA_OK;
+  // units and CTA starts travel in one copy (they are adjacent in the workspace)
+  std::vector<uint8_t> blob(lay.empty - lay.units, 0);
+  std::memcpy(blob.data(), units.data(), units.size() * 4);
+  std::memcpy(blob.data() + (lay.cta - lay.units), cta_start.data(), cta_start.size() * 4);
+  st = stage_to_device(ws + lay.units, blob.data(), blob.size(), stream);
+  if (st != JFA_OK) return st;
+
+  FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.offsets_dev = offsets_dev;
+  a.q_rows = c.q_rows;
+  a.kv_rows = c.kv_rows;
+  a.o_rows = c.o_rows;
+  a.H = num_heads;
+  a.Hkv = num_kv_heads;
+  a.D = head_dim;
+  a.nq = nq;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
+  a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
+  a.n_cta = n_cta;
+  a.err = reinterpret_cast<int*>(ws + lay.err);
+  a.stream = stream;
+  return launch_fwd(a);
+}
+
+extern "C" int jfa_bwd(const void*, const void*, const void*, const void*, const void*, const float*, void*, void*,
+                       void*, const int32_t*, const int32_t*, int, int, int, int, int, int, float, int, int, void*,
+                       size_t, void*) {
+  return JFA_ERR_UNSUPPORTED;
+}
+
+extern "C" int block_attn_fwd(const void*, const void*, const void*, void*, const int32_t*, const int32_t*, int, int,
+                              int, int, float, void*, size_t, void*) {
+  return JFA_ERR_UNSUPPORTED;
+}
+
+extern "C" int block_attn_bwd(const void*, const void*, const void*, const void*, const void*, void*, void*, void*,
+                              const int32_t*, const int32_t*, int, int, int, int, float, void*, size_t, void*) {
+  return JFA_ERR_UNSUPPORTED;
+}
+
+extern "C" int jfa_device_status(const void* workspace, void* stream) {
+  if (workspace == nullptr) return JFA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return JFA_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+  return err == 0 ? JFA_OK : JFA_ERR_DEVICE_TIMEOUT;
+}

@@ -1,0 +1,471 @@
+// fwd.cu -- jagged flash-attention forward for sm_103a.
+//
+// What it computes: for every packed sequence and head, O = softmax(scale Q K^T) V
+// and the natural-log log-sum-exp of each score row, with the online-softmax
+// recurrence of the standard flash-attention loop ("TLX Block Attention",
+// section 2.1, Listing 1): a running row maximum m and sum l, a correction
+// factor when m grows, O = acc / l at the end, L = m + log(l) stored for the
+// backward pass.
+//
+// How (one persistent CTA per SM, warp-specialised; the role split follows the
+// aixai.ru summary, "Framework", and the commentary page, "architecture"):
+//   warps 0-3   softmax of query tile 0 (one thread per row = one TMEM lane)
+//   warps 4-7   softmax of query tile 1
+//   warps 8-11  epilogue: O / l -> bf16 -> global, log-sum-exp
+//   warp 12     tcgen05 MMA issuer (one thread)
+//   warp 13     TMA loader (one thread): Q tiles, then a K/V ring in shared memory
+// A work unit is 256 query rows (two 128-row tiles) of one (sequence, head); both
+// tiles share every K/V block the loader brings in.  The MMA warp interleaves
+// the two tiles so the tensor core computes one tile's S = Q K^T while the
+// other tile's softmax runs:  S0 S1 | PV0 S0' PV1 S1' | PV0 S0'' ...
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D);
+// P (bf16, two per column) overwrites the first 64 columns of its S.
+// The running maximum is only moved (and O rescaled) when it grows by more than
+// 2^8; otherwise the stale maximum is kept, which is exact because numerator and
+// denominator share it.
+// Keys past the end of a sequence and, for causal attention, keys past the
+// query row are masked in separate, peeled iterations so the main loop has no
+// mask (aixai.ru summary, "Loop peeling against register spills").
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "host.h"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace fwd {
+
+constexpr int BM = 128;  // rows per query tile
+constexpr int BN = 128;  // keys per K/V block
+constexpr int kThreads = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int NCHUNK = D / 64;                  // 128-byte swizzle atoms across head_dim
+  static constexpr int TILE_BYTES = BM * D * 2;          // one Q tile or one K/V block
+  static constexpr int CHUNK_BYTES = BM * 128;           // one 64-column box
+  static constexpr int NSTAGE = D == 128 ? 4 : 6;        // K/V ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NSTAGE * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 4096;      // barriers, stats, TMEM address
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;   // slack for 1024-byte alignment
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* offsets;
+  const int4* units;
+  const int32_t* cta_start;
+  int* err;
+  int H, Hkv, nq, o_rows;
+  float scale_log2;
+};
+
+struct Unit {
+  int b, h, g, m;
+  int kv0, L;       // first K/V row, K/V length
+  int rows;         // query rows of the sequence (self) or of the shared Q (broadcast)
+  int q_row0;       // first query row of the unit in q
+  int o_row0;       // first output row of the unit in o
+  int n_kv;         // K/V blocks visited
+  int n_plain;      // leading blocks that need no mask
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode(const Params& p, int idx) {
+  const int4 e = p.units[idx];
+  Unit u;
+  u.b = e.x;
+  u.h = e.y;
+  u.m = e.z;
+  u.g = u.h / (p.H / p.Hkv);
+  u.kv0 = p.offsets[u.b];
+  u.L = p.offsets[u.b + 1] - u.kv0;
+  if (p.nq > 0) {
+    u.rows = p.nq;
+    u.q_row0 = 2 * BM * u.m;
+    u.o_row0 = u.b * p.nq + 2 * BM * u.m;
+  } else {
+    u.rows = u.L;
+    u.q_row0 = u.kv0 + 2 * BM * u.m;
+    u.o_row0 = u.q_row0;
+  }
+  if (CAUSAL) {
+    const int last = min(2 * BM * (u.m + 1), u.rows);
+    u.n_kv = (min(last, u.L) + BN - 1) / BN;
+    u.n_plain = min(u.L / BN, 2 * u.m);
+  } else {
+    u.n_kv = (u.L + BN - 1) / BN;
+    u.n_plain = u.L / BN;
+  }
+  return u;
+}
+
+struct Bars {
+  uint64_t q_full[2];
+  uint64_t q_empty;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t o_empty[2];
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t drain;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  float stat_m[2][BM];
+  float stat_l[2][BM];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sKV = smem + C::OFF_KV;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  static_assert(sizeof(Bars) <= 4096, "barrier block too large");
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int u_begin = p.cta_start[blockIdx.x];
+  const int u_end = p.cta_start[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], BM);
+      mbar_init(&bars->st_full[t], BM);
+      mbar_init(&bars->st_empty[t], BM);
+    }
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->drain, 1);
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Abort ab{&bars->abort_flag, p.err};
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    setmaxnreg_inc<176>();
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = threadIdx.x & 127;       // TMEM lane == row of the tile
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + t * BN;
+    const uint32_t tO = tmem + lane_addr + 256 + t * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t s_phase = 0, st_phase = 0;
+    for (int ui = u_begin; ui < u_end; ++ui) {
+      const Unit u = decode<CAUSAL>(p, ui);
+      const int qi = 2 * BM * u.m + BM * t + row;  // query index inside the sequence / shared Q
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < u.n_kv; ++j) {
+        if (!mbar_wait(&bars->s_full[t], s_phase, ab)) goto done;
+        s_phase ^= 1;
+        tc_fence_after();
+        uint32_t sr[BN];
+        tmem_ld32(tS + 0, sr + 0);
+        tmem_ld32(tS + 32, sr + 32);
+        tmem_ld32(tS + 64, sr + 64);
+        tmem_ld32(tS + 96, sr + 96);
+        tmem_wait_ld();
+        reg_fence<BN>(sr);
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
+        if (j >= u.n_plain) {  // peeled tail / diagonal iterations
+          int limit = u.L - j * BN;
+          if (CAUSAL) limit = min(limit, qi - j * BN + 1);
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= limit) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m_run, mx * sl2);
+        if (m_new > m_run + kRescaleThreshold) {
+          if (j > 0) {
+            const float alpha = ex2(m_run - m_new);
+            l_run *= alpha;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c, ov);
+              tmem_wait_ld();
+              reg_fence<32>(ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c, ov);
+            }
+          }
+          m_run = m_new;
+        }
+        float sum = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float p0 = ex2(fmaf(s[c], sl2, -m_run));
+          const float p1 = ex2(fmaf(s[c + 1], sl2, -m_run));
+          sum += p0 + p1;
+          pk[c / 2] = pack_bf16(p0, p1);
+        }
+        l_run += sum;
+        tmem_st32(tS + 0, pk);
+        tmem_st32(tS + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[t]);
+      }
+      // hand the row statistics to the epilogue
+      if (!mbar_wait(&bars->st_empty[t], st_phase ^ 1, ab)) goto done;
+      st_phase ^= 1;
+      bars->stat_m[t][row] = m_run;
+      bars->stat_l[t][row] = l_run;
+      mbar_arrive(&bars->st_full[t]);
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ epilogue
+    setmaxnreg_dec<64>();
+    const int row = threadIdx.x & 127;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t phase = 0;
+    for (int ui = u_begin; ui < u_end; ++ui) {
+      const Unit u = decode<CAUSAL>(p, ui);
+      for (int t = 0; t < 2; ++t) {
+        if (!mbar_wait(&bars->o_full[t], phase, ab)) goto done;
+        if (!mbar_wait(&bars->st_full[t], phase, ab)) goto done;
+        tc_fence_after();
+        const float m_fin = bars->stat_m[t][row];
+        const float l_fin = bars->stat_l[t][row];
+        mbar_arrive(&bars->st_empty[t]);
+        const int qi = 2 * BM * u.m + BM * t + row;
+        const bool valid = qi < u.rows;
+        const int orow = u.o_row0 + BM * t + row;
+        const float inv_l = 1.0f / l_fin;
+        __nv_bfloat16* dst = p.o + (static_cast<size_t>(orow) * p.H + u.h) * D;
+        const uint32_t tO = tmem + lane_addr + 256 + t * 128;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_wait_ld();
+          reg_fence<32>(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              st_global_v4(dst + c + 8 * i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty[t]);
+        if (valid && p.lse != nullptr)
+          p.lse[static_cast<size_t>(u.h) * p.o_rows + orow] = (m_fin + log2f(l_fin)) * 0.69314718055994531f;
+      }
+      phase ^= 1;
+    }
+  } else {
+    setmaxnreg_dec<96>();
+    if (warp == 12 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idesc_o = idesc_bf16(BM, D, 0, 1);
+      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
+      uint32_t kv_it = 0, u_phase = 0;
+      uint32_t p_phase[2] = {0, 0};
+      auto stage_of = [&](uint32_t it) { return it % C::NSTAGE; };
+      auto phase_of = [&](uint32_t it) { return (it / C::NSTAGE) & 1; };
+      auto issue_s = [&](int t, uint32_t stage) {
+        const uint32_t qa = sq + t * C::TILE_BYTES, ka = skv + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
+          mma_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
+                 k > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t stage, bool acc) {
+        const uint32_t va = skv + stage * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts(tmem + 256 + t * 128, tmem + t * BN + k * 8, sdesc_sw128(va + k * 2048, C::CHUNK_BYTES, 1024),
+                 idesc_o, (acc || k > 0) ? 1u : 0u);
+      };
+      for (int ui = u_begin; ui < u_end; ++ui) {
+        const Unit u = decode<CAUSAL>(p, ui);
+        if (!mbar_wait(&bars->q_full[0], u_phase, ab)) goto mma_done;
+        if (!mbar_wait(&bars->q_full[1], u_phase, ab)) goto mma_done;
+        uint32_t ks = stage_of(kv_it);
+        if (!mbar_wait(&bars->kv_full[ks], phase_of(kv_it), ab)) goto mma_done;
+        tc_fence_after();
+        issue_s(0, ks);
+        mma_commit(&bars->s_full[0]);
+        issue_s(1, ks);
+        mma_commit(&bars->s_full[1]);
+        mma_commit(&bars->kv_empty[ks]);
+        if (u.n_kv == 1) mma_commit(&bars->q_empty);
+        ++kv_it;
+        for (int j = 0; j < u.n_kv; ++j) {
+          const uint32_t vs = stage_of(kv_it);
+          if (!mbar_wait(&bars->kv_full[vs], phase_of(kv_it), ab)) goto mma_done;
+          ++kv_it;
+          const bool more = j + 1 < u.n_kv;
+          uint32_t ks2 = 0;
+          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
+          if (j == 0 && !mbar_wait(&bars->o_empty[0], u_phase ^ 1, ab)) goto mma_done;
+          if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
+          p_phase[0] ^= 1;
+          tc_fence_after();
+          issue_pv(0, vs, j > 0);
+          if (!more) mma_commit(&bars->o_full[0]);
+          if (more) {
+            ks2 = stage_of(kv_it);
+            if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
+            ++kv_it;
+            tc_fence_after();
+            issue_s(0, ks2);
+            mma_commit(&bars->s_full[0]);
+          }
+          // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+          if (j == 0 && !mbar_wait(&bars->o_empty[1], u_phase ^ 1, ab)) goto mma_done;
+          if (!mbar_wait(&bars->p_full[1], p_phase[1], ab)) goto mma_done;
+          p_phase[1] ^= 1;
+          tc_fence_after();
+          issue_pv(1, vs, j > 0);
+          mma_commit(&bars->kv_empty[vs]);
+          if (!more) mma_commit(&bars->o_full[1]);
+          if (more) {
+            issue_s(1, ks2);
+            mma_commit(&bars->s_full[1]);
+            mma_commit(&bars->kv_empty[ks2]);
+            if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+          }
+        }
+        u_phase ^= 1;
+      }
+    mma_done:
+      // wait until every issued MMA has landed before TMEM is released
+      mma_commit(&bars->drain);
+      {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+        }
+      }
+    } else if (warp == 13 && lane == 0) {
+      // ------------------------------------------------------------ TMA loader
+      uint32_t kv_it = 0, u_phase = 0;
+      for (int ui = u_begin; ui < u_end; ++ui) {
+        const Unit u = decode<CAUSAL>(p, ui);
+        if (!mbar_wait(&bars->q_empty, u_phase ^ 1, ab)) break;
+        for (int t = 0; t < 2; ++t) {
+          mbar_expect_tx(&bars->q_full[t], C::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_2d(&tm_q, &bars->q_full[t], sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, u.h * D + c * 64,
+                        u.q_row0 + BM * t);
+        }
+        bool ok = true;
+        for (int j = 0; j < u.n_kv && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t s = kv_it % C::NSTAGE, ph = (kv_it / C::NSTAGE) & 1;
+            if (!mbar_wait(&bars->kv_empty[s], ph ^ 1, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&bars->kv_full[s], C::TILE_BYTES);
+            const CUtensorMap* tm = w == 0 ? &tm_k : &tm_v;
+#pragma unroll
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_2d(tm, &bars->kv_full[s], sKV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, u.g * D + c * 64,
+                          u.kv0 + BN * j);
+            ++kv_it;
+          }
+        }
+        if (!ok) break;
+        u_phase ^= 1;
+      }
+      if (*ab.flag) {
+        // aborting: let copies already in flight land before the CTA exits
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  }
+done:
+  __syncwarp();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+int launch_impl(const FwdArgs& a) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  int st = make_map_2d(&tq, a.q, static_cast<uint64_t>(a.H) * D, a.q_rows, 64, BM);
+  if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BN);
+  if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BN);
+  if (st != JFA_OK) return st;
+  auto kern = fwd_kernel<D, CAUSAL>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
+      return JFA_ERR_CUDA;
+    attr_set = true;
+  }
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.offsets = a.offsets_dev;
+  p.units = reinterpret_cast<const int4*>(a.units);
+  p.cta_start = a.cta_start;
+  p.err = a.err;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.nq = a.nq;
+  p.o_rows = a.o_rows;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // namespace fwd
+
+int launch_fwd(const FwdArgs& a) {
+  if (a.D == 128) return a.causal ? fwd::launch_impl<128, true>(a) : fwd::launch_impl<128, false>(a);
+  return a.causal ? fwd::launch_impl<64, true>(a) : fwd::launch_impl<64, false>(a);
+}
+
+}  // namespace jfa

@@ -1,0 +1,48 @@
+// host.h -- host-side helpers shared by the launchers: tensor-map encoding,
+// device properties, error mapping.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/jfa.h"
+
+namespace jfa {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int max_smem_optin = 0;
+};
+
+// Properties of the current device (cached per device).  Returns JFA_OK or an error.
+int current_device(DeviceInfo* out);
+
+// 2-D bf16 tensor map over a row-major [rows, inner] matrix, 128-byte swizzle,
+// box {box_inner, box_rows}.  Rows past the end read as zero.
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                uint32_t box_rows);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Kernel launchers (one per .cu file).  They assume validated arguments.
+struct FwdArgs {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  const int32_t* offsets_dev;
+  int q_rows, kv_rows, o_rows;  // rows of q, of k/v, of o
+  int H, Hkv, D, nq;            // nq > 0: broadcast-Q
+  float scale;
+  int causal;
+  const int32_t* units;         // device, 4 ints per unit
+  const int32_t* cta_start;     // device, n_cta + 1
+  int n_cta;
+  int* err;                     // device error word
+  cudaStream_t stream;
+};
+int launch_fwd(const FwdArgs& a);
+
+}  // namespace jfa

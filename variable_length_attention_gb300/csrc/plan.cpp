@@ -1,0 +1,188 @@
+// plan.cpp -- host tile planners for the persistent kernels.
+//
+// Scheduling is decided on the CPU from the host copy of the offsets, so no
+// device synchronisation is needed before a launch ("TLX Block Attention",
+// section 5, scalar scheduling arithmetic on the CPU when CPU offsets exist).
+//
+// Forward: query work is split into units of 256 rows (two 128-row tiles that
+// share every K/V load).  A unit's cost is the number of 128-key blocks it
+// visits, which grows with the K/V length of its sequence.  Units are sorted by
+// cost, largest first, and dealt to the CTAs in snake order -- left to right on
+// even passes, right to left on odd ones -- so every CTA receives a mix of long
+// and short work (aixai.ru summary, "Tile balancing and Cluster Launch Control").
+//
+// Backward: a unit is one valid 128-key block of one (sequence, head); all such
+// units cost about the same (each loops over the same query rows) but their
+// number varies per sequence, so empty blocks are never listed and the list is
+// dealt round-robin.  Units are enumerated sequence-major, then head, then
+// block, so the CTAs working at the same moment share Q and dO through L2
+// (same source, same section).
+//
+// Block-diagonal: BLOCK_PER_BATCH is the prefix sum of 64-token block counts;
+// programs receive balanced contiguous ranges from closed-form divmod
+// ("TLX Block Attention", section 5).  A tile here is a pair of consecutive
+// global blocks for one head, because the tensor-core MMA used for it has 128
+// rows (two 64-token blocks).
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/jfa.h"
+#include "plan.h"
+
+namespace jfa {
+
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int check_offsets(const int32_t* offsets, int batch, int max_len) {
+  if (offsets == nullptr || batch < 0) return JFA_ERR_INVALID_ARG;
+  if (offsets[0] != 0) return JFA_ERR_BAD_OFFSETS;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+    if (L < 0) return JFA_ERR_BAD_OFFSETS;
+    if (max_len >= 0 && L > max_len) return JFA_ERR_BAD_OFFSETS;
+  }
+  return JFA_OK;
+}
+
+int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
+             std::vector<int32_t>* cta_start) {
+  struct U {
+    int32_t b, h, m, cost;
+  };
+  std::vector<U> all;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+    if (L == 0) continue;
+    const int64_t rows = nq > 0 ? nq : L;
+    const int64_t nm = cdiv(rows, kFwdRows);
+    for (int h = 0; h < H; ++h)
+      for (int64_t m = 0; m < nm; ++m) {
+        int64_t cost;
+        if (causal) {
+          const int64_t last_row = std::min<int64_t>(kFwdRows * (m + 1), rows);
+          cost = cdiv(std::min(last_row, L), kKvBlock);
+        } else {
+          cost = cdiv(L, kKvBlock);
+        }
+        all.push_back({b, h, static_cast<int32_t>(m), static_cast<int32_t>(cost)});
+      }
+  }
+  std::stable_sort(all.begin(), all.end(), [](const U& x, const U& y) { return x.cost > y.cost; });
+  const int64_t n = static_cast<int64_t>(all.size());
+  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
+  // snake deal: sorted index t -> pass p = t / P, slot r = t % P
+  std::vector<int32_t> cta_of(n), count(n_cta, 0);
+  for (int64_t t = 0; t < n; ++t) {
+    const int64_t p = t / n_cta, r = t % n_cta;
+    const int32_t c = static_cast<int32_t>((p % 2 == 0) ? r : n_cta - 1 - r);
+    cta_of[t] = c;
+    ++count[c];
+  }
+  std::vector<int32_t> start(n_cta + 1, 0);
+  for (int c = 0; c < n_cta; ++c) start[c + 1] = start[c] + count[c];
+  if (units) {
+    units->assign(4 * n, 0);
+    std::vector<int32_t> pos(start.begin(), start.end() - 1);
+    for (int64_t t = 0; t < n; ++t) {
+      const int64_t i = pos[cta_of[t]]++;
+      (*units)[4 * i + 0] = all[t].b;
+      (*units)[4 * i + 1] = all[t].h;
+      (*units)[4 * i + 2] = all[t].m;
+      (*units)[4 * i + 3] = all[t].cost;
+    }
+  }
+  if (cta_start) *cta_start = start;
+  return static_cast<int>(n);
+}
+
+int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
+             std::vector<int32_t>* cta_start) {
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) n += cdiv(static_cast<int64_t>(offsets[b + 1]) - offsets[b], kKvBlock) * H;
+  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
+  std::vector<int32_t> start(n_cta + 1, 0);
+  for (int c = 0; c < n_cta; ++c) {
+    const int64_t cnt = c < n ? (n - c + n_cta - 1) / n_cta : 0;
+    start[c + 1] = static_cast<int32_t>(start[c] + cnt);
+  }
+  if (units) {
+    units->assign(4 * n, 0);
+    int64_t u = 0;
+    for (int b = 0; b < batch; ++b) {
+      const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+      const int64_t rows = nq > 0 ? nq : L;
+      const int64_t q_tiles = cdiv(rows, kKvBlock);
+      for (int h = 0; h < H; ++h)
+        for (int64_t blk = 0; blk < cdiv(L, kKvBlock); ++blk, ++u) {
+          const int64_t c = u % n_cta, k = u / n_cta;
+          const int64_t i = start[c] + k;
+          (*units)[4 * i + 0] = b;
+          (*units)[4 * i + 1] = h;
+          (*units)[4 * i + 2] = static_cast<int32_t>(blk);
+          (*units)[4 * i + 3] = static_cast<int32_t>(causal ? q_tiles - blk : q_tiles);
+        }
+    }
+  }
+  if (cta_start) *cta_start = start;
+  return static_cast<int>(n);
+}
+
+int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<int32_t>* bpb,
+               std::vector<int32_t>* prog_start) {
+  std::vector<int32_t> pre(batch + 1, 0);
+  for (int b = 0; b < batch; ++b)
+    pre[b + 1] = static_cast<int32_t>(pre[b] + cdiv(static_cast<int64_t>(offsets[b + 1]) - offsets[b], kBlk));
+  const int64_t tiles = cdiv(pre[batch], 2) * H;
+  const int64_t P = std::min<int64_t>(n_sm, tiles);
+  if (prog_start) {
+    prog_start->assign(P + 1, 0);
+    if (P > 0) {
+      const int64_t q = tiles / P, r = tiles % P;
+      for (int64_t p = 0; p <= P; ++p) (*prog_start)[p] = static_cast<int32_t>(p * q + std::min(p, r));
+    }
+  }
+  if (bpb) *bpb = pre;
+  return static_cast<int>(P);
+}
+
+}  // namespace jfa
+
+// ------------------------------------------------------------- exported test hooks
+extern "C" int jfa_plan_fwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal,
+                            int n_cta, int32_t* units, int32_t* cta_start) {
+  if (num_heads <= 0 || n_cta <= 0 || nq_broadcast < 0) return -JFA_ERR_INVALID_ARG;
+  const int st = jfa::check_offsets(offsets_host, batch, -1);
+  if (st != JFA_OK) return -st;
+  std::vector<int32_t> u, s;
+  const int n = jfa::plan_fwd(offsets_host, batch, num_heads, nq_broadcast, causal, n_cta, units ? &u : nullptr,
+                              cta_start ? &s : nullptr);
+  if (units) std::copy(u.begin(), u.end(), units);
+  if (cta_start) std::copy(s.begin(), s.end(), cta_start);
+  return n;
+}
+
+extern "C" int jfa_plan_bwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal,
+                            int n_cta, int32_t* units, int32_t* cta_start) {
+  if (num_heads <= 0 || n_cta <= 0 || nq_broadcast < 0) return -JFA_ERR_INVALID_ARG;
+  const int st = jfa::check_offsets(offsets_host, batch, -1);
+  if (st != JFA_OK) return -st;
+  std::vector<int32_t> u, s;
+  const int n = jfa::plan_bwd(offsets_host, batch, num_heads, nq_broadcast, causal, n_cta, units ? &u : nullptr,
+                              cta_start ? &s : nullptr);
+  if (units) std::copy(u.begin(), u.end(), units);
+  if (cta_start) std::copy(s.begin(), s.end(), cta_start);
+  return n;
+}
+
+extern "C" int block_plan(const int32_t* offsets_host, int batch, int num_heads, int n_sm,
+                          int32_t* block_per_batch, int32_t* prog_start) {
+  if (num_heads <= 0 || n_sm <= 0) return -JFA_ERR_INVALID_ARG;
+  const int st = jfa::check_offsets(offsets_host, batch, -1);
+  if (st != JFA_OK) return -st;
+  std::vector<int32_t> b, p;
+  const int P = jfa::plan_block(offsets_host, batch, num_heads, n_sm, &b, &p);
+  if (block_per_batch) std::copy(b.begin(), b.end(), block_per_batch);
+  if (prog_start) std::copy(p.begin(), p.end(), prog_start);
+  return P;
+}

@@ -1,0 +1,25 @@
+// plan.h -- host planners shared by the API layer (see plan.cpp).
+#pragma once
+#include <cstdint>
+#include <vector>
+
+namespace jfa {
+
+constexpr int kFwdRows = 256;  // query rows per forward unit (two 128-row tiles)
+constexpr int kKvBlock = 128;  // keys per K/V block
+constexpr int kBlk = 64;       // block-diagonal block size
+
+// JFA_OK, or the status describing what is wrong with the offsets
+// (max_len < 0 skips the length bound).
+int check_offsets(const int32_t* offsets, int batch, int max_len);
+
+// Each returns the unit count; lists are CTA-major int32 quadruples.
+int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
+             std::vector<int32_t>* cta_start);
+int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
+             std::vector<int32_t>* cta_start);
+// Returns the number of programs P.
+int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<int32_t>* bpb,
+               std::vector<int32_t>* prog_start);
+
+}  // namespace jfa

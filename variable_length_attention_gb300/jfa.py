@@ -1,0 +1,238 @@
+"""Python binding of libjfa (ctypes).  Argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+include/jfa.h).  Tensors are torch tensors; PyTorch supplies device memory
+(outputs, workspace) and the current CUDA stream.  No arithmetic of the method
+happens in Python: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libjfa.so")
+
+JFA_OP_FWD, JFA_OP_BWD, JFA_OP_BLOCK_FWD, JFA_OP_BLOCK_BWD = 0, 1, 2, 3
+STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_BAD_OFFSETS",
+          4: "JFA_ERR_WORKSPACE_TOO_SMALL", 5: "JFA_ERR_ARCH", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT"}
+
+# exported symbols and their ctypes signatures
+_P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "jfa_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S, _P]),
+    "jfa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S, _P]),
+    "block_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "block_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "jfa_workspace_size": (_S, [_I, _P, _I, _I, _I, _I, _I, _I]),
+    "jfa_status_string": (ctypes.c_char_p, [_I]),
+    "jfa_device_status": (_I, [_P, _P]),
+    "jfa_plan_fwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "jfa_plan_bwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "block_plan": (_I, [_P, _I, _I, _I, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class JfaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+def load(path: str | None = None):
+    """Load libjfa.so (built by ``variable_length_attention_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libjfa.so is not built ({p}); run variable_length_attention_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype, f.argtypes = res, args
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _host_offsets(offsets, offsets_host):
+    if offsets_host is None:
+        offsets_host = offsets.detach().to("cpu")
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    return h
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(name, st):
+    if st != 0:
+        raise JfaError(name, st)
+
+
+def _workspace(op, offs_h, batch, nq, H, D, causal, bq, workspace, device):
+    need = load().jfa_workspace_size(op, offs_h.ctypes.data_as(ctypes.c_void_p), batch, nq, H, D, int(causal),
+                                     int(bq))
+    if need == 0 and batch >= 0:
+        need = 256
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, need
+
+
+def jfa_workspace_size(op, offsets_host, batch, nq_broadcast, num_heads, head_dim, causal, broadcast_q):
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    return load().jfa_workspace_size(op, h.ctypes.data_as(ctypes.c_void_p), batch, nq_broadcast, num_heads,
+                                     head_dim, int(causal), int(broadcast_q))
+
+
+def jfa_status_string(status: int) -> str:
+    return load().jfa_status_string(status).decode()
+
+
+def jfa_device_status(workspace) -> int:
+    return load().jfa_device_status(_ptr(workspace), _stream())
+
+
+def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False, scale=None,
+            out=None, lse=None, return_lse=True, workspace=None):
+    """Forward.  Returns (o, lse); lse is None if return_lse is False."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    bq = nq_broadcast > 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o_rows = batch * nq_broadcast if bq else int(offs_h[-1])
+    if out is None:
+        out = torch.empty((o_rows, H, D), dtype=torch.bfloat16, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((H, o_rows), dtype=torch.float32, device=q.device)
+    if not return_lse:
+        lse = None
+    workspace, need = _workspace(JFA_OP_FWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    st = L.jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
+                   offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv, D,
+                   float(scale), int(causal), int(bq), _ptr(workspace), workspace.numel(), _stream())
+    _check("jfa_fwd", st)
+    return out, lse
+
+
+def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False,
+            scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """Backward.  Returns (dq, dk, dv)."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    bq = nq_broadcast > 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    workspace, need = _workspace(JFA_OP_BWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    st = L.jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                   _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast),
+                   H, Hkv, D, float(scale), int(causal), int(bq), _ptr(workspace), workspace.numel(), _stream())
+    _check("jfa_bwd", st)
+    return dq, dk, dv
+
+
+def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=None, out=None, workspace=None):
+    """Block-diagonal (64-token blocks) forward.  Returns o."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    H, D = q.shape[1], q.shape[2]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty_like(q) if out is None else out
+    workspace, need = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    st = L.block_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p),
+                          batch, int(max_len), H, D, float(scale), _ptr(workspace), workspace.numel(), _stream())
+    _check("block_attn_fwd", st)
+    return out
+
+
+def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None, scale=None, dq=None, dk=None,
+                   dv=None, workspace=None):
+    """Block-diagonal backward.  Returns (dq, dk, dv)."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    H, D = q.shape[1], q.shape[2]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    workspace, need = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    st = L.block_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), H, D,
+                          float(scale), _ptr(workspace), workspace.numel(), _stream())
+    _check("block_attn_bwd", st)
+    return dq, dk, dv
+
+
+def _plan(fn_name, offsets_host, num_heads, nq, causal, n_cta):
+    L = load()
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    fn = getattr(L, fn_name)
+    n = fn(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, nq, int(causal), n_cta, None, None)
+    if n < 0:
+        raise JfaError(fn_name, -n)
+    units = np.zeros(4 * n, dtype=np.int32)
+    start = np.zeros(n_cta + 1, dtype=np.int32)
+    n2 = fn(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, nq, int(causal), n_cta,
+            units.ctypes.data_as(ctypes.c_void_p), start.ctypes.data_as(ctypes.c_void_p))
+    assert n2 == n
+    return units, start
+
+
+def jfa_plan_fwd(offsets_host, num_heads, n_cta, *, nq=0, causal=False):
+    """Host forward plan: (units int32[4n], cta_start int32[n_cta+1])."""
+    return _plan("jfa_plan_fwd", offsets_host, num_heads, nq, causal, n_cta)
+
+
+def jfa_plan_bwd(offsets_host, num_heads, n_cta, *, nq=0, causal=False):
+    """Host backward plan: (units int32[4n], cta_start int32[n_cta+1])."""
+    return _plan("jfa_plan_bwd", offsets_host, num_heads, nq, causal, n_cta)
+
+
+def block_plan(offsets_host, num_heads, n_sm):
+    """Block plan: (block_per_batch int32[B+1], prog_start int32[P+1])."""
+    L = load()
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    P = L.block_plan(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, n_sm, None, None)
+    if P < 0:
+        raise JfaError("block_plan", -P)
+    bpb = np.zeros(len(h), dtype=np.int32)
+    ps = np.zeros(P + 1, dtype=np.int32)
+    L.block_plan(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, n_sm,
+                 bpb.ctypes.data_as(ctypes.c_void_p), ps.ctypes.data_as(ctypes.c_void_p))
+    return bpb, ps
