@@ -82,3 +82,39 @@ def assert_fwd_ok(res):
     assert res["o_rel_l2"] <= O_REL_L2, res
     assert res["lse_max_abs"] <= LSE_MAX_ABS, res
     assert res["lse_inf_match"], res
+
+
+def kv_rows_of(offsets, sel, H):
+    """Boolean [kv_rows, H] mask of key rows covered by a unit selection."""
+    B = len(offsets) - 1
+    mask = np.zeros((int(offsets[-1]), H), dtype=bool)
+    for b in range(B):
+        mask[int(offsets[b]):int(offsets[b + 1])] = sel[b][None, :]
+    return mask
+
+
+def check_bwd(w, sel=None, nthreads=0):
+    """Runs jfa_fwd then jfa_bwd on the GPU and compares dQ, dK, dV with the oracle."""
+    (q, k, v, do), offs, cpu = gpu_inputs(w)
+    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale)
+    dq, dk, dv = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq,
+                           scale=w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.attn_bwd(to64(cpu[0]), to64(cpu[1]), to64(cpu[2]), to64(cpu[3]), w.offsets, scale=w.scale,
+                          causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads)
+    got = [to64(dq), to64(dk), to64(dv)]
+    want = list(ref[:3])
+    if sel is not None:
+        mq = rows_of(w.offsets, sel, w.num_heads) if not w.nq else np.ones(got[0].shape[:2], bool)
+        mk = kv_rows_of(w.offsets, sel, w.num_heads)
+        got = [got[0][mq], got[1][mk], got[2][mk]]
+        want = [want[0][mq], want[1][mk], want[2][mk]]
+    res = {name: rel_l2(g, r) for name, g, r in zip(("dq", "dk", "dv"), got, want)}
+    res["finite"] = bool(all(np.all(np.isfinite(g)) for g in got))
+    return res
+
+
+def assert_bwd_ok(res):
+    assert res["finite"], res
+    for name in ("dq", "dk", "dv"):
+        assert res[name] <= GRAD_REL_L2, res

@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "../../include/jfa.h"
+#include "bwd.h"
 #include "host.h"
 #include "plan.h"
 
@@ -135,6 +136,20 @@ static FwdLayout fwd_layout(int n_units, int n_cta, int batch) {
   return l;
 }
 
+struct BwdLayout {
+  size_t err = 0, units = 0, cta = 0, lse2 = 0, di = 0, dq_acc = 0, total = 0;
+};
+static BwdLayout bwd_layout(int n_units, int n_cta, int q_rows, int o_rows, int H, int D) {
+  BwdLayout l;
+  l.units = 256;
+  l.cta = l.units + align256(static_cast<size_t>(n_units) * 16);
+  l.lse2 = l.cta + align256(static_cast<size_t>(n_cta + 1) * 4);
+  l.di = l.lse2 + align256(static_cast<size_t>(H) * o_rows * 4);
+  l.dq_acc = l.di + align256(static_cast<size_t>(H) * o_rows * 4);
+  l.total = l.dq_acc + align256(static_cast<size_t>(q_rows) * H * D * 4);
+  return l;
+}
+
 __global__ void fill_empty_broadcast_kernel(const int32_t* empty_seq, int n_empty, int nq, int H, int D,
                                             int o_rows, __nv_bfloat16* o, float* lse) {
   // one block row per (empty sequence, query row); threads over H*D
@@ -204,7 +219,13 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
     const int n = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
     return fwd_layout(n, plan_ctas(dev, n), batch).total;
   }
-  (void)head_dim;
+  if (op == JFA_OP_BWD) {
+    if (head_dim != 64 && head_dim != 128) return 0;
+    const int n = plan_bwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+    const int q_rows = broadcast_q ? nq : offsets_host[batch];
+    const int o_rows = broadcast_q ? batch * nq : offsets_host[batch];
+    return bwd_layout(n, plan_ctas(dev, n), q_rows, o_rows, num_heads, head_dim).total;
+  }
   return 0;
 }
 
@@ -276,10 +297,73 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   return launch_fwd(a);
 }
 
-extern "C" int jfa_bwd(const void*, const void*, const void*, const void*, const void*, const float*, void*, void*,
-                       void*, const int32_t*, const int32_t*, int, int, int, int, int, int, float, int, int, void*,
-                       size_t, void*) {
-  return JFA_ERR_UNSUPPORTED;
+extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                       void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                       int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale,
+                       int causal, int broadcast_q, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Common c;
+  const int nq = broadcast_q ? nq_broadcast : 0;
+  int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
+                           head_dim, scale, causal, broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  if (num_kv_heads != num_heads) return JFA_ERR_UNSUPPORTED;  // backward needs a single query group
+  if (c.o_rows > 0 && (dout == nullptr || lse == nullptr || dq == nullptr)) return JFA_ERR_INVALID_ARG;
+  if (c.kv_rows > 0 && (dk == nullptr || dv == nullptr)) return JFA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
+
+  std::vector<int32_t> units, cta_start;
+  const int n_probe = plan_bwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+  const int n_cta = plan_ctas(c.dev, n_probe);
+  int n = 0;
+  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_heads, nq, causal, n_cta, &units, &cta_start);
+  const BwdLayout lay = bwd_layout(n, n_cta, c.q_rows, c.o_rows, num_heads, head_dim);
+  if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
+
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.offsets_dev = offsets_dev;
+  a.q_rows = c.q_rows;
+  a.kv_rows = c.kv_rows;
+  a.o_rows = c.o_rows;
+  a.H = num_heads;
+  a.D = head_dim;
+  a.nq = nq;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
+  a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
+  a.n_cta = n_cta;
+  a.lse2 = reinterpret_cast<float*>(ws + lay.lse2);
+  a.di = reinterpret_cast<float*>(ws + lay.di);
+  a.dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
+  a.err = reinterpret_cast<int*>(ws + lay.err);
+  a.stream = stream;
+
+  const size_t acc_bytes = static_cast<size_t>(c.q_rows) * num_heads * head_dim * 4;
+  if (acc_bytes && cudaMemsetAsync(a.dq_acc, 0, acc_bytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
+  if (n > 0) {
+    std::vector<uint8_t> blob(lay.lse2 - lay.units, 0);
+    std::memcpy(blob.data(), units.data(), units.size() * 4);
+    std::memcpy(blob.data() + (lay.cta - lay.units), cta_start.data(), cta_start.size() * 4);
+    st = stage_to_device(ws + lay.units, blob.data(), blob.size(), stream);
+    if (st != JFA_OK) return st;
+    st = launch_bwd_prep(a);
+    if (st != JFA_OK) return st;
+    st = launch_bwd_main(a);
+    if (st != JFA_OK) return st;
+  }
+  return launch_dq_convert(a, c.dev.num_sms);
 }
 
 extern "C" int block_attn_fwd(const void*, const void*, const void*, void*, const int32_t*, const int32_t*, int, int,

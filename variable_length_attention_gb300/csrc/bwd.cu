@@ -1,0 +1,576 @@
+// bwd.cu -- jagged flash-attention backward for sm_103a.
+//
+// What it computes, per (sequence, head), given Q, K, V, O, dO and the forward's
+// log-sum-exp L ("TLX Block Attention", section 4; the aixai.ru summary counts
+// five GEMMs per K/V block, "Paired CTAs"):
+//   P  = exp(scale Q K^T - L)            (recomputed, no stored P)
+//   dV = P^T dO,  dP = dO V^T,  Di = rowsum(dO o O),  dS = P o (dP - Di)
+//   dQ = scale dS K,  dK = scale dS^T Q
+// Broadcast-Q sums dQ of the shared Q over every sequence.
+//
+// Kernels, in launch order:
+//   prep_kernel   Di = rowsum(dO o O) and L * log2(e) per (row, head)
+//   bwd_kernel    persistent, one CTA per SM, one work unit = one valid block of
+//                 128 keys of one (sequence, head); it loops over the 128-row query
+//                 tiles that attend to those keys, keeps dK and dV in TMEM and
+//                 adds each tile's dQ into an fp32 accumulator
+//   dq_convert    dQ = scale * accumulator -> bf16
+//
+// bwd_kernel roles (warp specialisation as in the aixai.ru summary, "Framework",
+// including the dedicated dQ-reduction role):
+//   warps 0-3 / 4-7  one thread per key (TMEM lane); warpgroup w handles query
+//                    columns [64w, 64w+64): P^T (bf16, into TMEM) and dS^T (bf16,
+//                    into swizzled shared memory); at the end of a unit they write
+//                    dV (warpgroup 0) and dK (warpgroup 1)
+//   warps 8-11       dQ reduction: one thread per query row; reads dQ from TMEM,
+//                    releases TMEM as soon as the last slice is in registers, and
+//                    adds the row into the fp32 accumulator with vector reductions
+//                    (aixai.ru summary, "dQ epilogue": early TMEM release)
+//   warp 12          tcgen05 MMA issuer
+//   warp 13          loader: K, V by TMA once per unit; per query tile Q and dO by
+//                    TMA into a 2-deep ring, and L, Di into shared memory
+// TMEM: S^T [0,128) (P^T overwrites columns 0-31 and 64-95; dQ reuses [0,D)),
+//       dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+// Per tile the tensor core runs dP^T = V dO^T, S^T = K Q^T, dV += P^T dO,
+// dK += dS^T Q, dQ = dS K.
+// Masks: keys past the sequence end and query rows past it are zeroed per thread
+// (a key flag and L = +inf), so only the causal diagonal tile needs an
+// element-wise mask, and it is peeled into its own code path.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bwd.h"
+#include "host.h"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace bwd {
+
+constexpr int BQ = 128;  // query rows per tile
+constexpr int BK = 128;  // keys per unit
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static constexpr int TILE = 128 * D * 2;      // one 128-row bf16 tile
+  static constexpr int CHUNK = 128 * 128;        // one 64-column swizzle box (bytes)
+  static constexpr int NQS = 2;                  // Q/dO ring depth
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;                 // NQS x (Q, dO)
+  static constexpr int OFF_DS = OFF_Q + NQS * 2 * TILE;      // dS^T [128 keys][128 queries] bf16
+  static constexpr int OFF_BAR = OFF_DS + 128 * 128 * 2;
+  static constexpr int OFF_LD = OFF_BAR + 256;                    // per-stage L and Di, 128 floats each
+  static constexpr int SMEM_BYTES = OFF_LD + NQS * 1024;
+  // No alignment slack: at head_dim 128 this is within 1 KB of the 227 KB limit.
+  // The kernel checks that dynamic shared memory starts 1024-byte aligned.
+  static constexpr int SMEM_ALLOC = SMEM_BYTES;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr uint32_t COL_DV = 256;
+  static constexpr uint32_t COL_DK = 256 + D;
+};
+
+struct Params {
+  const int4* units;
+  const int32_t* cta_start;
+  const int32_t* offsets;
+  const float* lse2;   // [H, o_rows]  L * log2(e)
+  const float* di;     // [H, o_rows]
+  float* dq_acc;       // [q_rows, H, D]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* err;
+  int H, nq, o_rows;
+  float scale, scale_log2;
+};
+
+struct Unit {
+  int b, h, n;
+  int kv0, L;          // first key row of the sequence, its length
+  int rows;            // query rows (L, or nq in broadcast mode)
+  int i0, i1;          // query tiles [i0, i1)
+  int q_base, o_base;  // row of query 0 in q / in o
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode(const Params& p, int idx) {
+  const int4 e = p.units[idx];
+  Unit u;
+  u.b = e.x;
+  u.h = e.y;
+  u.n = e.z;
+  u.kv0 = p.offsets[u.b];
+  u.L = p.offsets[u.b + 1] - u.kv0;
+  if (p.nq > 0) {
+    u.rows = p.nq;
+    u.q_base = 0;
+    u.o_base = u.b * p.nq;
+  } else {
+    u.rows = u.L;
+    u.q_base = u.kv0;
+    u.o_base = u.kv0;
+  }
+  u.i0 = CAUSAL ? u.n : 0;
+  u.i1 = (u.rows + BQ - 1) / BQ;
+  return u;
+}
+
+struct Bars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023) != 0) {  // the layout below needs 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, kDevMisaligned);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  static_assert(sizeof(Bars) <= 256, "barrier block");
+  float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LD);  // [NQS][128]
+  float* s_di = s_lse + C::NQS * 128;                          // [NQS][128]
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int u_begin = p.cta_start[blockIdx.x];
+  const int u_end = p.cta_start[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 32);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->ds_empty, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 4);
+    mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->dkv_empty, 8);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Abort ab{&bars->abort_flag, p.err};
+
+  if (warp < 8) {
+    // -------------------------------------------------------- P^T and dS^T
+    setmaxnreg_inc<168>();
+    const int wg = warp >> 2;              // query half
+    const int k = threadIdx.x & 127;       // key row == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + 64 * wg;          // S^T columns of this half
+    const uint32_t tP = tmem + lane_addr + 64 * wg;          // P^T packed (32 columns)
+    const uint32_t tDP = tmem + lane_addr + 128 + 64 * wg;
+    uint8_t* sDS = smem + C::OFF_DS + wg * C::CHUNK + k * 128;  // row k of this half's box
+    const float sl2 = p.scale_log2;
+    uint32_t ph = 0, ds_ph = 0, dkv_ph = 0, q_it = 0;
+    for (int ui = u_begin; ui < u_end; ++ui) {
+      const Unit u = decode<CAUSAL>(p, ui);
+      const bool key_ok = BK * u.n + k < u.L;
+      for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+        const int st = q_it & 1;
+        const float* lse_s = s_lse + st * 128 + 64 * wg;
+        const float* di_s = s_di + st * 128 + 64 * wg;
+        if (!mbar_wait(&bars->s_full, ph, ab)) goto done;
+        if (!mbar_wait(&bars->dp_full, ph, ab)) goto done;
+        ph ^= 1;
+        tc_fence_after();
+        const bool diag = CAUSAL && i == u.n;
+        // dS^T goes to shared memory once the previous tile's dK/dQ MMAs have read
+        // it (they were issued before this tile's S^T, so this rarely waits)
+        if (!mbar_wait(&bars->ds_empty, ds_ph ^ 1, ab)) goto done;
+        ds_ph ^= 1;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tS + 32 * pass, sr);
+          tmem_ld32(tDP + 32 * pass, dr);
+          tmem_wait_ld();
+          reg_fence<32>(sr);
+          reg_fence<32>(dr);
+          uint32_t pw[16], dsw[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * pass + c);
+            const float4 d4 = *reinterpret_cast<const float4*>(di_s + 32 * pass + c);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pe = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, -lv[e]));
+              if (diag && (64 * wg + 32 * pass + c + e) < k) pe = 0.f;
+              pe = key_ok ? pe : 0.f;
+              pv[e] = pe;
+              dsv[e] = pe * (__uint_as_float(dr[c + e]) - dv[e]);
+            }
+            pw[c / 2] = pack_bf16(pv[0], pv[1]);
+            pw[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
+            dsw[c / 2] = pack_bf16(dsv[0], dsv[1]);
+            dsw[c / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
+          }
+          tmem_st16(tP + 16 * pass, pw);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int chunk = 4 * pass + j;
+            const uint32_t addr = smem_u32(sDS + ((chunk ^ (k & 7)) << 4));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dsw[4 * j]),
+                         "r"(dsw[4 * j + 1]), "r"(dsw[4 * j + 2]), "r"(dsw[4 * j + 3])
+                         : "memory");
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->p_full);
+          mbar_arrive(&bars->ds_full);
+        }
+      }
+      // unit done: write dV (warpgroup 0) or dK (warpgroup 1)
+      if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
+      dkv_ph ^= 1;
+      tc_fence_after();
+      {
+        const uint32_t tAcc = tmem + lane_addr + (wg == 0 ? C::COL_DV : C::COL_DK);
+        const float mul = wg == 0 ? 1.0f : p.scale;
+        __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + (static_cast<size_t>(u.kv0 + BK * u.n + k) * p.H + u.h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tAcc + c, ov);
+          tmem_wait_ld();
+          reg_fence<32>(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
+          if (key_ok) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dkv_empty);
+    }
+  } else if (warp < 12) {
+    // -------------------------------------------------------- dQ reduction
+    setmaxnreg_dec<96>();
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tQ = tmem + lane_addr;
+    uint32_t ph = 0;
+    for (int ui = u_begin; ui < u_end; ++ui) {
+      const Unit u = decode<CAUSAL>(p, ui);
+      for (int i = u.i0; i < u.i1; ++i) {
+        if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
+        ph ^= 1;
+        tc_fence_after();
+        const bool valid = BQ * i + r < u.rows;
+        float* dst = p.dq_acc + (static_cast<size_t>(u.q_base + BQ * i + r) * p.H + u.h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tQ + c, v);
+          tmem_wait_ld();
+          reg_fence<32>(v);
+          if (c + 32 == D) {  // last slice is in registers: hand TMEM back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->dq_empty);
+          }
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c + 4 * e),
+                           "f"(__uint_as_float(v[4 * e])), "f"(__uint_as_float(v[4 * e + 1])),
+                           "f"(__uint_as_float(v[4 * e + 2])), "f"(__uint_as_float(v[4 * e + 3]))
+                           : "memory");
+          }
+        }
+      }
+    }
+  } else {
+    setmaxnreg_dec<80>();
+    if (warp == 12) {
+      if (lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+        const uint32_t id_kv = idesc_bf16(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
+        const uint32_t id_q = idesc_bf16(128, D, 1, 1);     // dQ: A (dS) and B (K) MN-major
+        const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+        const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+        uint32_t kv_ph = 0, ph = 0, dq_ph = 0, dkv_ph = 0, q_it = 0;
+        for (int ui = u_begin; ui < u_end; ++ui) {
+          const Unit u = decode<CAUSAL>(p, ui);
+          if (!mbar_wait(&bars->kv_full, kv_ph, ab)) goto mma_done;
+          kv_ph ^= 1;
+          for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+            const uint32_t st = q_it & 1;
+            const uint32_t sQ = smem_u32(smem + C::OFF_Q + st * 2 * C::TILE);
+            const uint32_t sDO = sQ + C::TILE;
+            if (!mbar_wait(&bars->q_full[st], (q_it >> 1) & 1, ab)) goto mma_done;
+            tc_fence_after();
+            // dP^T = V dO^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+              mma_ss(tmem + 128, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0);
+            }
+            mma_commit(&bars->dp_full);
+            // S^T = K Q^T, once the previous dQ has left TMEM
+            if (i > u.i0 || ui > u_begin) {
+              if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
+              dq_ph ^= 1;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+              mma_ss(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0);
+            }
+            mma_commit(&bars->s_full);
+            // dV += P^T dO  (A from TMEM)
+            if (i == u.i0) {
+              if (!mbar_wait(&bars->dkv_empty, dkv_ph ^ 1, ab)) goto mma_done;
+              dkv_ph ^= 1;
+            }
+            if (!mbar_wait(&bars->p_full, ph, ab)) goto mma_done;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
+              mma_ts(tmem + C::COL_DV, tmem + pcol, sdesc_sw128(sDO + kk * 2048, C::CHUNK, 1024), id_kv,
+                     (i > u.i0 || kk > 0) ? 1u : 0u);
+            }
+            // dK += dS^T Q ; dQ = dS K
+            if (!mbar_wait(&bars->ds_full, ph, ab)) goto mma_done;
+            ph ^= 1;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+              mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(sQ + kk * 2048, C::CHUNK, 1024),
+                     id_kv, (i > u.i0 || kk > 0) ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
+                     id_q, kk > 0);
+            mma_commit(&bars->dq_full);
+            mma_commit(&bars->ds_empty);
+            mma_commit(&bars->q_empty[st]);
+          }
+          mma_commit(&bars->dkv_full);
+          mma_commit(&bars->kv_empty);
+        }
+      mma_done:
+        mma_commit(&bars->drain);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - t0 < kWaitTimeoutNs) {
+        }
+      }
+    } else if (warp == 13) {
+      // ------------------------------------------------------ loader (whole warp)
+      uint32_t kv_ph = 0, q_it = 0;
+      bool ok = true;
+      for (int ui = u_begin; ui < u_end && ok; ++ui) {
+        const Unit u = decode<CAUSAL>(p, ui);
+        if (!mbar_wait(&bars->kv_empty, kv_ph ^ 1, ab)) break;
+        kv_ph ^= 1;
+        if (lane == 0) {
+          mbar_expect_tx(&bars->kv_full, 2 * C::TILE);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n);
+            tma_load_2d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n);
+          }
+        }
+        for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+          const uint32_t st = q_it & 1;
+          if (!mbar_wait(&bars->q_empty[st], ((q_it >> 1) & 1) ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          // L and Di of the tile's 128 query rows (rows past the end: L = +inf so P = 0)
+          const size_t lbase = static_cast<size_t>(u.h) * p.o_rows + u.o_base + BQ * i;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * lane + e;
+            const bool v = BQ * i + r < u.rows;
+            s_lse[st * 128 + r] = v ? p.lse2[lbase + r] : INFINITY;
+            s_di[st * 128 + r] = v ? p.di[lbase + r] : 0.f;
+          }
+          uint8_t* sQ = smem + C::OFF_Q + st * 2 * C::TILE;
+          if (lane == 0) {
+            mbar_expect_tx(&bars->q_full[st], 2 * C::TILE);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_2d(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, u.h * D + c * 64, u.q_base + BQ * i);
+              tma_load_2d(&tm_do, &bars->q_full[st], sQ + C::TILE + c * C::CHUNK, u.h * D + c * 64,
+                          u.o_base + BQ * i);
+            }
+          } else {
+            mbar_arrive(&bars->q_full[st]);
+          }
+        }
+      }
+      if (*ab.flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  }
+done:
+  __syncwarp();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Di[h, r] = sum_d dO[r,h,d] O[r,h,d];  lse2[h, r] = L[h, r] log2(e).
+// 16 threads per (row, head) for D = 128 (8 per head for D = 64), 8 bf16 each.
+template <int D>
+__global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                            const float* __restrict__ lse, float* __restrict__ di, float* __restrict__ lse2,
+                            int rows, int H) {
+  constexpr int TPR = D / 8;
+  const long gid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long pair = gid / TPR;  // (row, head) index = row * H + h
+  const int part = static_cast<int>(gid % TPR);
+  float acc = 0.f;
+  const bool in = pair < static_cast<long>(rows) * H;
+  if (in) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + pair * D + part * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + pair * D + part * 8);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(a2[e]);
+      const float2 fb = __bfloat1622float2(b2[e]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && part == 0) {
+    const int r = static_cast<int>(pair / H), h = static_cast<int>(pair % H);
+    di[static_cast<size_t>(h) * rows + r] = acc;
+    lse2[static_cast<size_t>(h) * rows + r] = lse[static_cast<size_t>(h) * rows + r] * kLog2e;
+  }
+}
+
+__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4, float scale) {
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    uint2 w;
+    w.x = pack_bf16(v.x * scale, v.y * scale);
+    w.y = pack_bf16(v.z * scale, v.w * scale);
+    reinterpret_cast<uint2*>(dq)[i] = w;
+  }
+}
+
+template <int D, bool CAUSAL>
+int launch_main(const BwdArgs& a) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  int st = make_map_2d(&tq, a.q, static_cast<uint64_t>(a.H) * D, a.q_rows, 64, BQ);
+  if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BQ);
+  if (st != JFA_OK) return st;
+  auto kern = bwd_kernel<D, CAUSAL>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
+      return JFA_ERR_CUDA;
+    attr_set = true;
+  }
+  Params p;
+  p.units = reinterpret_cast<const int4*>(a.units);
+  p.cta_start = a.cta_start;
+  p.offsets = a.offsets_dev;
+  p.lse2 = a.lse2;
+  p.di = a.di;
+  p.dq_acc = a.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.err = a.err;
+  p.H = a.H;
+  p.nq = a.nq;
+  p.o_rows = a.o_rows;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // namespace bwd
+
+int launch_bwd_prep(const BwdArgs& a) {
+  if (a.o_rows == 0) return JFA_OK;
+  const long threads = static_cast<long>(a.o_rows) * a.H * (a.D / 8);
+  const int block = 256;
+  const long grid = (threads + block - 1) / block;
+  if (a.D == 128)
+    bwd::prep_kernel<128><<<grid, block, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.o),
+                                                         static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di,
+                                                         a.lse2, a.o_rows, a.H);
+  else
+    bwd::prep_kernel<64><<<grid, block, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.o),
+                                                        static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di,
+                                                        a.lse2, a.o_rows, a.H);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+int launch_bwd_main(const BwdArgs& a) {
+  if (a.D == 128) return a.causal ? bwd::launch_main<128, true>(a) : bwd::launch_main<128, false>(a);
+  return a.causal ? bwd::launch_main<64, true>(a) : bwd::launch_main<64, false>(a);
+}
+
+int launch_dq_convert(const BwdArgs& a, int num_sms) {
+  const long n4 = static_cast<long>(a.q_rows) * a.H * a.D / 4;
+  if (n4 == 0) return JFA_OK;
+  long grid = (n4 + 255) / 256;
+  if (grid > 8L * num_sms) grid = 8L * num_sms;
+  bwd::dq_convert_kernel<<<static_cast<int>(grid), 256, 0, a.stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq),
+                                                                       n4, a.scale);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // namespace jfa

@@ -15,6 +15,7 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 enum DeviceError : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,
+  kDevMisaligned = 2,   // dynamic shared memory not 1024-byte aligned
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
