@@ -171,6 +171,18 @@ int jfa_plan_bwd(const int32_t* offsets_host, int batch, int num_heads, int nq_b
 int block_plan(const int32_t* offsets_host, int batch, int num_heads, int n_sm, int32_t* block_per_batch,
                int32_t* prog_start);
 
+/*
+ * Optional kernel timing (no counterpart on the pages; measurement support).
+ * jfa_profile_enable(1) starts bracketing every library kernel launch with CUDA
+ * events on its stream (and forgets earlier records); jfa_profile_enable(0)
+ * stops it.  jfa_profile_read(kind, &ms, &n) synchronises on the recorded
+ * events and returns the summed device time and the launch count of one kernel
+ * kind: 0 forward, 1 backward prepass (Di), 2 backward main, 3 dQ convert,
+ * 4 block forward, 5 block backward, 6 empty-sequence fill.
+ */
+int jfa_profile_enable(int on);
+int jfa_profile_read(int kind, double* total_ms, int* launches);
+
 #ifdef __cplusplus
 }
 #endif

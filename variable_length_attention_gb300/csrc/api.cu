@@ -14,6 +14,7 @@
 #include "bwd.h"
 #include "host.h"
 #include "plan.h"
+#include "profile.h"
 
 namespace jfa {
 
@@ -260,6 +261,7 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
     st = stage_to_device(ws + lay.empty, empty.data(), empty.size() * 4, stream);
     if (st != JFA_OK) return st;
     const int blocks = static_cast<int>(empty.size()) * nq;
+    ProfileScope prof(kKindFill, stream);
     fill_empty_broadcast_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const int32_t*>(ws + lay.empty),
                                                              static_cast<int>(empty.size()), nq, num_heads,
                                                              head_dim, c.o_rows, static_cast<__nv_bfloat16*>(o), lse);

@@ -42,6 +42,7 @@
 
 #include "bwd.h"
 #include "host.h"
+#include "profile.h"
 #include "ptx.cuh"
 
 namespace jfa {
@@ -536,6 +537,7 @@ int launch_main(const BwdArgs& a) {
   p.o_rows = a.o_rows;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  ProfileScope prof(kKindBwdMain, a.stream);
   kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -547,6 +549,7 @@ int launch_bwd_prep(const BwdArgs& a) {
   const long threads = static_cast<long>(a.o_rows) * a.H * (a.D / 8);
   const int block = 256;
   const long grid = (threads + block - 1) / block;
+  ProfileScope prof(kKindBwdPrep, a.stream);
   if (a.D == 128)
     bwd::prep_kernel<128><<<grid, block, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.o),
                                                          static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di,
@@ -568,6 +571,7 @@ int launch_dq_convert(const BwdArgs& a, int num_sms) {
   if (n4 == 0) return JFA_OK;
   long grid = (n4 + 255) / 256;
   if (grid > 8L * num_sms) grid = 8L * num_sms;
+  ProfileScope prof(kKindDqConvert, a.stream);
   bwd::dq_convert_kernel<<<static_cast<int>(grid), 256, 0, a.stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq),
                                                                        n4, a.scale);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include "host.h"
+#include "profile.h"
 #include "ptx.cuh"
 
 namespace jfa {
@@ -457,6 +458,7 @@ int launch_impl(const FwdArgs& a) {
   p.nq = a.nq;
   p.o_rows = a.o_rows;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  ProfileScope prof(kKindFwd, a.stream);
   kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }

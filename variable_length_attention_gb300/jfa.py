@@ -35,7 +35,11 @@ SIGNATURES = {
     "jfa_plan_fwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "jfa_plan_bwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "block_plan": (_I, [_P, _I, _I, _I, _P, _P]),
+    "jfa_profile_enable": (_I, [_I]),
+    "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
+KERNEL_KINDS = {"fwd": 0, "bwd_prep": 1, "bwd_main": 2, "dq_convert": 3, "block_fwd": 4, "block_bwd": 5,
+                "fill": 6}
 
 _lock = threading.Lock()
 _lib = None
@@ -236,3 +240,16 @@ def block_plan(offsets_host, num_heads, n_sm):
     L.block_plan(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, n_sm,
                  bpb.ctypes.data_as(ctypes.c_void_p), ps.ctypes.data_as(ctypes.c_void_p))
     return bpb, ps
+
+
+def jfa_profile_enable(on: bool = True):
+    """Start (or stop) bracketing every library kernel launch with CUDA events."""
+    _check("jfa_profile_enable", load().jfa_profile_enable(int(on)))
+
+
+def jfa_profile_read(kind) -> tuple[float, int]:
+    """(summed device milliseconds, launches) of one kernel kind since enabling."""
+    k = KERNEL_KINDS[kind] if isinstance(kind, str) else int(kind)
+    ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+    _check("jfa_profile_read", load().jfa_profile_read(k, ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
