@@ -99,7 +99,8 @@ int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, co
  *   P = exp(scale q k^T - lse), dV = P^T dO, dP = dO V^T, Di = rowsum(dO o O),
  *   dS = P o (dP - Di), dQ = scale dS K, dK = scale dS^T Q.
  * Requires num_kv_heads == num_heads.  In broadcast-Q mode dq is summed over all
- * sequences.  Valid 128-key blocks are dealt round-robin to the CTAs.
+ * sequences.  Only valid 128-key blocks are listed; they are sorted by cost
+ * and snake-dealt to the CTAs (see jfa_plan_bwd).
  */
 int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
@@ -156,7 +157,8 @@ int jfa_device_status(const void* workspace, void* stream);
  *   jfa_plan_fwd: unit = 256 query rows (b, h, m); cost = 128-key blocks
  *     visited; stable sort by cost descending; snake deal over n_cta.
  *   jfa_plan_bwd: unit = one valid 128-key block (b, h, n), enumerated b, h, n
- *     (n innermost), dealt round-robin; cost = 128-row query tiles visited.
+ *     (n innermost); cost = 128-row query tiles visited; stable sort by cost
+ *     descending, snake deal (equal costs keep the enumeration order).
  */
 int jfa_plan_fwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal, int n_cta,
                  int32_t* units, int32_t* cta_start);

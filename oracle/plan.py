@@ -16,7 +16,10 @@ P-1-r on odd passes.
 Backward (jagged): a unit is (b, h, n), the n-th block of 128 keys of sequence b,
 head h; only blocks that hold at least one key exist.  They are enumerated b
 outer, h middle, n inner (units of one (b, h) run side by side and share the
-same Q and dO in L2) and dealt round-robin: unit u goes to CTA u mod P.
+same Q and dO in L2); their cost is the number of 128-row query tiles they
+visit.  They are stably sorted by cost, largest first, and dealt in the same
+snake order as the forward (with equal costs this is the enumeration order
+dealt back and forth).
 
 Block-diagonal: each sequence has ceil(L/64) blocks; BLOCK_PER_BATCH is their
 exclusive prefix sum.  A tile is a pair of consecutive global blocks (2p, 2p+1)
@@ -76,9 +79,14 @@ def plan_bwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
                 else:
                     cost = _cdiv(rows, FWD_ROWS // 2)
                 units.append((b, h, n, cost))
+    # stable sort by cost, largest first (a no-op when all costs are equal, as in
+    # broadcast-Q), then the same snake deal as the forward
+    order = sorted(range(len(units)), key=lambda i: -units[i][3])
     per_cta = [[] for _ in range(n_cta)]
-    for u, e in enumerate(units):
-        per_cta[u % n_cta].append(e)
+    for t, i in enumerate(order):
+        p, r = divmod(t, n_cta)
+        cta = r if p % 2 == 0 else n_cta - 1 - r
+        per_cta[cta].append(units[i])
     return _flatten(per_cta)
 
 

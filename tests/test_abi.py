@@ -1,0 +1,101 @@
+"""The C ABI: the library loads on a machine without a GPU, exports every entry
+point include/jfa.h declares, and rejects bad arguments before any device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import variable_length_attention_gb300 as V
+from variable_length_attention_gb300 import jfa as J
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "jfa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol():
+    lib = J.load()
+    names = _declared()
+    assert "jfa_fwd" in names and "jfa_bwd" in names and "block_attn_fwd" in names and "block_attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding knows every one of them
+    assert set(names) <= set(J.SIGNATURES), set(names) - set(J.SIGNATURES)
+
+
+def test_status_strings():
+    for code in range(8):
+        s = V.jfa_status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert V.jfa_status_string(99) == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)        # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def _fwd(offsets, *, q=FAKE, D=128, H=2, Hkv=2, causal=0, bq=0, nq=0, scale=0.1, max_len=None, batch=None):
+    lib = J.load()
+    h = np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
+    if max_len is None:
+        max_len = int(np.max(np.diff(h))) if len(h) > 1 else 0
+    if batch is None:
+        batch = len(h) - 1
+    return lib.jfa_fwd(q, FAKE, FAKE, FAKE, None, FAKE, h.ctypes.data_as(ctypes.c_void_p), batch, max_len, nq, H,
+                       Hkv, D, scale, causal, bq, FAKE, 1 << 20, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(D=96), 2),                          # head_dim not 64/128
+    (dict(H=3, Hkv=2), 2),                    # heads not a multiple of kv heads
+    (dict(causal=1, bq=1, nq=8), 2),          # causal broadcast is undefined
+    (dict(bq=1, nq=0), 1),                    # broadcast without query rows
+    (dict(scale=0.0), 1),                     # scale must be positive
+    (dict(scale=float("nan")), 1),
+    (dict(q=MISALIGNED), 1),                  # TMA needs 16-byte aligned bases
+    (dict(max_len=10), 3),                    # a sequence longer than max_len
+    (dict(batch=-1), 1),
+])
+def test_fwd_argument_errors(kwargs, status):
+    assert _fwd([0, 17, 40], **kwargs) == status
+
+
+@pytest.mark.parametrize("offsets", [[5, 10], [0, 10, 4], [0, -1]])
+def test_bad_offsets(offsets):
+    assert _fwd(offsets, max_len=100) == 3
+
+
+def test_bwd_rejects_gqa_before_device_work():
+    lib = J.load()
+    h = np.array([0, 10, 20], dtype=np.int32)
+    st = lib.jfa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, h.ctypes.data_as(ctypes.c_void_p),
+                     2, 10, 0, 4, 2, 64, 0.125, 0, 0, FAKE, 1 << 20, None)
+    assert st == 2
+
+
+def test_planner_hooks_reject_bad_input():
+    lib = J.load()
+    h = np.array([1, 5], dtype=np.int32)
+    assert lib.jfa_plan_fwd(h.ctypes.data_as(ctypes.c_void_p), 1, 2, 0, 0, 4, None, None) == -3
+    h = np.array([0, 5], dtype=np.int32)
+    assert lib.jfa_plan_fwd(h.ctypes.data_as(ctypes.c_void_p), 1, 0, 0, 0, 4, None, None) == -1
+    assert lib.block_plan(h.ctypes.data_as(ctypes.c_void_p), 1, 2, 0, None, None) == -1
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        J._lib_missing = True
+        ctypes_path = str(tmp_path / "nope.so")
+        # a fresh loader pointed at a missing file must raise, never fall back
+        saved = J._lib
+        J._lib = None
+        try:
+            J.load(ctypes_path)
+        finally:
+            J._lib = saved

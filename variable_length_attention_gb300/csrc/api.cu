@@ -186,7 +186,7 @@ static int validate_common(const void* q, const void* k, const void* v, const vo
   if (c->o_rows > 0 && (q == nullptr || o == nullptr)) return JFA_ERR_INVALID_ARG;
   if (c->kv_rows > 0 && (k == nullptr || v == nullptr)) return JFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return JFA_ERR_INVALID_ARG;
-  return current_device(&c->dev);
+  return JFA_OK;  // the caller queries the device after its own argument checks
 }
 
 static int plan_ctas(const DeviceInfo& dev, int n_units) { return n_units < dev.num_sms ? n_units : dev.num_sms; }
@@ -241,6 +241,8 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
                            head_dim, scale, causal, broadcast_q, &c);
   if (st != JFA_OK) return st;
   if (workspace == nullptr && workspace_bytes > 0) return JFA_ERR_INVALID_ARG;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
 
   std::vector<int32_t> units, cta_start;
   const int n_probe = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
@@ -313,6 +315,8 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   if (c.o_rows > 0 && (dout == nullptr || lse == nullptr || dq == nullptr)) return JFA_ERR_INVALID_ARG;
   if (c.kv_rows > 0 && (dk == nullptr || dv == nullptr)) return JFA_ERR_INVALID_ARG;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
 
   std::vector<int32_t> units, cta_start;
   const int n_probe = plan_bwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // -------------------------------------------------------- P^T and dS^T
-    setmaxnreg_inc<168>();
+    // register split 144 / 144 / 144 / 80 over the four warpgroups (65,536 total)
+    setmaxnreg_inc<144>();
     const int wg = warp >> 2;              // query half
     const int k = threadIdx.x & 127;       // key row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -203,40 +204,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph ^= 1;
         tc_fence_after();
         const bool diag = CAUSAL && i == u.n;
-        // dS^T goes to shared memory once the previous tile's dK/dQ MMAs have read
-        // it (they were issued before this tile's S^T, so this rarely waits)
-        if (!mbar_wait(&bars->ds_empty, ds_ph ^ 1, ab)) goto done;
-        ds_ph ^= 1;
+        // P^T first: the dV MMA can start while dS^T is being formed
+        float pf[64];
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-          uint32_t sr[32], dr[32];
+          uint32_t sr[32];
           tmem_ld32(tS + 32 * pass, sr);
-          tmem_ld32(tDP + 32 * pass, dr);
           tmem_wait_ld();
           reg_fence<32>(sr);
-          reg_fence<32>(dr);
-          uint32_t pw[16], dsw[16];
+          uint32_t pw[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * pass + c);
-            const float4 d4 = *reinterpret_cast<const float4*>(di_s + 32 * pass + c);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               float pe = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, -lv[e]));
               if (diag && (64 * wg + 32 * pass + c + e) < k) pe = 0.f;
-              pe = key_ok ? pe : 0.f;
-              pv[e] = pe;
-              dsv[e] = pe * (__uint_as_float(dr[c + e]) - dv[e]);
+              pf[32 * pass + c + e] = key_ok ? pe : 0.f;
             }
-            pw[c / 2] = pack_bf16(pv[0], pv[1]);
-            pw[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
+            pw[c / 2] = pack_bf16(pf[32 * pass + c], pf[32 * pass + c + 1]);
+            pw[c / 2 + 1] = pack_bf16(pf[32 * pass + c + 2], pf[32 * pass + c + 3]);
+          }
+          tmem_st16(tP + 16 * pass, pw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+        // dS^T = P^T o (dP^T - Di) into shared memory, once the previous tile's
+        // dK/dQ MMAs have read it (they were issued before this tile's S^T, so
+        // this rarely waits)
+        if (!mbar_wait(&bars->ds_empty, ds_ph ^ 1, ab)) goto done;
+        ds_ph ^= 1;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          uint32_t dr[32];
+          tmem_ld32(tDP + 32 * pass, dr);
+          tmem_wait_ld();
+          reg_fence<32>(dr);
+          uint32_t dsw[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(di_s + 32 * pass + c);
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dsv[e] = pf[32 * pass + c + e] * (__uint_as_float(dr[c + e]) - dv[e]);
             dsw[c / 2] = pack_bf16(dsv[0], dsv[1]);
             dsw[c / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
           }
-          tmem_st16(tP + 16 * pass, pw);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int chunk = 4 * pass + j;
@@ -246,14 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
         }
-        tmem_wait_st();
         tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->p_full);
-          mbar_arrive(&bars->ds_full);
-        }
+        if (lane == 0) mbar_arrive(&bars->ds_full);
       }
       // unit done: write dV (warpgroup 0) or dK (warpgroup 1)
       if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
@@ -286,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // -------------------------------------------------------- dQ reduction
-    setmaxnreg_dec<96>();
+    setmaxnreg_inc<144>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tQ = tmem + lane_addr;
@@ -299,25 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool valid = BQ * i + r < u.rows;
         float* dst = p.dq_acc + (static_cast<size_t>(u.q_base + BQ * i + r) * p.H + u.h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tQ + c, v);
-          tmem_wait_ld();
-          reg_fence<32>(v);
-          if (c + 32 == D) {  // last slice is in registers: hand TMEM back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->dq_empty);
-          }
-          if (valid) {
+        // the whole row into registers first, then TMEM goes back to the MMA warp
+        // before any reduction is issued
+        uint32_t v[D];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c + 4 * e),
-                           "f"(__uint_as_float(v[4 * e])), "f"(__uint_as_float(v[4 * e + 1])),
-                           "f"(__uint_as_float(v[4 * e + 2])), "f"(__uint_as_float(v[4 * e + 3]))
-                           : "memory");
-          }
+        for (int c = 0; c < D; c += 32) tmem_ld32(tQ + c, v + c);
+        tmem_wait_ld();
+        reg_fence<D>(v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dq_empty);
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < D / 4; ++e)
+            asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * e),
+                         "f"(__uint_as_float(v[4 * e])), "f"(__uint_as_float(v[4 * e + 1])),
+                         "f"(__uint_as_float(v[4 * e + 2])), "f"(__uint_as_float(v[4 * e + 3]))
+                         : "memory");
         }
       }
     }

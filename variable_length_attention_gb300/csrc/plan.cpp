@@ -11,12 +11,17 @@
 // even passes, right to left on odd ones -- so every CTA receives a mix of long
 // and short work (aixai.ru summary, "Tile balancing and Cluster Launch Control").
 //
-// Backward: a unit is one valid 128-key block of one (sequence, head); all such
-// units cost about the same (each loops over the same query rows) but their
-// number varies per sequence, so empty blocks are never listed and the list is
-// dealt round-robin.  Units are enumerated sequence-major, then head, then
-// block, so the CTAs working at the same moment share Q and dO through L2
-// (same source, same section).
+// Backward: a unit is one valid 128-key block of one (sequence, head).  The
+// pages describe the backward tiles as near-equal in cost with a varying count,
+// so only valid blocks are listed and they are dealt round-robin, in an order
+// where neighbouring tiles reuse the same data in L2 (same source, same
+// section).  That holds for broadcast-Q, where every unit loops over the same
+// shared query rows.  In self-attention a unit loops over the query tiles of
+// its own sequence, so its cost grows with the sequence length; this planner
+// therefore sorts units by cost (stably: equal costs keep the enumeration order
+// sequence, head, block) and deals them in the same snake order as the
+// forward.  With equal costs that is the pages' enumeration, dealt back and
+// forth instead of strictly round-robin.
 //
 // Block-diagonal: BLOCK_PER_BATCH is the prefix sum of 64-token block counts;
 // programs receive balanced contiguous ranges from closed-form divmod
@@ -98,30 +103,42 @@ int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
 
 int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
-  int64_t n = 0;
-  for (int b = 0; b < batch; ++b) n += cdiv(static_cast<int64_t>(offsets[b + 1]) - offsets[b], kKvBlock) * H;
-  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
-  std::vector<int32_t> start(n_cta + 1, 0);
-  for (int c = 0; c < n_cta; ++c) {
-    const int64_t cnt = c < n ? (n - c + n_cta - 1) / n_cta : 0;
-    start[c + 1] = static_cast<int32_t>(start[c] + cnt);
+  struct U {
+    int32_t b, h, n, cost;
+  };
+  std::vector<U> all;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+    const int64_t rows = nq > 0 ? nq : L;
+    const int64_t q_tiles = cdiv(rows, kKvBlock);
+    for (int h = 0; h < H; ++h)
+      for (int64_t blk = 0; blk < cdiv(L, kKvBlock); ++blk)
+        all.push_back({b, h, static_cast<int32_t>(blk), static_cast<int32_t>(causal ? q_tiles - blk : q_tiles)});
   }
+  const int64_t n = static_cast<int64_t>(all.size());
+  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
+  // Equal costs (broadcast-Q) keep the enumeration order; unequal ones (self-
+  // attention, where a unit loops over its sequence's query tiles) are sorted
+  // largest first so the snake deal balances them.
+  std::stable_sort(all.begin(), all.end(), [](const U& x, const U& y) { return x.cost > y.cost; });
+  std::vector<int32_t> cta_of(n), count(n_cta, 0);
+  for (int64_t t = 0; t < n; ++t) {
+    const int64_t p = t / n_cta, r = t % n_cta;
+    const int32_t c = static_cast<int32_t>((p % 2 == 0) ? r : n_cta - 1 - r);
+    cta_of[t] = c;
+    ++count[c];
+  }
+  std::vector<int32_t> start(n_cta + 1, 0);
+  for (int c = 0; c < n_cta; ++c) start[c + 1] = start[c] + count[c];
   if (units) {
     units->assign(4 * n, 0);
-    int64_t u = 0;
-    for (int b = 0; b < batch; ++b) {
-      const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
-      const int64_t rows = nq > 0 ? nq : L;
-      const int64_t q_tiles = cdiv(rows, kKvBlock);
-      for (int h = 0; h < H; ++h)
-        for (int64_t blk = 0; blk < cdiv(L, kKvBlock); ++blk, ++u) {
-          const int64_t c = u % n_cta, k = u / n_cta;
-          const int64_t i = start[c] + k;
-          (*units)[4 * i + 0] = b;
-          (*units)[4 * i + 1] = h;
-          (*units)[4 * i + 2] = static_cast<int32_t>(blk);
-          (*units)[4 * i + 3] = static_cast<int32_t>(causal ? q_tiles - blk : q_tiles);
-        }
+    std::vector<int32_t> pos(start.begin(), start.end() - 1);
+    for (int64_t t = 0; t < n; ++t) {
+      const int64_t i = pos[cta_of[t]]++;
+      (*units)[4 * i + 0] = all[t].b;
+      (*units)[4 * i + 1] = all[t].h;
+      (*units)[4 * i + 2] = all[t].n;
+      (*units)[4 * i + 3] = all[t].cost;
     }
   }
   if (cta_start) *cta_start = start;
