@@ -72,7 +72,8 @@ typedef enum {
   JFA_ERR_WORKSPACE_TOO_SMALL = 4,
   JFA_ERR_ARCH = 5,                 /* current device is not compute capability 10.x */
   JFA_ERR_CUDA = 6,                 /* a CUDA runtime call or launch failed */
-  JFA_ERR_DEVICE_TIMEOUT = 7        /* a kernel wait ran out (see jfa_device_status) */
+  JFA_ERR_DEVICE_TIMEOUT = 7,       /* a kernel wait ran out (see jfa_device_status) */
+  JFA_ERR_TOO_LARGE = 8             /* jfa_fwd_noalloc: the plan exceeds its static scratch */
 } jfa_status;
 
 typedef enum { JFA_OP_FWD = 0, JFA_OP_BWD = 1, JFA_OP_BLOCK_FWD = 2, JFA_OP_BLOCK_BWD = 3 } jfa_op;
@@ -129,6 +130,28 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
                    void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
                    int max_len, int num_heads, int head_dim, float scale, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/*
+ * jfa_fwd_noalloc -- jfa_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.  Some callers cannot give
+ * the library a workspace: code inside a host framework whose memory manager
+ * owns all device memory and forbids extensions from calling cudaMalloc, or a
+ * serving loop that must never allocate.  This variant takes the same arguments
+ * as jfa_fwd minus the workspace and keeps its scratch (tile plan, error word,
+ * empty-sequence list) in one static device array of jfa_fwd_noalloc_capacity()
+ * bytes (1 MiB), held by every GPU that loads the library until the process
+ * exits.  A problem whose plan does not fit returns JFA_ERR_TOO_LARGE (about
+ * 60,000 forward units of 256 query rows).  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.  All calls share the array: calls that overlap on
+ * the GPU (different streams with no ordering) race, and the array keeps the
+ * last call's contents.  The first call on each device looks up the array's
+ * device address; make it before any stream capture.
+ */
+int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+                    const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
+                    int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* stream);
+/* Size in bytes of jfa_fwd_noalloc's static scratch array. */
+size_t jfa_fwd_noalloc_capacity(void);
 
 /*
  * jfa_workspace_size -- device workspace in bytes that `op` needs for this

@@ -191,6 +191,34 @@ static int validate_common(const void* q, const void* k, const void* v, const vo
 
 static int plan_ctas(const DeviceInfo& dev, int n_units) { return n_units < dev.num_sms ? n_units : dev.num_sms; }
 
+// ---------------------------------------------------------------- helpers for noalloc.cu
+// The same argument checks as jfa_fwd, then the device query; fills the row
+// counts and the SM count.
+int fwd_arg_checks(const void* q, const void* k, const void* v, const void* o, const int32_t* offsets_dev,
+                   const int32_t* offsets_host, int batch, int max_len, int nq, int H, int Hkv, int D, float scale,
+                   int causal, int broadcast_q, int* q_rows, int* kv_rows, int* o_rows, int* num_sms) {
+  Common c;
+  int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, H, Hkv, D, scale, causal,
+                           broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
+  *q_rows = c.q_rows;
+  *kv_rows = c.kv_rows;
+  *o_rows = c.o_rows;
+  *num_sms = c.dev.num_sms;
+  return JFA_OK;
+}
+
+// Zero output rows and -inf log-sum-exp for empty sequences in broadcast mode.
+int launch_fill_empty(const int32_t* empty_dev, int n_empty, int nq, int H, int D, int o_rows, void* o, float* lse,
+                      cudaStream_t stream) {
+  if (n_empty == 0) return JFA_OK;
+  fill_empty_broadcast_kernel<<<n_empty * nq, 256, 0, stream>>>(empty_dev, n_empty, nq, H, D, o_rows,
+                                                                 static_cast<__nv_bfloat16*>(o), lse);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
 }  // namespace jfa
 
 using namespace jfa;
@@ -205,6 +233,7 @@ extern "C" const char* jfa_status_string(int status) {
     case JFA_ERR_ARCH: return "device is not compute capability 10.x";
     case JFA_ERR_CUDA: return "CUDA error";
     case JFA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case JFA_ERR_TOO_LARGE: return "problem too large for the static scratch of jfa_fwd_noalloc";
     default: return "unknown status";
   }
 }

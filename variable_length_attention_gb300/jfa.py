@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libjfa.so")
 
 JFA_OP_FWD, JFA_OP_BWD, JFA_OP_BLOCK_FWD, JFA_OP_BLOCK_BWD = 0, 1, 2, 3
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_BAD_OFFSETS",
-          4: "JFA_ERR_WORKSPACE_TOO_SMALL", 5: "JFA_ERR_ARCH", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT"}
+          4: "JFA_ERR_WORKSPACE_TOO_SMALL", 5: "JFA_ERR_ARCH", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT",
+          8: "JFA_ERR_TOO_LARGE"}
 
 # exported symbols and their ctypes signatures
 _P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -35,6 +36,8 @@ SIGNATURES = {
     "jfa_plan_fwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "jfa_plan_bwd": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "block_plan": (_I, [_P, _I, _I, _I, _P, _P]),
+    "jfa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "jfa_fwd_noalloc_capacity": (_S, []),
     "jfa_profile_enable": (_I, [_I]),
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
@@ -253,3 +256,29 @@ def jfa_profile_read(kind) -> tuple[float, int]:
     ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
     _check("jfa_profile_read", load().jfa_profile_read(k, ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
+
+
+def jfa_fwd_noalloc(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False,
+                    scale=None, out=None, lse=None):
+    """jfa_fwd without a workspace, for callers that cannot allocate device
+    memory: the library's own fixed 1 MiB static scratch holds the plan.  Outputs
+    must still be supplied by the caller (or are allocated here by torch, for
+    convenience).  Calls that overlap on the GPU race on the shared scratch."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    bq = nq_broadcast > 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o_rows = batch * nq_broadcast if bq else int(offs_h[-1])
+    if out is None:
+        out = torch.empty((o_rows, H, D), dtype=torch.bfloat16, device=q.device)
+    st = L.jfa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
+                           offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv,
+                           D, float(scale), int(causal), int(bq), _stream())
+    _check("jfa_fwd_noalloc", st)
+    return out, lse
