@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "../../include/jfa.h"
+#include "block.h"
 #include "bwd.h"
 #include "host.h"
 #include "plan.h"
@@ -151,6 +152,17 @@ static BwdLayout bwd_layout(int n_units, int n_cta, int q_rows, int o_rows, int 
   return l;
 }
 
+struct BlockLayout {
+  size_t err = 0, bpb = 0, prog = 0, total = 0;
+};
+static BlockLayout block_layout(int batch, int n_prog) {
+  BlockLayout l;
+  l.bpb = 256;
+  l.prog = l.bpb + align256(static_cast<size_t>(batch + 1) * 4);
+  l.total = l.prog + align256(static_cast<size_t>(n_prog + 1) * 4);
+  return l;
+}
+
 __global__ void fill_empty_broadcast_kernel(const int32_t* empty_seq, int n_empty, int nq, int H, int D,
                                             int o_rows, __nv_bfloat16* o, float* lse) {
   // one block row per (empty sequence, query row); threads over H*D
@@ -255,6 +267,10 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
     const int q_rows = broadcast_q ? nq : offsets_host[batch];
     const int o_rows = broadcast_q ? batch * nq : offsets_host[batch];
     return bwd_layout(n, plan_ctas(dev, n), q_rows, o_rows, num_heads, head_dim).total;
+  }
+  if (op == JFA_OP_BLOCK_FWD || op == JFA_OP_BLOCK_BWD) {
+    const int P = plan_block(offsets_host, batch, num_heads, dev.num_sms, nullptr, nullptr);
+    return block_layout(batch, P).total;
   }
   return 0;
 }
@@ -401,14 +417,75 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   return launch_dq_convert(a, c.dev.num_sms);
 }
 
-extern "C" int block_attn_fwd(const void*, const void*, const void*, void*, const int32_t*, const int32_t*, int, int,
-                              int, int, float, void*, size_t, void*) {
-  return JFA_ERR_UNSUPPORTED;
+// Shared by the two block-diagonal entry points: checks, host plan, staging.
+static int block_common(const void* q, const void* k, const void* v, const void* out0, const int32_t* offsets_dev,
+                        const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream, BlockArgs* a) {
+  Common c;
+  int st = validate_common(q, k, v, out0, offsets_dev, offsets_host, batch, max_len, 0, num_heads, num_heads,
+                           head_dim, scale, 0, 0, &c);
+  if (st != JFA_OK) return st;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
+  std::vector<int32_t> bpb, prog;
+  const int P = plan_block(offsets_host, batch, num_heads, c.dev.num_sms, &bpb, &prog);
+  const BlockLayout lay = block_layout(batch, P);
+  if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
+  a->q = q;
+  a->k = k;
+  a->v = v;
+  a->offsets_dev = offsets_dev;
+  a->bpb = reinterpret_cast<const int32_t*>(ws + lay.bpb);
+  a->prog_start = reinterpret_cast<const int32_t*>(ws + lay.prog);
+  a->err = reinterpret_cast<int*>(ws + lay.err);
+  a->rows = c.kv_rows;
+  a->batch = batch;
+  a->H = num_heads;
+  a->D = head_dim;
+  a->n_blocks = bpb[batch];
+  a->n_prog = P;
+  a->scale = scale;
+  a->stream = stream;
+  if (P == 0) return JFA_OK;
+  std::vector<uint8_t> blob(lay.total - lay.bpb, 0);
+  std::memcpy(blob.data(), bpb.data(), bpb.size() * 4);
+  std::memcpy(blob.data() + (lay.prog - lay.bpb), prog.data(), prog.size() * 4);
+  return stage_to_device(ws + lay.bpb, blob.data(), blob.size(), stream);
 }
 
-extern "C" int block_attn_bwd(const void*, const void*, const void*, const void*, const void*, void*, void*, void*,
-                              const int32_t*, const int32_t*, int, int, int, int, float, void*, size_t, void*) {
-  return JFA_ERR_UNSUPPORTED;
+extern "C" int block_attn_fwd(const void* q, const void* k, const void* v, void* o, const int32_t* offsets_dev,
+                              const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim,
+                              float scale, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  BlockArgs a{};
+  int st = block_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
+                        workspace_bytes, stream, &a);
+  if (st != JFA_OK || a.n_prog == 0) return st;
+  a.o = o;
+  return launch_block_fwd(a);
+}
+
+extern "C" int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,
+                              void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                              int max_len, int num_heads, int head_dim, float scale, void* workspace,
+                              size_t workspace_bytes, void* stream_) {
+  (void)o;  // Di is formed inline as rowsum(P o dP); O itself is not read
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (offsets_host != nullptr && batch >= 0 && offsets_host[batch] > 0 &&
+      (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
+  BlockArgs a{};
+  int st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale,
+                        workspace, workspace_bytes, stream, &a);
+  if (st != JFA_OK || a.n_prog == 0) return st;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  return launch_block_bwd(a);
 }
 
 extern "C" int jfa_device_status(const void* workspace, void* stream) {

@@ -1,0 +1,608 @@
+// block.cu -- fixed 64-token block-diagonal attention for sm_103a.
+//
+// What it computes ("TLX Block Attention", sections 1 and 2.1): every sequence
+// is cut into blocks of 64 tokens (the last one may be shorter) and each block
+// attends only within itself.  Because a query block meets exactly one key
+// block, the score tile is complete after one GEMM: the row max and sum are
+// final at once, so there is no running-max correction, no stored log-sum-exp
+// and every accumulator starts fresh (use_acc = false).  The backward (section 4)
+// recomputes P from Q and K, forms Di = rowsum(P o dP) inline, and every block
+// owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
+//
+// Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
+// consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
+// rows 64-127 block 2p+1, and the off-diagonal quadrants of the 128 x 128 score
+// tile are masked.  That doubles the tensor work, which is free here: the kernel
+// moves ~33 FLOP per byte, far below the ridge, so it is bound by HBM
+// ("TLX Block Attention", section 3.3).  Persistent programs take balanced
+// contiguous ranges of (pair, head) tiles from the host plan, and find the
+// sequence of a global block by a branchless binary search over the per-batch
+// block prefix sums (section 5).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "block.h"
+#include "host.h"
+#include "profile.h"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace blk {
+
+constexpr int kBlk = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Params {
+  const int32_t* offsets;
+  const int32_t* bpb;         // [batch+1] prefix sums of blocks per sequence
+  const int32_t* prog_start;  // [P+1]
+  int* err;
+  __nv_bfloat16 *o, *dq, *dk, *dv;
+  int batch, H, n_blocks;
+  float scale, scale_log2;
+};
+
+// One 64-token block: first token row and length (0 if the block does not exist).
+struct Blk {
+  int row0, len;
+};
+
+__device__ __forceinline__ Blk locate(const Params& p, int g) {
+  Blk r{0, 0};
+  if (g >= p.n_blocks) return r;
+  // largest b in [0, batch) with bpb[b] <= g (branchless halving search)
+  int lo = 0, n = p.batch;
+  while (n > 1) {
+    const int half = n >> 1;
+    lo = (__ldg(p.bpb + lo + half) <= g) ? lo + half : lo;
+    n -= half;
+  }
+  const int j = g - __ldg(p.bpb + lo);
+  const int s = __ldg(p.offsets + lo);
+  const int L = __ldg(p.offsets + lo + 1) - s;
+  r.row0 = s + kBlk * j;
+  r.len = min(kBlk, L - kBlk * j);
+  return r;
+}
+
+template <int D>
+struct FwdCfg {
+  static constexpr int TILE = 128 * D * 2;         // 128 rows x D, bf16
+  static constexpr int CHUNK = 128 * 128;          // 64 columns x 128 rows
+  static constexpr int STAGE = 3 * TILE;           // Q, K, V
+  static constexpr int NST = D == 128 ? 2 : 4;
+  static constexpr int OFF_BAR = NST * STAGE;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
+};
+
+struct FwdBars {
+  uint64_t full[4], empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Loads rows [row0, row0+64) of every 64-column chunk of head h into rows
+// [64*half, 64*half+64) of a 128-row swizzled tile.
+template <int D>
+__device__ __forceinline__ void load_half(const CUtensorMap* tm, uint64_t* bar, uint8_t* tile, int half, int h, int row0) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) tma_load_2d(tm, bar, tile + c * 16384 + half * 8192, h * D + c * 64, row0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    block_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::OFF_BAR);
+  const int warp = warp_id(), lane = lane_id();
+  const int t0 = p.prog_start[blockIdx.x], t1 = p.prog_start[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 4);
+      mbar_init(&bars->o_full[b], 1);
+      mbar_init(&bars->t_free[b], 4);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Abort ab{&bars->abort_flag, p.err};
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- loader
+    for (int t = t0; t < t1; ++t) {
+      const int i = t - t0, st = i % C::NST;
+      if (!mbar_wait(&bars->empty[st], ((i / C::NST) & 1) ^ 1, ab)) break;
+      const int pair = t / p.H, h = t % p.H;
+      const Blk a = locate(p, 2 * pair);
+      Blk b = locate(p, 2 * pair + 1);
+      if (b.len == 0) b = a;  // nothing there: reload block a, masked later
+      uint8_t* base = smem + st * C::STAGE;
+      mbar_expect_tx(&bars->full[st], C::STAGE);
+      load_half<D>(&tm_q, &bars->full[st], base, 0, h, a.row0);
+      load_half<D>(&tm_q, &bars->full[st], base, 1, h, b.row0);
+      load_half<D>(&tm_k, &bars->full[st], base + C::TILE, 0, h, a.row0);
+      load_half<D>(&tm_k, &bars->full[st], base + C::TILE, 1, h, b.row0);
+      load_half<D>(&tm_v, &bars->full[st], base + 2 * C::TILE, 0, h, a.row0);
+      load_half<D>(&tm_v, &bars->full[st], base + 2 * C::TILE, 1, h, b.row0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, D, 0, 1);
+    const uint32_t sb = smem_u32(smem);
+    auto issue_s = [&](int i) {
+      const int st = i % C::NST, b = i & 1;
+      const uint32_t q = sb + st * C::STAGE, k = q + C::TILE;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + 256 * b, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_s, kk > 0);
+      }
+      mma_commit(&bars->s_full[b]);
+    };
+    auto issue_pv = [&](int i) {
+      const int st = i % C::NST, b = i & 1;
+      const uint32_t v = sb + st * C::STAGE + 2 * C::TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + 256 * b + 128, tmem + 256 * b + 8 * kk, sdesc_sw128(v + kk * 2048, C::CHUNK, 1024), id_o,
+               kk > 0);
+      mma_commit(&bars->o_full[b]);
+      mma_commit(&bars->empty[st]);
+    };
+    const int n = t1 - t0;
+    for (int i = 0; i <= n; ++i) {
+      if (i < n) {  // S of tile i, once its operands landed and its TMEM buffer is free
+        if (!mbar_wait(&bars->full[i % C::NST], (i / C::NST) & 1, ab)) break;
+        if (!mbar_wait(&bars->t_free[i & 1], ((i >> 1) & 1) ^ 1, ab)) break;
+        tc_fence_after();
+        issue_s(i);
+      }
+      if (i > 0) {  // PV of tile i-1
+        const int j = i - 1;
+        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, ab)) break;
+        tc_fence_after();
+        issue_pv(j);
+      }
+    }
+    mma_commit(&bars->drain);
+    const uint64_t tw = global_timer_ns();
+    while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int b = (warp - 4) >> 2;          // TMEM buffer / tile parity of this warpgroup
+    const int r = threadIdx.x & 127;        // row of the tile == TMEM lane
+    const int half = r >> 6;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + 256 * b;
+    const uint32_t tO = tS + 128;
+    const float sl2 = p.scale_log2;
+    for (int i = b; i < t1 - t0; i += 2) {
+      const int t = t0 + i;
+      const int pair = t / p.H, h = t % p.H;
+      const Blk blk = locate(p, 2 * pair + half);
+      const int rr = r & 63;
+      if (!mbar_wait(&bars->s_full[b], (i >> 1) & 1, ab)) goto done;
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(tS + 64 * half, sr);
+      tmem_ld32(tS + 64 * half + 32, sr + 32);
+      tmem_wait_ld();
+      reg_fence<64>(sr);
+      float s[64];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        s[c] = c < blk.len ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+        mx = fmaxf(mx, s[c]);
+      }
+      if (blk.len == 0) mx = 0.f;
+      float l = 0.f;
+      uint32_t pk[32], zero[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = ex2(s[c] - mx), p1 = ex2(s[c + 1] - mx);
+        l += p0 + p1;
+        pk[c / 2] = pack_bf16(p0, p1);
+        zero[c / 2] = 0u;
+      }
+      // P packed two per column: keys of this row's block, zeros elsewhere
+      tmem_st32(tS + 32 * half, pk);
+      tmem_st32(tS + 32 * (1 - half), zero);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (!mbar_wait(&bars->o_full[b], (i >> 1) & 1, ab)) goto done;
+      tc_fence_after();
+      const bool valid = rr < blk.len;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      __nv_bfloat16* dst = p.o + (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c, ov);
+        tmem_wait_ld();
+        reg_fence<32>(ov);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->t_free[b]);
+    }
+  }
+done:
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ backward
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int CHUNK = 128 * 128;
+  static constexpr int STAGE = 4 * TILE;            // Q, K, V, dO
+  static constexpr int NST = D == 128 ? 1 : 2;
+  static constexpr int OFF_P = NST * STAGE;         // P  [128 q][128 keys] bf16
+  static constexpr int OFF_DS = OFF_P + 32768;      // dS [128 q][128 keys] bf16
+  static constexpr int OFF_BAR = OFF_DS + 32768;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+};
+
+struct BwdBars {
+  uint64_t full[2], empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, acc_full, t_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Row q of a [128][128] bf16 tile stored as two swizzled 64-column boxes:
+// 16-byte piece j (columns 8j..8j+7) of box c.
+__device__ __forceinline__ void st_row_piece(uint8_t* tile, int q, int c, int j, const uint32_t* w) {
+  const uint32_t addr = smem_u32(tile + c * 16384 + q * 128 + ((j ^ (q & 7)) << 4));
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const Params p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
+  const int warp = warp_id(), lane = lane_id();
+  const int t0 = p.prog_start[blockIdx.x], t1 = p.prog_start[blockIdx.x + 1];
+  // TMEM columns: S (then dQ) [0,128), dP (then dK) [128,256), dV [256, 256+D)
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->ds_full, 4);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->t_free, 4);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Abort ab{&bars->abort_flag, p.err};
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- loader
+    for (int t = t0; t < t1; ++t) {
+      const int i = t - t0, st = i % C::NST;
+      if (!mbar_wait(&bars->empty[st], ((i / C::NST) & 1) ^ 1, ab)) break;
+      const int pair = t / p.H, h = t % p.H;
+      const Blk a = locate(p, 2 * pair);
+      Blk b = locate(p, 2 * pair + 1);
+      if (b.len == 0) b = a;
+      uint8_t* base = smem + st * C::STAGE;
+      mbar_expect_tx(&bars->full[st], C::STAGE);
+      const CUtensorMap* maps[4] = {&tm_q, &tm_k, &tm_v, &tm_do};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        load_half<D>(maps[m], &bars->full[st], base + m * C::TILE, 0, h, a.row0);
+        load_half<D>(maps[m], &bars->full[st], base + m * C::TILE, 1, h, b.row0);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
+    const uint32_t id_kv = idesc_bf16(128, D, 1, 1);    // dV = P^T dO, dK = dS^T Q
+    const uint32_t id_q = idesc_bf16(128, D, 0, 1);     // dQ = dS K
+    const uint32_t sP = smem_u32(smem + C::OFF_P), sDS = smem_u32(smem + C::OFF_DS);
+    for (int i = 0; i < t1 - t0; ++i) {
+      const int st = i % C::NST;
+      const uint32_t q = smem_u32(smem + st * C::STAGE), k = q + C::TILE, v = q + 2 * C::TILE, dO = q + 3 * C::TILE;
+      if (!mbar_wait(&bars->full[st], (i / C::NST) & 1, ab)) break;
+      if (!mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + COL_S, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_s, kk > 0);
+      }
+      mma_commit(&bars->s_full);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + COL_DP, sdesc_sw128(dO + off, 16, 1024), sdesc_sw128(v + off, 16, 1024), id_s, kk > 0);
+      }
+      mma_commit(&bars->dp_full);
+      // dV = P^T dO: A = P^T (P stored query-major: MN-major), B = dO (MN-major)
+      if (!mbar_wait(&bars->p_full, i & 1, ab)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + COL_DV, sdesc_sw128(sP + kk * 2048, C::CHUNK, 1024), sdesc_sw128(dO + kk * 2048, C::CHUNK, 1024),
+               id_kv, kk > 0);
+      // dK = dS^T Q into the dP columns, dQ = dS K into the S columns
+      if (!mbar_wait(&bars->ds_full, i & 1, ab)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + COL_DP, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(q + kk * 2048, C::CHUNK, 1024),
+               id_kv, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + COL_S, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(k + kk * 2048, C::CHUNK, 1024), id_q,
+               kk > 0);
+      }
+      mma_commit(&bars->acc_full);
+      mma_commit(&bars->empty[st]);
+    }
+    mma_commit(&bars->drain);
+    const uint64_t tw = global_timer_ns();
+    while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax, dS, epilogue
+    const int r = threadIdx.x & 127;
+    const int half = r >> 6, rr = r & 63;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint8_t* sP = smem + C::OFF_P;
+    uint8_t* sDS = smem + C::OFF_DS;
+    const float sl2 = p.scale_log2;
+    const uint32_t zero[4] = {0u, 0u, 0u, 0u};
+    for (int i = 0; i < t1 - t0; ++i) {
+      const int t = t0 + i;
+      const int pair = t / p.H, h = t % p.H;
+      const Blk blk = locate(p, 2 * pair + half);
+      if (!mbar_wait(&bars->s_full, i & 1, ab)) goto done;
+      tc_fence_after();
+      float pr[64];
+      {
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_addr + COL_S + 64 * half, sr);
+        tmem_ld32(tmem + lane_addr + COL_S + 64 * half + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence<64>(sr);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          pr[c] = c < blk.len ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+          mx = fmaxf(mx, pr[c]);
+        }
+        if (blk.len == 0) mx = 0.f;
+        float l = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          pr[c] = ex2(pr[c] - mx);
+          l += pr[c];
+        }
+        const float inv_l = (rr < blk.len && l > 0.f) ? 1.0f / l : 0.f;  // rows past the block: P = 0
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pr[c] *= inv_l;
+      }
+      // P row into shared memory (zeros in the other block's columns)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16(pr[8 * j + 2 * e], pr[8 * j + 2 * e + 1]);
+        st_row_piece(sP, r, half, j, w);
+        st_row_piece(sP, r, 1 - half, j, zero);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      // dS = P o (dP - Di), Di = rowsum(P o dP) over this block's keys
+      if (!mbar_wait(&bars->dp_full, i & 1, ab)) goto done;
+      tc_fence_after();
+      {
+        uint32_t dr[64];
+        tmem_ld32(tmem + lane_addr + COL_DP + 64 * half, dr);
+        tmem_ld32(tmem + lane_addr + COL_DP + 64 * half + 32, dr + 32);
+        tmem_wait_ld();
+        reg_fence<64>(dr);
+        float di = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) di = fmaf(pr[c], __uint_as_float(dr[c]), di);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * j + 2 * e;
+            w[e] = pack_bf16(pr[c] * (__uint_as_float(dr[c]) - di), pr[c + 1] * (__uint_as_float(dr[c + 1]) - di));
+          }
+          st_row_piece(sDS, r, half, j, w);
+          st_row_piece(sDS, r, 1 - half, j, zero);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+      // epilogue: row r is query r for dQ and key r for dK, dV (same block, same token)
+      if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
+      tc_fence_after();
+      {
+        const bool valid = rr < blk.len;
+        const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+#pragma unroll 1
+        for (int which = 0; which < 3; ++which) {
+          const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
+          const float mul = which == 2 ? 1.0f : p.scale;
+          __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + col + c, v);
+            tmem_wait_ld();
+            reg_fence<32>(v);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            if (valid) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->t_free);
+    }
+  }
+done:
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch_fwd_impl(const BlockArgs& a) {
+  using C = FwdCfg<D>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
+  CUtensorMap tq, tk, tv;
+  const uint64_t inner = static_cast<uint64_t>(a.H) * D;
+  int st = make_map_2d(&tq, a.q, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tk, a.k, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tv, a.v, inner, a.rows, 64, kBlk);
+  if (st != JFA_OK) return st;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return JFA_ERR_CUDA;
+    attr = true;
+  }
+  Params p{};
+  p.offsets = a.offsets_dev;
+  p.bpb = a.bpb;
+  p.prog_start = a.prog_start;
+  p.err = a.err;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.batch = a.batch;
+  p.H = a.H;
+  p.n_blocks = a.n_blocks;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  ProfileScope prof(kKindBlockFwd, a.stream);
+  block_fwd_kernel<D><<<a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+template <int D>
+int launch_bwd_impl(const BlockArgs& a) {
+  using C = BwdCfg<D>;
+  static_assert(C::SMEM <= 232448, "shared memory budget");
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t inner = static_cast<uint64_t>(a.H) * D;
+  int st = make_map_2d(&tq, a.q, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tk, a.k, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tv, a.v, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, inner, a.rows, 64, kBlk);
+  if (st != JFA_OK) return st;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return JFA_ERR_CUDA;
+    attr = true;
+  }
+  Params p{};
+  p.offsets = a.offsets_dev;
+  p.bpb = a.bpb;
+  p.prog_start = a.prog_start;
+  p.err = a.err;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.batch = a.batch;
+  p.H = a.H;
+  p.n_blocks = a.n_blocks;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  ProfileScope prof(kKindBlockBwd, a.stream);
+  block_bwd_kernel<D><<<a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // namespace blk
+
+int launch_block_fwd(const BlockArgs& a) {
+  return a.D == 128 ? blk::launch_fwd_impl<128>(a) : blk::launch_fwd_impl<64>(a);
+}
+int launch_block_bwd(const BlockArgs& a) {
+  return a.D == 128 ? blk::launch_bwd_impl<128>(a) : blk::launch_bwd_impl<64>(a);
+}
+
+}  // namespace jfa

@@ -1,0 +1,24 @@
+// block.h -- launchers of the block-diagonal kernels (see block.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace jfa {
+
+struct BlockArgs {
+  const void *q, *k, *v, *dout;
+  void *o, *dq, *dk, *dv;
+  const int32_t* offsets_dev;
+  const int32_t* bpb;         // device, [batch+1]
+  const int32_t* prog_start;  // device, [n_prog+1]
+  int* err;
+  int rows, batch, H, D, n_blocks, n_prog;
+  float scale;
+  cudaStream_t stream;
+};
+
+int launch_block_fwd(const BlockArgs& a);
+int launch_block_bwd(const BlockArgs& a);
+
+}  // namespace jfa
