@@ -62,6 +62,22 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int) -> float:
+    """Largest value of x over all ranks (the slowest rank sets the job time)."""
+    if ws <= 1:
+        return float(x)
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_flops: float, steps: int, max_ms: float, ws: int) -> float:
+    """Whole-job TFLOP/s: every rank runs the same step (weak scaling)."""
+    return ws * step_flops * steps / (max_ms * 1e-3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -282,14 +298,9 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in evs]
     prof = {kind: V.jfa_profile_read(kind) for kind in V.jfa.KERNEL_KINDS}
     V.jfa_profile_enable(False)
-    total_ms = float(sum(step_ms))
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), ws)
     ms_per_step = total_ms / args.steps
-    value = ws * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(step_flops, args.steps, total_ms, ws)
 
     # ---------------------------------------------------------------- e2e through host buffers
     o_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for _, o, _, dq, dk, dv, _ in outs
@@ -318,13 +329,8 @@ def main():
         b.record()
         torch.cuda.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e_total = float(sum(e_ms))
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_total = float(t.item())
-    e2e_value = ws * step_flops * args.steps / (e_total * 1e-3) / 1e12
+    e_total = max_over_ranks(float(sum(e_ms)), ws)
+    e2e_value = job_throughput(step_flops, args.steps, e_total, ws)
 
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, peak_src = _peaks()
