@@ -197,6 +197,21 @@ int block_plan(const int32_t* offsets_host, int batch, int num_heads, int n_sm, 
                int32_t* prog_start);
 
 /*
+ * Work distribution of the persistent jagged forward [R "Tile balancing and
+ * Cluster Launch Control"; C "load balancing"].
+ *   0  static plan: units sorted by cost and snake-dealt to one CTA per SM;
+ *   1  Cluster Launch Control: one CTA per unit, launched in cost order; a CTA
+ *      that finishes a unit cancels the launch of a CTA that has not started
+ *      yet and processes that CTA's unit instead, so residual imbalance is
+ *      absorbed at run time.
+ * The initial mode comes from the environment variable JFA_SCHED ("static" or
+ * "clc"), else the library default; jfa_set_schedule() changes it for
+ * subsequent calls (process-wide).  jfa_get_schedule() returns the mode in use.
+ */
+int jfa_set_schedule(int mode);
+int jfa_get_schedule(void);
+
+/*
  * Optional kernel timing (no counterpart on the pages; measurement support).
  * jfa_profile_enable(1) starts bracketing every library kernel launch with CUDA
  * events on its stream (and forgets earlier records); jfa_profile_enable(0)

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -203,6 +204,18 @@ static int validate_common(const void* q, const void* k, const void* v, const vo
 
 static int plan_ctas(const DeviceInfo& dev, int n_units) { return n_units < dev.num_sms ? n_units : dev.num_sms; }
 
+static std::atomic<int> g_sched_mode{-1};
+
+int sched_mode() {
+  int m = g_sched_mode.load(std::memory_order_relaxed);
+  if (m < 0) {
+    const char* e = std::getenv("JFA_SCHED");
+    m = (e != nullptr && std::strcmp(e, "static") == 0) ? 0 : (e != nullptr && std::strcmp(e, "clc") == 0 ? 1 : kDefaultSched);
+    g_sched_mode.store(m, std::memory_order_relaxed);
+  }
+  return m;
+}
+
 // ---------------------------------------------------------------- helpers for noalloc.cu
 // The same argument checks as jfa_fwd, then the device query; fills the row
 // counts and the SM count.
@@ -292,8 +305,10 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   std::vector<int32_t> units, cta_start;
   const int n_probe = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
   const int n_cta = plan_ctas(c.dev, n_probe);
+  const int clc = sched_mode();
   int n = 0;
-  if (n_cta > 0) n = plan_fwd(offsets_host, batch, num_heads, nq, causal, n_cta, &units, &cta_start);
+  // Cluster Launch Control takes the units in plain cost order (the plan dealt to one CTA)
+  if (n_cta > 0) n = plan_fwd(offsets_host, batch, num_heads, nq, causal, clc ? 1 : n_cta, &units, &cta_start);
   std::vector<int32_t> empty;
   if (broadcast_q)
     for (int b = 0; b < batch; ++b)
@@ -341,6 +356,8 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
   a.n_cta = n_cta;
+  a.n_units = n;
+  a.use_clc = clc;
   a.err = reinterpret_cast<int*>(ws + lay.err);
   a.stream = stream;
   return launch_fwd(a);
@@ -487,6 +504,14 @@ extern "C" int block_attn_bwd(const void* q, const void* k, const void* v, const
   a.dv = dv;
   return launch_block_bwd(a);
 }
+
+extern "C" int jfa_set_schedule(int mode) {
+  if (mode != 0 && mode != 1) return JFA_ERR_INVALID_ARG;
+  g_sched_mode.store(mode, std::memory_order_relaxed);
+  return JFA_OK;
+}
+
+extern "C" int jfa_get_schedule(void) { return sched_mode(); }
 
 extern "C" int jfa_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return JFA_ERR_INVALID_ARG;

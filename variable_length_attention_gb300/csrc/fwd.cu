@@ -60,9 +60,11 @@ struct Params {
   float* lse;
   const int32_t* offsets;
   const int4* units;
-  const int32_t* cta_start;
+  const int32_t* cta_start;  // static plan: CTA c takes units [cta_start[c], cta_start[c+1])
   int* err;
   int H, Hkv, nq, o_rows;
+  int n_units;
+  int use_clc;               // 1: one CTA per unit in cost order, idle CTAs claim pending ones
   float scale_log2;
 };
 
@@ -118,11 +120,32 @@ struct Bars {
   uint64_t drain;
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
+  // unit schedule: the loader publishes each unit index (or -1 at the end) to
+  // every role through this ring
+  uint64_t sched_full[4], sched_empty[4], clc_bar;
+  int4 clc_resp;
+  int sched_unit[4];
   float stat_m[2][BM];
   float stat_l[2][BM];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+constexpr int kSchedConsumers = 13;  // MMA thread + 8 softmax warps + 4 epilogue warps
+
+// Next unit index from the schedule ring; -1 at the end, -2 if the CTA aborts.
+__device__ __forceinline__ int sched_pop(Bars* bars, uint32_t it, const Abort& ab, bool per_warp) {
+  const int slot = it & 3;
+  if (!mbar_wait(&bars->sched_full[slot], (it >> 2) & 1, ab)) return -2;
+  const int ui = *reinterpret_cast<volatile int*>(&bars->sched_unit[slot]);
+  if (per_warp) {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(&bars->sched_empty[slot]);
+  } else {
+    mbar_arrive(&bars->sched_empty[slot]);
+  }
+  return ui;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,10 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int u_begin = p.cta_start[blockIdx.x];
-  const int u_end = p.cta_start[blockIdx.x + 1];
+  const int u_begin = p.use_clc ? 0 : p.cta_start[blockIdx.x];
+  const int u_end = p.use_clc ? 0 : p.cta_start[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->sched_full[s], 1);
+      mbar_init(&bars->sched_empty[s], kSchedConsumers);
+    }
+    mbar_init(&bars->clc_bar, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->q_full[t], 1);
       mbar_init(&bars->s_full[t], 1);
@@ -180,7 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_addr + 256 + t * 128;
     const float sl2 = p.scale_log2;
     uint32_t s_phase = 0, st_phase = 0;
-    for (int ui = u_begin; ui < u_end; ++ui) {
+    for (uint32_t it = 0;; ++it) {
+      const int ui = sched_pop(bars, it, ab, true);
+      if (ui == -2) goto done;
+      if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
       const int qi = 2 * BM * u.m + BM * t + row;  // query index inside the sequence / shared Q
       float m_run = -INFINITY, l_run = 0.f;
@@ -256,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t phase = 0;
-    for (int ui = u_begin; ui < u_end; ++ui) {
+    for (uint32_t it = 0;; ++it) {
+      const int ui = sched_pop(bars, it, ab, true);
+      if (ui == -2) goto done;
+      if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
       for (int t = 0; t < 2; ++t) {
         if (!mbar_wait(&bars->o_full[t], phase, ab)) goto done;
@@ -321,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + 256 + t * 128, tmem + t * BN + k * 8, sdesc_sw128(va + k * 2048, C::CHUNK_BYTES, 1024),
                  idesc_o, (acc || k > 0) ? 1u : 0u);
       };
-      for (int ui = u_begin; ui < u_end; ++ui) {
+      for (uint32_t it = 0;; ++it) {
+        const int ui = sched_pop(bars, it, ab, false);
+        if (ui < 0) break;
         const Unit u = decode<CAUSAL>(p, ui);
         if (!mbar_wait(&bars->q_full[0], u_phase, ab)) goto mma_done;
         if (!mbar_wait(&bars->q_full[1], u_phase, ab)) goto mma_done;
@@ -382,10 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 13 && lane == 0) {
-      // ------------------------------------------------------------ TMA loader
+      // ------------------------------------------------------------ TMA loader + scheduler
+      // Static plan: this CTA's slice of the list.  Cluster Launch Control: the
+      // CTA starts with its own index and, while loading a unit, asks the
+      // hardware for a CTA that has not launched yet and takes over its unit
+      // (aixai.ru summary, "Tile balancing and Cluster Launch Control").
       uint32_t kv_it = 0, u_phase = 0;
-      for (int ui = u_begin; ui < u_end; ++ui) {
-        const Unit u = decode<CAUSAL>(p, ui);
+      int cur = p.use_clc ? static_cast<int>(blockIdx.x) : (u_begin < u_end ? u_begin : -1);
+      for (uint32_t it = 0;; ++it) {
+        const int slot = it & 3;
+        if (!mbar_wait(&bars->sched_empty[slot], ((it >> 2) & 1) ^ 1, ab)) break;
+        bars->sched_unit[slot] = cur;
+        mbar_arrive(&bars->sched_full[slot]);
+        if (cur < 0) break;
+        if (p.use_clc) {
+          mbar_expect_tx(&bars->clc_bar, 16);
+          clc_try_cancel(&bars->clc_resp, &bars->clc_bar);
+        }
+        const Unit u = decode<CAUSAL>(p, cur);
         if (!mbar_wait(&bars->q_empty, u_phase ^ 1, ab)) break;
         for (int t = 0; t < 2; ++t) {
           mbar_expect_tx(&bars->q_full[t], C::TILE_BYTES);
@@ -413,6 +463,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         u_phase ^= 1;
+        int nxt;
+        if (p.use_clc) {
+          if (!mbar_wait(&bars->clc_bar, it & 1, ab)) break;
+          nxt = clc_cancelled_x(&bars->clc_resp);
+          if (nxt >= p.n_units) nxt = -1;
+        } else {
+          nxt = cur + 1 < u_end ? cur + 1 : -1;
+        }
+        cur = nxt;
       }
       if (*ab.flag) {
         // aborting: let copies already in flight land before the CTA exits
@@ -458,8 +517,10 @@ int launch_impl(const FwdArgs& a) {
   p.nq = a.nq;
   p.o_rows = a.o_rows;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.n_units = a.n_units;
+  p.use_clc = a.use_clc;
   ProfileScope prof(kKindFwd, a.stream);
-  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, p);
+  kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

@@ -38,11 +38,19 @@ struct FwdArgs {
   float scale;
   int causal;
   const int32_t* units;         // device, 4 ints per unit
-  const int32_t* cta_start;     // device, n_cta + 1
-  int n_cta;
+  const int32_t* cta_start;     // device, n_cta + 1 (static plan only)
+  int n_cta;                    // static plan: CTAs launched
+  int n_units;
+  int use_clc;                  // 1: launch n_units CTAs, units in cost order, Cluster Launch Control
   int* err;                     // device error word
   cudaStream_t stream;
 };
 int launch_fwd(const FwdArgs& a);
+
+// Scheduling mode of the persistent jagged kernels: 0 static plan, 1 Cluster
+// Launch Control.  Initially JFA_SCHED ("static" or "clc") if set, else
+// kDefaultSched; jfa_set_schedule() changes it.
+constexpr int kDefaultSched = 1;  // measured faster on every jagged workload
+int sched_mode();
 
 }  // namespace jfa

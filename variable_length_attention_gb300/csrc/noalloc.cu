@@ -137,6 +137,8 @@ extern "C" int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void
   a.units = reinterpret_cast<const int32_t*>(ws + off_units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + off_cta);
   a.n_cta = n_cta;
+  a.n_units = static_cast<int>(units.size() / 4);
+  a.use_clc = 0;  // always the static plan here
   a.err = reinterpret_cast<int*>(ws);
   a.stream = stream;
   return launch_fwd(a);

@@ -38,6 +38,8 @@ SIGNATURES = {
     "block_plan": (_I, [_P, _I, _I, _I, _P, _P]),
     "jfa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "jfa_fwd_noalloc_capacity": (_S, []),
+    "jfa_set_schedule": (_I, [_I]),
+    "jfa_get_schedule": (_I, []),
     "jfa_profile_enable": (_I, [_I]),
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
@@ -243,6 +245,17 @@ def block_plan(offsets_host, num_heads, n_sm):
     L.block_plan(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, n_sm,
                  bpb.ctypes.data_as(ctypes.c_void_p), ps.ctypes.data_as(ctypes.c_void_p))
     return bpb, ps
+
+
+def jfa_set_schedule(mode):
+    """Work distribution of the jagged forward: 0 / "static" (host plan, one CTA
+    per SM) or 1 / "clc" (Cluster Launch Control)."""
+    m = {"static": 0, "clc": 1}.get(mode, mode)
+    _check("jfa_set_schedule", load().jfa_set_schedule(int(m)))
+
+
+def jfa_get_schedule() -> int:
+    return load().jfa_get_schedule()
 
 
 def jfa_profile_enable(on: bool = True):
