@@ -44,6 +44,10 @@ def _args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["jagged", "broadcast", "dense", "block"], default="jagged",
+                    help="jagged (default) is the headline step; the others are diagnostic lines")
+    ap.add_argument("--block-batch", type=int, default=1152)
+    ap.add_argument("--head-dim", type=int, default=128)
     return ap.parse_args()
 
 
@@ -246,34 +250,12 @@ def main():
         run_reference(args, ws, rank)
         return
     import variable_length_attention_gb300 as V
-    from variable_length_attention_gb300 import workloads as W
 
     assert torch.cuda.is_available(), "bench.py needs a GPU"
     dev = torch.device("cuda", local)
-    wls = _workloads()
-    w = wls[0]
-    # identical inputs for both variants (same seeds); generated on the host, then resident in HBM
-    hq, hk, hv, hdo = [t.pin_memory() for t in w.tensors("cpu")]
-    q, k, v, do = [t.to(dev) for t in (hq, hk, hv, hdo)]
-    offs_h = w.offsets
-    offs = torch.from_numpy(offs_h).to(dev)
-    outs = []
-    for wl in wls:
-        o = torch.empty_like(q)
-        lse = torch.empty((w.num_heads, w.total_tokens), dtype=torch.float32, device=dev)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        need = max(V.jfa_workspace_size(0, offs_h, w.batch, 0, w.num_heads, w.head_dim, wl.causal, 0),
-                   V.jfa_workspace_size(1, offs_h, w.batch, 0, w.num_heads, w.head_dim, wl.causal, 0))
-        wsb = torch.empty(need, dtype=torch.uint8, device=dev)
-        outs.append((wl, o, lse, dq, dk, dv, wsb))
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
-    fl = [W.flops(wl) for wl in wls]
-    step_flops = float(sum(f + b for f, b in fl))
-
-    def step(qq, kk, vv, dd):
-        for wl, o, lse, dq, dk, dv, wsb in outs:
-            V.jfa_fwd(qq, kk, vv, offs, offs_h, causal=wl.causal, out=o, lse=lse, workspace=wsb)
-            V.jfa_bwd(qq, kk, vv, o, dd, lse, offs, offs_h, causal=wl.causal, dq=dq, dk=dk, dv=dv, workspace=wsb)
+    job = build_job(args, dev)
+    step, flush = job["step"], torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+    step_flops = float(sum(job["flops"].values()))
 
     def barrier():
         if ws > 1:
@@ -282,7 +264,7 @@ def main():
         torch.cuda.synchronize()
 
     for _ in range(max(args.warmup, 3)):
-        step(q, k, v, do)
+        step(job["dev_inputs"])
     barrier()
     # ---------------------------------------------------------------- timed region (device)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -292,7 +274,7 @@ def main():
         for i in range(args.steps):
             flush.zero_()  # L2 flush between timed steps, outside the events
             evs[i][0].record()
-            step(q, k, v, do)
+            step(job["dev_inputs"])
             evs[i][1].record()
         barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -303,74 +285,157 @@ def main():
     value = job_throughput(step_flops, args.steps, total_ms, ws)
 
     # ---------------------------------------------------------------- e2e through host buffers
-    o_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for _, o, _, dq, dk, dv, _ in outs
-           for t in (o, dq, dk, dv)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + offs_h.nbytes
-    d2h = sum(t.numel() * t.element_size() for t in o_h)
+    e2e = None
+    host_in = job["host_inputs"]
+    if host_in is not None:
+        outs = job["outputs"]
+        o_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in) + job["offsets_bytes"]
+        d2h = sum(t.numel() * t.element_size() for t in o_h)
 
-    def e2e_step():
-        qq, kk, vv, dd = [t.to(dev, non_blocking=True) for t in (hq, hk, hv, hdo)]
-        step(qq, kk, vv, dd)
-        i = 0
-        for _, o, _, dq, dk, dv, _ in outs:
-            for t in (o, dq, dk, dv):
-                o_h[i].copy_(t, non_blocking=True)
-                i += 1
+        def e2e_step():
+            step([t.to(dev, non_blocking=True) for t in host_in])
+            for dst, src in zip(o_h, outs):
+                dst.copy_(src, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e_ms = []
-    for i in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        e2e_step()
-        b.record()
-        torch.cuda.synchronize()
-        e_ms.append(a.elapsed_time(b))
-    e_total = max_over_ranks(float(sum(e_ms)), ws)
-    e2e_value = job_throughput(step_flops, args.steps, e_total, ws)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e_ms = []
+        for i in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            e2e_step()
+            b.record()
+            torch.cuda.synchronize()
+            e_ms.append(a.elapsed_time(b))
+        e_total = max_over_ranks(float(sum(e_ms)), ws)
+        e2e = {"value": job_throughput(step_flops, args.steps, e_total, ws), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, peak_src = _peaks()
     kind_ms = {k: v[0] for k, v in prof.items()}
-    dominant = max(kind_ms, key=kind_ms.get)
-    bwd_ms, bwd_n = prof["bwd_main"]
-    fwd_ms, fwd_n = prof["fwd"]
-    bwd_flops = args.steps * sum(b for _, b in fl)
-    fwd_flops = args.steps * sum(f for f, _ in fl)
-    achieved = bwd_flops / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None
-    peak = peaks["bf16_tflops"]
-    traffic = _traffic()
-    roofline = {"kernel": "bwd_main", "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": (achieved / peak) if achieved else None, "peak_source": f"{peak_src} bf16 burst",
-                "traffic": traffic, "launches": bwd_n, "avg_launch_ms": bwd_ms / max(bwd_n, 1),
-                "dominant_by_time": dominant}
-    launches = int(sum(n for _, n in prof.values()))
-
+    dom = job["dominant"]
+    dom_ms, dom_n = prof[dom]
+    if job["bound"] == "tensor":
+        achieved = args.steps * job["flops"][dom] / (dom_ms * 1e-3) / 1e12 if dom_ms > 0 else None
+        peak, unit, psrc = peaks["bf16_tflops"], "TFLOP/s", f"{peak_src} bf16 burst"
+    else:
+        achieved = args.steps * job["bytes"][dom] / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
+        peak, unit, psrc = peaks["hbm_gbs"], "GB/s", f"{peak_src} HBM copy"
+    roofline = {"kernel": dom, "bound": job["bound"], "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": (achieved / peak) if achieved else None, "peak_source": psrc,
+                "traffic": _traffic() if args.workload == "jagged" else None, "launches": dom_n,
+                "avg_launch_ms": dom_ms / max(dom_n, 1), "dominant_by_time": max(kind_ms, key=kind_ms.get)}
+    per_kind = {k: args.steps * f / (kind_ms[k] * 1e-3) / 1e12 for k, f in job["flops"].items() if kind_ms.get(k)}
     clocks = clk.summary()
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name + " fwd+bwd, non-causal and causal", "batch": w.batch,
-                       "heads": w.num_heads, "head_dim": w.head_dim, "tokens": w.total_tokens,
-                       "max_len": w.max_len, "parallelism": f"replicas x{ws}",
-                       "l2": "flushed (256 MiB write) before every timed step, outside the events"},
-            "pct_of_peak": value / ws / peak * 100.0,
-            "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
-            "bwd_tflops": achieved,
+            "config": dict(job["config"], parallelism=f"replicas x{ws}",
+                           l2="flushed (256 MiB write) before every timed step, outside the events"),
+            "pct_of_peak": value / ws / peaks["bf16_tflops"] * 100.0,
+            "kernel_tflops": per_kind,
             "kernel_ms": {k: v for k, v in kind_ms.items() if v > 0},
-            "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h)}}
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            "roofline": roofline, "clocks": clocks, "gpu_launches": int(sum(n for _, n in prof.values())),
+            "e2e": e2e}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == "jagged":
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def build_job(args, dev):
+    """Inputs, outputs and the step function of one workload."""
+    import variable_length_attention_gb300 as V
+    from variable_length_attention_gb300 import workloads as W
+
+    def nbytes(ts):
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    if args.workload in ("jagged", "broadcast", "dense"):
+        wls = {"jagged": [W.jagged(False), W.jagged(True)], "broadcast": [W.broadcast()],
+               "dense": [W.dense(False), W.dense(True)]}[args.workload]
+        w = wls[0]
+        host = [t.pin_memory() for t in w.tensors("cpu")]
+        dev_in = [t.to(dev) for t in host]
+        offs_h = w.offsets
+        offs = torch.from_numpy(offs_h).to(dev)
+        calls, outputs = [], []
+        for wl in wls:
+            kv_heads = wl.num_kv_heads
+            extra = None
+            if kv_heads != w.num_kv_heads:  # GQA forward: its own K, V with fewer heads
+                g = wl.tensors("cpu")
+                extra = [g[1].to(dev), g[2].to(dev)]
+            o = torch.empty((wl.o_rows, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((wl.num_heads, wl.o_rows), dtype=torch.float32, device=dev)
+            grads = None
+            if wl.bwd:
+                grads = (torch.empty_like(dev_in[0]), torch.empty_like(dev_in[1]), torch.empty_like(dev_in[2]))
+                outputs += [o, *grads]
+            else:
+                outputs.append(o)
+            need = max(V.jfa_workspace_size(0, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
+                                            wl.nq > 0),
+                       V.jfa_workspace_size(1, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
+                                            wl.nq > 0) if wl.bwd else 0)
+            calls.append((wl, o, lse, grads, extra, torch.empty(need, dtype=torch.uint8, device=dev)))
+
+        def step(inp):
+            q, k, v, do = inp
+            for wl, o, lse, grads, extra, wsb in calls:
+                kk, vv = (extra[0], extra[1]) if extra is not None else (k, v)
+                V.jfa_fwd(q, kk, vv, offs, offs_h, causal=wl.causal, nq_broadcast=wl.nq, out=o, lse=lse,
+                          workspace=wsb)
+                if grads is not None:
+                    V.jfa_bwd(q, kk, vv, o, do, lse, offs, offs_h, causal=wl.causal, nq_broadcast=wl.nq,
+                              dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+
+        fl = [W.flops(wl) for wl in wls]
+        flops = {"fwd": float(sum(f for f, _ in fl)),
+                 "bwd_main": float(sum(b for (_, b), wl in zip(fl, wls) if wl.bwd))}
+        suffix = {"jagged": " fwd+bwd, non-causal and causal", "broadcast": " fwd+bwd",
+                  "dense": " fwd+bwd, plus the GQA 16/4 forward"}[args.workload]
+        cfg = {"workload": w.name + suffix, "batch": w.batch, "heads": w.num_heads, "head_dim": w.head_dim,
+               "tokens": w.total_tokens, "max_len": w.max_len}
+        if w.nq:
+            cfg["nq_broadcast"] = w.nq
+        return {"step": step, "dev_inputs": dev_in, "host_inputs": host, "outputs": outputs,
+                "offsets_bytes": offs_h.nbytes, "flops": flops, "bytes": {}, "dominant": "bwd_main",
+                "bound": "tensor", "config": cfg}
+
+    # block-diagonal: inputs drawn on the device (the full workload is 4.8 GB per tensor)
+    w = W.block(args.head_dim, batch=args.block_batch)
+    dev_in = list(w.tensors(str(dev)))
+    offs_h = w.offsets
+    offs = torch.from_numpy(offs_h).to(dev)
+    o = torch.empty_like(dev_in[0])
+    grads = [torch.empty_like(dev_in[i]) for i in range(3)]
+    wsb = torch.empty(V.jfa_workspace_size(2, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
+                      dtype=torch.uint8, device=dev)
+
+    def step(inp):
+        q, k, v, do = inp
+        V.block_attn_fwd(q, k, v, offs, offs_h, out=o, workspace=wsb)
+        V.block_attn_bwd(q, k, v, o, do, offs, offs_h, dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+
+    f, b = W.flops(w)
+    t_bytes = dev_in[0].numel() * 2
+    host = None
+    if 4 * t_bytes <= (4 << 30):  # e2e only when the inputs fit a modest pinned host buffer
+        host = [t.cpu().pin_memory() for t in dev_in]
+    return {"step": step, "dev_inputs": dev_in, "host_inputs": host, "outputs": [o] + grads,
+            "offsets_bytes": offs_h.nbytes, "flops": {"block_fwd": float(f), "block_bwd": float(b)},
+            "bytes": {"block_fwd": 4.0 * t_bytes, "block_bwd": 7.0 * t_bytes}, "dominant": "block_bwd",
+            "bound": "hbm",
+            "config": {"workload": w.name + " fwd+bwd", "batch": w.batch, "heads": w.num_heads,
+                       "head_dim": w.head_dim, "tokens": w.total_tokens, "block": 64}}
 
 
 if __name__ == "__main__":
