@@ -29,10 +29,11 @@
 //   warp 12          tcgen05 MMA issuer
 //   warp 13          loader: K, V by TMA once per unit; per query tile Q and dO by
 //                    TMA into a 2-deep ring, and L, Di into shared memory
-// TMEM: S^T [0,128) (P^T overwrites columns 0-31 and 64-95; dQ reuses [0,D)),
-//       dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
-// Per tile the tensor core runs dP^T = V dO^T, S^T = K Q^T, dV += P^T dO,
-// dK += dS^T Q, dQ = dS K.
+// TMEM: two 128-column regions that S^T and dP^T swap every tile (P^T overwrites
+// columns 0-31 and 64-95 of S^T's region; that tile's dQ then reuses the region),
+// dV [256,256+D), dK [256+D, 256+2D).
+// Per tile the tensor core runs S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
+// dK += dS^T Q, dQ = dS K; the next S^T never waits for the dQ drain.
 // Masks: keys past the sequence end and query rows past it are zeroed per thread
 // (a key flag and L = +inf), so only the causal diagonal tile needs an
 // element-wise mask, and it is peeled into its own code path.
@@ -118,6 +119,10 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
   return u;
 }
 
+// TMEM column of this tile's S^T (and later of its dQ); dP^T takes the other
+// 128-column region.  The two swap every tile.
+__device__ __forceinline__ uint32_t region_s(uint32_t tile_counter) { return (tile_counter & 1) ? 128u : 0u; }
+
 struct Bars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
@@ -186,9 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;              // query half
     const int k = threadIdx.x & 127;       // key row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + 64 * wg;          // S^T columns of this half
-    const uint32_t tP = tmem + lane_addr + 64 * wg;          // P^T packed (32 columns)
-    const uint32_t tDP = tmem + lane_addr + 128 + 64 * wg;
     uint8_t* sDS = smem + C::OFF_DS + wg * C::CHUNK + k * 128;  // row k of this half's box
     const float sl2 = p.scale_log2;
     uint32_t ph = 0, ds_ph = 0, dkv_ph = 0, q_it = 0;
@@ -199,9 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = q_it & 1;
         const float* lse_s = s_lse + st * 128 + 64 * wg;
         const float* di_s = s_di + st * 128 + 64 * wg;
+        // S^T and dP^T swap TMEM regions every tile (see the MMA issuer)
+        const uint32_t rs = region_s(q_it), rd = 128 - rs;
+        const uint32_t tS = tmem + lane_addr + rs + 64 * wg;   // S^T columns of this half
+        const uint32_t tP = tS;                                // P^T packed (32 columns)
+        const uint32_t tDP = tmem + lane_addr + rd + 64 * wg;
         if (!mbar_wait(&bars->s_full, ph, ab)) goto done;
-        if (!mbar_wait(&bars->dp_full, ph, ab)) goto done;
-        ph ^= 1;
         tc_fence_after();
         const bool diag = CAUSAL && i == u.n;
         // P^T first: the dV MMA can start while dS^T is being formed
@@ -237,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this rarely waits)
         if (!mbar_wait(&bars->ds_empty, ds_ph ^ 1, ab)) goto done;
         ds_ph ^= 1;
+        if (!mbar_wait(&bars->dp_full, ph, ab)) goto done;
+        ph ^= 1;
+        tc_fence_after();
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
           uint32_t dr[32];
@@ -302,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<144>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tQ = tmem + lane_addr;
-    uint32_t ph = 0;
+    uint32_t ph = 0, q_it = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
-      for (int i = u.i0; i < u.i1; ++i) {
+      for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+        const uint32_t tQ = tmem + lane_addr + region_s(q_it);  // dQ sits where this tile's S^T was
         if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
         ph ^= 1;
         tc_fence_after();
@@ -353,14 +361,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sDO = sQ + C::TILE;
             if (!mbar_wait(&bars->q_full[st], (q_it >> 1) & 1, ab)) goto mma_done;
             tc_fence_after();
-            // dP^T = V dO^T
+            // S^T and dP^T swap TMEM regions every tile: S^T goes where the
+            // previous dP^T was (already consumed), dP^T where the previous S^T
+            // was, which now holds the previous tile's dQ; so only dP^T waits
+            // for the dQ drain, and the softmax can start on S^T meanwhile.
+            const uint32_t rs = region_s(q_it), rd = 128 - rs;
+            // S^T = K Q^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tmem + 128, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0);
+              mma_ss(tmem + rs, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0);
             }
-            mma_commit(&bars->dp_full);
-            // S^T = K Q^T, once the previous dQ has left TMEM
+            mma_commit(&bars->s_full);
+            // dP^T = V dO^T, once the previous dQ has left TMEM
             if (i > u.i0 || ui > u_begin) {
               if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
               dq_ph ^= 1;
@@ -369,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0);
+              mma_ss(tmem + rd, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_s, kk > 0);
             }
-            mma_commit(&bars->s_full);
+            mma_commit(&bars->dp_full);
             // dV += P^T dO  (A from TMEM)
             if (i == u.i0) {
               if (!mbar_wait(&bars->dkv_empty, dkv_ph ^ 1, ab)) goto mma_done;
@@ -382,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
-              mma_ts(tmem + C::COL_DV, tmem + pcol, sdesc_sw128(sDO + kk * 2048, C::CHUNK, 1024), id_kv,
+              mma_ts(tmem + C::COL_DV, tmem + rs + pcol, sdesc_sw128(sDO + kk * 2048, C::CHUNK, 1024), id_kv,
                      (i > u.i0 || kk > 0) ? 1u : 0u);
             }
             // dK += dS^T Q ; dQ = dS K
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
+              mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
                      id_q, kk > 0);
             mma_commit(&bars->dq_full);
             mma_commit(&bars->ds_empty);
