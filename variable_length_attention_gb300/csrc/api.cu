@@ -75,6 +75,20 @@ int make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
   return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_INVALID_ARG;
 }
 
+int make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return JFA_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_INVALID_ARG;
+}
+
 // ---------------------------------------------------------------- pinned staging
 // Plans are built on the host every call.  They reach the device through a small
 // ring of pinned host buffers so the copy never forces a host-device sync; each

@@ -23,9 +23,10 @@
 //                    into swizzled shared memory); at the end of a unit they write
 //                    dV (warpgroup 0) and dK (warpgroup 1)
 //   warps 8-11       dQ reduction: one thread per query row; reads dQ from TMEM,
-//                    releases TMEM as soon as the last slice is in registers, and
-//                    adds the row into the fp32 accumulator with vector reductions
-//                    (aixai.ru summary, "dQ epilogue": early TMEM release)
+//                    releases TMEM as soon as the whole row is in registers, stages
+//                    the tile in shared memory and reduce-adds it into the fp32
+//                    accumulator with TMA (aixai.ru summary, "dQ epilogue": staged
+//                    writeback and early TMEM release)
 //   warp 12          tcgen05 MMA issuer
 //   warp 13          loader: K, V by TMA once per unit; per query tile Q and dO by
 //                    TMA into a 2-deep ring, and L, Di into shared memory
@@ -127,6 +128,7 @@ struct Bars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty;
+  uint64_t stg_full, stg_free;  // dQ staging: rows written by all 128 drain threads / read out by TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -136,7 +138,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const Params p) {
+               const __grid_constant__ CUtensorMap tm_dq, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023) != 0) {  // the layout below needs 1024-byte alignment
@@ -170,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_empty, 4);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 8);
+    mbar_init(&bars->stg_full, 128);
+    mbar_init(&bars->stg_free, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<144>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t ph = 0, q_it = 0;
+    uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
@@ -318,10 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
         ph ^= 1;
         tc_fence_after();
-        const bool valid = BQ * i + r < u.rows;
-        float* dst = p.dq_acc + (static_cast<size_t>(u.q_base + BQ * i + r) * p.H + u.h) * D;
         // the whole row into registers first, then TMEM goes back to the MMA warp
-        // before any reduction is issued
         uint32_t v[D];
 #pragma unroll
         for (int c = 0; c < D; c += 32) tmem_ld32(tQ + c, v + c);
@@ -330,16 +331,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
-        if (valid) {
+        // Stage the rows in the dS^T buffer -- free now: this tile's dK and dQ
+        // MMAs, its last readers, have completed -- and reduce-add them into the
+        // fp32 accumulator with TMA, 64 columns (two 32-column swizzled boxes) per
+        // round (aixai.ru summary, "dQ epilogue": staged writeback).  Rows past
+        // the end of the query set are exactly zero (their P is zero), so adding
+        // them is harmless, and TMA clips rows past the end of the tensor.
+        uint8_t* stage = smem + C::OFF_DS;
+        const int y = u.q_base + BQ * i;
 #pragma unroll
-          for (int e = 0; e < D / 4; ++e)
-            asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * e),
-                         "f"(__uint_as_float(v[4 * e])), "f"(__uint_as_float(v[4 * e + 1])),
-                         "f"(__uint_as_float(v[4 * e + 2])), "f"(__uint_as_float(v[4 * e + 3]))
-                         : "memory");
+        for (int rnd = 0; rnd < D / 64; ++rnd) {
+          if (rnd > 0) {  // the previous round's boxes must have been read out
+            if (threadIdx.x == 256) {
+              bulk_wait_read_all();
+              mbar_arrive(&bars->stg_free);
+            }
+            if (!mbar_wait(&bars->stg_free, free_ph, ab)) goto done;
+            free_ph ^= 1;
+          }
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            uint8_t* row = stage + b * 16384 + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c = 64 * rnd + 32 * b + 4 * j;
+              const uint32_t addr = smem_u32(row + ((j ^ (r & 7)) << 4));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[c]), "r"(v[c + 1]),
+                           "r"(v[c + 2]), "r"(v[c + 3])
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->stg_full);
+          if (!mbar_wait(&bars->stg_full, full_ph, ab)) goto done;
+          full_ph ^= 1;
+          if (threadIdx.x == 256) {
+            tma_reduce_add_2d(&tm_dq, stage, u.h * D + 64 * rnd, y);
+            tma_reduce_add_2d(&tm_dq, stage + 16384, u.h * D + 64 * rnd + 32, y);
+            bulk_commit_group();
+          }
+        }
+        if (threadIdx.x == 256) {  // staging read out: the softmax may write the next dS^T
+          bulk_wait_read_all();
+          mbar_arrive(&bars->ds_empty);
         }
       }
     }
+    if (threadIdx.x == 256) bulk_wait_all();
   } else {
     setmaxnreg_dec<80>();
     if (warp == 12) {
@@ -413,7 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
                      id_q, kk > 0);
             mma_commit(&bars->dq_full);
-            mma_commit(&bars->ds_empty);
             mma_commit(&bars->q_empty[st]);
           }
           mma_commit(&bars->dkv_full);
@@ -538,6 +575,8 @@ int launch_main(const BwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
   if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
   if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BQ);
+  CUtensorMap tdq;  // fp32 dQ accumulator, 32-column boxes for the staged reduce-add
+  if (st == JFA_OK) st = make_map_2d_f32(&tdq, a.dq_acc, static_cast<uint64_t>(a.H) * D, a.q_rows, 32, BQ);
   if (st != JFA_OK) return st;
   auto kern = bwd_kernel<D, CAUSAL>;
   static bool attr_set = false;
@@ -562,7 +601,7 @@ int launch_main(const BwdArgs& a) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   ProfileScope prof(kKindBwdMain, a.stream);
-  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, p);
+  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

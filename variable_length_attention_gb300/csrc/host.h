@@ -24,6 +24,9 @@ int current_device(DeviceInfo* out);
 // box {box_inner, box_rows}.  Rows past the end read as zero.
 int make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                 uint32_t box_rows);
+// Same for an fp32 matrix (box_inner * 4 bytes must be 128 for the swizzle).
+int make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
