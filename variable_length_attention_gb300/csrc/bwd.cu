@@ -28,8 +28,9 @@
 //                    accumulator with TMA (aixai.ru summary, "dQ epilogue": staged
 //                    writeback and early TMEM release)
 //   warp 12          tcgen05 MMA issuer
-//   warp 13          loader: K, V by TMA once per unit; per query tile Q and dO by
-//                    TMA into a 2-deep ring, and L, Di into shared memory
+//   warp 13          loader: K, V by TMA once per unit; per query tile Q by TMA into
+//                    a 2-deep ring (with L, Di into shared memory) and dO into a
+//                    single buffer (dV, its last reader, runs early in each tile)
 // TMEM: two 128-column regions that S^T and dP^T swap every tile (P^T overwrites
 // columns 0-31 and 64-95 of S^T's region; that tile's dQ then reuses the region),
 // dV [256,256+D), dK [256+D, 256+2D).
@@ -62,9 +63,12 @@ struct Cfg {
   static constexpr int NQS = 2;                  // Q/dO ring depth
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;                 // NQS x (Q, dO)
-  static constexpr int OFF_DS = OFF_Q + NQS * 2 * TILE;      // dS^T [128 keys][128 queries] bf16
-  static constexpr int OFF_BAR = OFF_DS + 128 * 128 * 2;
+  static constexpr int OFF_Q = OFF_V + TILE;                 // NQS x Q
+  static constexpr int OFF_DO = OFF_Q + NQS * TILE;          // one dO tile: dV, its last reader,
+                                                             // runs early in a tile, so one buffer suffices
+  static constexpr int OFF_DS = OFF_DO + TILE;               // dS^T [128 keys][128 queries] bf16
+  static constexpr int OFF_STG = OFF_DS + 128 * 128 * 2;     // dQ staging: two 32-column fp32 boxes
+  static constexpr int OFF_BAR = OFF_STG + 2 * 128 * 128;
   static constexpr int OFF_LD = OFF_BAR + 256;                    // per-stage L and Di, 128 floats each
   static constexpr int SMEM_BYTES = OFF_LD + NQS * 1024;
   // No alignment slack: at head_dim 128 this is within 1 KB of the 227 KB limit.
@@ -126,7 +130,7 @@ __device__ __forceinline__ uint32_t region_s(uint32_t tile_counter) { return (ti
 
 struct Bars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty;
   uint64_t stg_full, stg_free;  // dQ staging: rows written by all 128 drain threads / read out by TMA
   uint64_t drain;
@@ -163,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_full[s], 32);
       mbar_init(&bars->q_empty[s], 1);
     }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 8);
@@ -190,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // -------------------------------------------------------- P^T and dS^T
-    // register split 144 / 144 / 144 / 80 over the four warpgroups (65,536 total)
-    setmaxnreg_inc<144>();
+    // register split 136 / 136 / 152 / 88 over the four warpgroups (65,536 total)
+    setmaxnreg_inc<136>();
     const int wg = warp >> 2;              // query half
     const int k = threadIdx.x & 127;       // key row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // -------------------------------------------------------- dQ reduction
-    setmaxnreg_inc<144>();
+    setmaxnreg_inc<152>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0;
@@ -331,17 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
-        // Stage the rows in the dS^T buffer -- free now: this tile's dK and dQ
-        // MMAs, its last readers, have completed -- and reduce-add them into the
-        // fp32 accumulator with TMA, 64 columns (two 32-column swizzled boxes) per
+        // Stage the rows in shared memory and reduce-add them into the fp32
+        // accumulator with TMA, 64 columns (two 32-column swizzled boxes) per
         // round (aixai.ru summary, "dQ epilogue": staged writeback).  Rows past
         // the end of the query set are exactly zero (their P is zero), so adding
         // them is harmless, and TMA clips rows past the end of the tensor.
-        uint8_t* stage = smem + C::OFF_DS;
+        uint8_t* stage = smem + C::OFF_STG;
         const int y = u.q_base + BQ * i;
 #pragma unroll
         for (int rnd = 0; rnd < D / 64; ++rnd) {
-          if (rnd > 0) {  // the previous round's boxes must have been read out
+          if (rnd > 0 || q_it > 0) {  // the previous round's boxes must have been read out
             if (threadIdx.x == 256) {
               bulk_wait_read_all();
               mbar_arrive(&bars->stg_free);
@@ -371,15 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
-        if (threadIdx.x == 256) {  // staging read out: the softmax may write the next dS^T
-          bulk_wait_read_all();
-          mbar_arrive(&bars->ds_empty);
-        }
       }
     }
     if (threadIdx.x == 256) bulk_wait_all();
   } else {
-    setmaxnreg_dec<80>();
+    setmaxnreg_dec<88>();
     if (warp == 12) {
       if (lane == 0) {
         // ------------------------------------------------------ MMA issuer
@@ -395,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           kv_ph ^= 1;
           for (int i = u.i0; i < u.i1; ++i, ++q_it) {
             const uint32_t st = q_it & 1;
-            const uint32_t sQ = smem_u32(smem + C::OFF_Q + st * 2 * C::TILE);
-            const uint32_t sDO = sQ + C::TILE;
+            const uint32_t sQ = smem_u32(smem + C::OFF_Q + st * C::TILE);
+            const uint32_t sDO = smem_u32(smem + C::OFF_DO);
             if (!mbar_wait(&bars->q_full[st], (q_it >> 1) & 1, ab)) goto mma_done;
             tc_fence_after();
             // S^T and dP^T swap TMEM regions every tile: S^T goes where the
@@ -415,8 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i > u.i0 || ui > u_begin) {
               if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
               dq_ph ^= 1;
-              tc_fence_after();
             }
+            if (!mbar_wait(&bars->do_full, q_it & 1, ab)) goto mma_done;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
@@ -436,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ts(tmem + C::COL_DV, tmem + rs + pcol, sdesc_sw128(sDO + kk * 2048, C::CHUNK, 1024), id_kv,
                      (i > u.i0 || kk > 0) ? 1u : 0u);
             }
+            mma_commit(&bars->do_empty);  // dV was dO's last reader: the next dO may load
             // dK += dS^T Q ; dQ = dS K
             if (!mbar_wait(&bars->ds_full, ph, ab)) goto mma_done;
             ph ^= 1;
@@ -451,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
                      id_q, kk > 0);
             mma_commit(&bars->dq_full);
+            mma_commit(&bars->ds_empty);
             mma_commit(&bars->q_empty[st]);
           }
           mma_commit(&bars->dkv_full);
@@ -493,17 +497,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_lse[st * 128 + r] = v ? p.lse2[lbase + r] : INFINITY;
             s_di[st * 128 + r] = v ? p.di[lbase + r] : 0.f;
           }
-          uint8_t* sQ = smem + C::OFF_Q + st * 2 * C::TILE;
+          uint8_t* sQ = smem + C::OFF_Q + st * C::TILE;
           if (lane == 0) {
-            mbar_expect_tx(&bars->q_full[st], 2 * C::TILE);
+            mbar_expect_tx(&bars->q_full[st], C::TILE);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / 64; ++c)
               tma_load_2d(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, u.h * D + c * 64, u.q_base + BQ * i);
-              tma_load_2d(&tm_do, &bars->q_full[st], sQ + C::TILE + c * C::CHUNK, u.h * D + c * 64,
-                          u.o_base + BQ * i);
-            }
           } else {
             mbar_arrive(&bars->q_full[st]);
+          }
+          // dO: a single buffer, free once the previous tile's dV has read it
+          if (!mbar_wait(&bars->do_empty, (q_it & 1) ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(&bars->do_full, C::TILE);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, u.h * D + c * 64,
+                          u.o_base + BQ * i);
           }
         }
       }
