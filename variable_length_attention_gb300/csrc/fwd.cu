@@ -76,6 +76,8 @@ struct Unit {
   int o_row0;       // first output row of the unit in o
   int n_kv;         // K/V blocks visited
   int n_plain;      // leading blocks that need no mask
+  int n_kv0;        // blocks query tile 0 needs (causal: it skips the unit's last block when
+                    // that block lies wholly in its masked future)
 };
 
 template <bool CAUSAL>
@@ -101,9 +103,11 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
     const int last = min(2 * BM * (u.m + 1), u.rows);
     u.n_kv = (min(last, u.L) + BN - 1) / BN;
     u.n_plain = min(u.L / BN, 2 * u.m);
+    u.n_kv0 = min(u.n_kv, 2 * u.m + 1);
   } else {
     u.n_kv = (u.L + BN - 1) / BN;
     u.n_plain = u.L / BN;
+    u.n_kv0 = u.n_kv;
   }
   return u;
 }
@@ -215,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit u = decode<CAUSAL>(p, ui);
       const int qi = 2 * BM * u.m + BM * t + row;  // query index inside the sequence / shared Q
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < u.n_kv; ++j) {
+      const int n_kv_t = t == 0 ? u.n_kv0 : u.n_kv;
+      for (int j = 0; j < n_kv_t; ++j) {
         if (!mbar_wait(&bars->s_full[t], s_phase, ab)) goto done;
         s_phase ^= 1;
         tc_fence_after();
@@ -377,20 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kv_it;
           const bool more = j + 1 < u.n_kv;
           uint32_t ks2 = 0;
-          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-          if (j == 0 && !mbar_wait(&bars->o_empty[0], u_phase ^ 1, ab)) goto mma_done;
-          if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
-          p_phase[0] ^= 1;
-          tc_fence_after();
-          issue_pv(0, vs, j > 0);
-          if (!more) mma_commit(&bars->o_full[0]);
-          if (more) {
+          if (more) {  // K_{j+1}
             ks2 = stage_of(kv_it);
             if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
             ++kv_it;
+          }
+          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop one block early)
+          if (j < u.n_kv0) {
+            if (j == 0 && !mbar_wait(&bars->o_empty[0], u_phase ^ 1, ab)) goto mma_done;
+            if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
+            p_phase[0] ^= 1;
             tc_fence_after();
-            issue_s(0, ks2);
-            mma_commit(&bars->s_full[0]);
+            issue_pv(0, vs, j > 0);
+            if (j + 1 == u.n_kv0) mma_commit(&bars->o_full[0]);
+            if (j + 1 < u.n_kv0) {
+              issue_s(0, ks2);
+              mma_commit(&bars->s_full[0]);
+            }
           }
           // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
           if (j == 0 && !mbar_wait(&bars->o_empty[1], u_phase ^ 1, ab)) goto mma_done;
