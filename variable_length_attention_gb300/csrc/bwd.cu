@@ -20,9 +20,10 @@
 // including the dedicated dQ-reduction role):
 //   warps 0-3 / 4-7  one thread per key (TMEM lane); warpgroup w handles query
 //                    columns [64w, 64w+64): P^T (bf16, into TMEM) and dS^T (bf16,
-//                    into swizzled shared memory); at the end of a unit they write
-//                    dV (warpgroup 0) and dK (warpgroup 1)
-//   warps 8-11       dQ reduction: one thread per query row; reads dQ from TMEM,
+//                    into swizzled shared memory)
+//   warps 8-11       dQ reduction and dK/dV epilogue: one thread per TMEM lane; at
+//                    the end of a unit it writes dV and dK (before that tile's dQ,
+//                    so the next unit's dV/dK MMAs can start); per tile it reads dQ,
 //                    releases TMEM as soon as the whole row is in registers, stages
 //                    the tile in shared memory and reduce-adds it into the fp32
 //                    accumulator with TMA (aixai.ru summary, "dQ epilogue": staged
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 4);
     mbar_init(&bars->dkv_full, 1);
-    mbar_init(&bars->dkv_empty, 8);
+    mbar_init(&bars->dkv_empty, 4);
     mbar_init(&bars->stg_full, 128);
     mbar_init(&bars->stg_free, 1);
     mbar_init(&bars->drain, 1);
@@ -196,14 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // -------------------------------------------------------- P^T and dS^T
-    // register split 136 / 136 / 152 / 88 over the four warpgroups (65,536 total)
-    setmaxnreg_inc<136>();
+    // register split 128 / 128 / 160 / 96 over the four warpgroups (65,536 total)
+    setmaxnreg_inc<128>();
     const int wg = warp >> 2;              // query half
     const int k = threadIdx.x & 127;       // key row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint8_t* sDS = smem + C::OFF_DS + wg * C::CHUNK + k * 128;  // row k of this half's box
     const float sl2 = p.scale_log2;
-    uint32_t ph = 0, ds_ph = 0, dkv_ph = 0, q_it = 0;
+    uint32_t ph = 0, ds_ph = 0, q_it = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       const bool key_ok = BK * u.n + k < u.L;
@@ -286,45 +287,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ds_full);
       }
-      // unit done: write dV (warpgroup 0) or dK (warpgroup 1)
-      if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
-      dkv_ph ^= 1;
-      tc_fence_after();
-      {
-        const uint32_t tAcc = tmem + lane_addr + (wg == 0 ? C::COL_DV : C::COL_DK);
-        const float mul = wg == 0 ? 1.0f : p.scale;
-        __nv_bfloat16* dst = (wg == 0 ? p.dv : p.dk) + (static_cast<size_t>(u.kv0 + BK * u.n + k) * p.H + u.h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tAcc + c, ov);
-          tmem_wait_ld();
-          reg_fence<32>(ov);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
-          if (key_ok) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dkv_empty);
     }
   } else if (warp < 12) {
     // -------------------------------------------------------- dQ reduction
-    setmaxnreg_inc<152>();
+    setmaxnreg_inc<160>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0;
+    uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0, dkv_ph = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
         const uint32_t tQ = tmem + lane_addr + region_s(q_it);  // dQ sits where this tile's S^T was
+        if (i + 1 == u.i1) {
+          // unit done: dV and dK leave TMEM first (the next unit's first dV/dK
+          // MMAs wait for them); one thread per key row
+          if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
+          dkv_ph ^= 1;
+          tc_fence_after();
+          const bool key_ok = BK * u.n + r < u.L;
+          const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.H + u.h) * D;
+#pragma unroll 1
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t tAcc = tmem + lane_addr + (which == 0 ? C::COL_DV : C::COL_DK);
+            const float mul = which == 0 ? 1.0f : p.scale;
+            __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tAcc + c, ov);
+              tmem_wait_ld();
+              reg_fence<32>(ov);
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
+              if (key_ok) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->dkv_empty);
+        }
         if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
         ph ^= 1;
         tc_fence_after();
@@ -380,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 256) bulk_wait_all();
   } else {
-    setmaxnreg_dec<88>();
+    setmaxnreg_dec<96>();
     if (warp == 12) {
       if (lane == 0) {
         // ------------------------------------------------------ MMA issuer
@@ -439,26 +446,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (i > u.i0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->do_empty);  // dV was dO's last reader: the next dO may load
-            // dK += dS^T Q ; dQ = dS K
+            // dQ = dS K first (K's last reader in the tile), then dK += dS^T Q
             if (!mbar_wait(&bars->ds_full, ph, ab)) goto mma_done;
             ph ^= 1;
             tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
+                     id_q, kk > 0);
+            mma_commit(&bars->dq_full);
+            if (i + 1 == u.i1) mma_commit(&bars->kv_empty);  // K and V are done: the next unit's may load
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
               mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(sQ + kk * 2048, C::CHUNK, 1024),
                      id_kv, (i > u.i0 || kk > 0) ? 1u : 0u);
             }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
-                     id_q, kk > 0);
-            mma_commit(&bars->dq_full);
             mma_commit(&bars->ds_empty);
             mma_commit(&bars->q_empty[st]);
           }
           mma_commit(&bars->dkv_full);
-          mma_commit(&bars->kv_empty);
         }
       mma_done:
         mma_commit(&bars->drain);
