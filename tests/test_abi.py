@@ -99,3 +99,16 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             J.load(ctypes_path)
         finally:
             J._lib = saved
+
+
+def test_binding_rejects_mismatched_shapes():
+    # broadcast-Q called without nq_broadcast: q has the shared rows only, so the
+    # binding must refuse before the library is asked to read past its end
+    import torch
+    offs = torch.tensor([0, 300, 700], dtype=torch.int32)
+    q = torch.zeros((256, 2, 64), dtype=torch.bfloat16)
+    k = torch.zeros((700, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="q: expected shape"):
+        J._check_problem(q, k, k, offs, offs.numpy(), 0)
+    with pytest.raises(ValueError, match="CUDA"):  # right shapes, but host tensors
+        J._check_problem(q, k, k, offs, offs.numpy(), 256)

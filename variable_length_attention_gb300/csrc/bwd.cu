@@ -35,8 +35,9 @@
 // TMEM: two 128-column regions that S^T and dP^T swap every tile (P^T overwrites
 // columns 0-31 and 64-95 of S^T's region; that tile's dQ then reuses the region),
 // dV [256,256+D), dK [256+D, 256+2D).
-// Per tile the tensor core runs S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
-// dK += dS^T Q, dQ = dS K; the next S^T never waits for the dQ drain.
+// Per tile the tensor core runs dP^T = V dO^T, dV += P^T dO, dQ = dS K, the next
+// tile's S^T = K Q^T, then dK += dS^T Q: the next tile's P phase overlaps dK and
+// the next dP^T, and no S^T waits for the dQ drain.
 // Masks: keys past the sequence end and query rows past it are zeroed per thread
 // (a key flag and L = +inf), so only the causal diagonal tile needs an
 // element-wise mask, and it is peeled into its own code path.
@@ -397,28 +398,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
         const uint32_t sDS = smem_u32(smem + C::OFF_DS);
         uint32_t kv_ph = 0, ph = 0, dq_ph = 0, dkv_ph = 0, q_it = 0;
+        // S^T = K Q^T of tile t into its region; false if the CTA aborts
+        auto issue_s = [&](uint32_t t) -> bool {
+          const uint32_t st_t = t & 1;
+          if (!mbar_wait(&bars->q_full[st_t], (t >> 1) & 1, ab)) return false;
+          tc_fence_after();
+          const uint32_t sQt = smem_u32(smem + C::OFF_Q + st_t * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+            mma_ss(tmem + region_s(t), sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQt + off, 16, 1024), id_s,
+                   kk > 0);
+          }
+          mma_commit(&bars->s_full);
+          return true;
+        };
         for (int ui = u_begin; ui < u_end; ++ui) {
           const Unit u = decode<CAUSAL>(p, ui);
           if (!mbar_wait(&bars->kv_full, kv_ph, ab)) goto mma_done;
           kv_ph ^= 1;
+          if (!issue_s(q_it)) goto mma_done;  // the unit's first tile
           for (int i = u.i0; i < u.i1; ++i, ++q_it) {
             const uint32_t st = q_it & 1;
             const uint32_t sQ = smem_u32(smem + C::OFF_Q + st * C::TILE);
             const uint32_t sDO = smem_u32(smem + C::OFF_DO);
-            if (!mbar_wait(&bars->q_full[st], (q_it >> 1) & 1, ab)) goto mma_done;
-            tc_fence_after();
             // S^T and dP^T swap TMEM regions every tile: S^T goes where the
             // previous dP^T was (already consumed), dP^T where the previous S^T
-            // was, which now holds the previous tile's dQ; so only dP^T waits
-            // for the dQ drain, and the softmax can start on S^T meanwhile.
+            // was, which holds the previous tile's dQ until the drain has read it.
             const uint32_t rs = region_s(q_it), rd = 128 - rs;
-            // S^T = K Q^T
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tmem + rs, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s, kk > 0);
-            }
-            mma_commit(&bars->s_full);
             // dP^T = V dO^T, once the previous dQ has left TMEM
             if (i > u.i0 || ui > u_begin) {
               if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
@@ -446,15 +453,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (i > u.i0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->do_empty);  // dV was dO's last reader: the next dO may load
-            // dQ = dS K first (K's last reader in the tile), then dK += dS^T Q
             if (!mbar_wait(&bars->ds_full, ph, ab)) goto mma_done;
             ph ^= 1;
             tc_fence_after();
+            // dQ = dS K first (the drain can start), then the next tile's S^T into
+            // this tile's dP^T region (read by the dS phase that just finished),
+            // then dK += dS^T Q: the next tile's P phase overlaps dK.
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
                      id_q, kk > 0);
             mma_commit(&bars->dq_full);
+            if (i + 1 < u.i1 && !issue_s(q_it + 1)) goto mma_done;
             if (i + 1 == u.i1) mma_commit(&bars->kv_empty);  // K and V are done: the next unit's may load
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {

@@ -92,6 +92,38 @@ def _check(name, st):
         raise JfaError(name, st)
 
 
+def _expect(name, t, shape, dtype=torch.bfloat16):
+    """The C ABI sees only pointers; check here that each tensor really is the
+    contiguous device buffer the call will read or write."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+
+
+def _check_problem(q, k, v, offsets, offs_h, nq, *, o=None, dout=None, lse=None, dq=None, dk=None, dv=None):
+    batch = len(offs_h) - 1
+    T = int(offs_h[-1]) if batch >= 0 else 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    q_rows = nq if nq > 0 else T
+    o_rows = batch * nq if nq > 0 else T
+    _expect("q", q, (q_rows, H, D))
+    _expect("k", k, (T, Hkv, D))
+    _expect("v", v, (T, Hkv, D))
+    _expect("offsets", offsets, (batch + 1,), torch.int32)
+    _expect("o", o, (o_rows, H, D))
+    _expect("dout", dout, (o_rows, H, D))
+    _expect("lse", lse, (H, o_rows), torch.float32)
+    _expect("dq", dq, (q_rows, H, D))
+    _expect("dk", dk, (T, Hkv, D))
+    _expect("dv", dv, (T, Hkv, D))
+
+
 def _workspace(op, offs_h, batch, nq, H, D, causal, bq, workspace, device):
     need = load().jfa_workspace_size(op, offs_h.ctypes.data_as(ctypes.c_void_p), batch, nq, H, D, int(causal),
                                      int(bq))
@@ -136,6 +168,7 @@ def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0
         lse = torch.empty((H, o_rows), dtype=torch.float32, device=q.device)
     if not return_lse:
         lse = None
+    _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
     workspace, need = _workspace(JFA_OP_FWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
     st = L.jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
                    offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv, D,
@@ -160,6 +193,7 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv)
     workspace, need = _workspace(JFA_OP_BWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
     st = L.jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                    _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast),
@@ -179,6 +213,7 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     out = torch.empty_like(q) if out is None else out
+    _check_problem(q, k, v, offsets, offs_h, 0, o=out)
     workspace, need = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     st = L.block_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p),
                           batch, int(max_len), H, D, float(scale), _ptr(workspace), workspace.numel(), _stream())
@@ -200,6 +235,7 @@ def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_problem(q, k, v, offsets, offs_h, 0, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
     workspace, need = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     st = L.block_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                           _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), H, D,
@@ -290,6 +326,7 @@ def jfa_fwd_noalloc(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_bro
     o_rows = batch * nq_broadcast if bq else int(offs_h[-1])
     if out is None:
         out = torch.empty((o_rows, H, D), dtype=torch.bfloat16, device=q.device)
+    _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
     st = L.jfa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
                            offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv,
                            D, float(scale), int(causal), int(bq), _stream())
