@@ -387,15 +387,17 @@ def build_job(args, dev):
                                             wl.nq > 0) if wl.bwd else 0)
             calls.append((wl, o, lse, grads, extra, torch.empty(need, dtype=torch.uint8, device=dev)))
 
+        max_len = w.max_len  # the caller's bound on sequence length, as the interface takes it
+
         def step(inp):
             q, k, v, do = inp
             for wl, o, lse, grads, extra, wsb in calls:
                 kk, vv = (extra[0], extra[1]) if extra is not None else (k, v)
-                V.jfa_fwd(q, kk, vv, offs, offs_h, causal=wl.causal, nq_broadcast=wl.nq, out=o, lse=lse,
-                          workspace=wsb)
+                V.jfa_fwd(q, kk, vv, offs, offs_h, max_len=max_len, causal=wl.causal, nq_broadcast=wl.nq, out=o,
+                          lse=lse, workspace=wsb)
                 if grads is not None:
-                    V.jfa_bwd(q, kk, vv, o, do, lse, offs, offs_h, causal=wl.causal, nq_broadcast=wl.nq,
-                              dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+                    V.jfa_bwd(q, kk, vv, o, do, lse, offs, offs_h, max_len=max_len, causal=wl.causal,
+                              nq_broadcast=wl.nq, dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
 
         fl = [W.flops(wl) for wl in wls]
         flops = {"fwd": float(sum(f for f, _ in fl)),
@@ -422,8 +424,9 @@ def build_job(args, dev):
 
     def step(inp):
         q, k, v, do = inp
-        V.block_attn_fwd(q, k, v, offs, offs_h, out=o, workspace=wsb)
-        V.block_attn_bwd(q, k, v, o, do, offs, offs_h, dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+        V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=o, workspace=wsb)
+        V.block_attn_bwd(q, k, v, o, do, offs, offs_h, max_len=w.max_len, dq=grads[0], dk=grads[1], dv=grads[2],
+                         workspace=wsb)
 
     f, b = W.flops(w)
     t_bytes = dev_in[0].numel() * 2

@@ -330,7 +330,6 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   const FwdLayout lay = fwd_layout(n, n_cta, batch);
   if (workspace_bytes < lay.total || workspace == nullptr) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
 
   if (!empty.empty()) {
     // one staging copy for the list of empty sequences, then a fill kernel
@@ -343,12 +342,13 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
                                                              head_dim, c.o_rows, static_cast<__nv_bfloat16*>(o), lse);
     if (cudaGetLastError() != cudaSuccess) return JFA_ERR_CUDA;
   }
-  if (n == 0) return JFA_OK;
-  // units and CTA starts travel in one copy (they are adjacent in the workspace)
-  std::vector<uint8_t> blob(lay.empty - lay.units, 0);
-  std::memcpy(blob.data(), units.data(), units.size() * 4);
-  std::memcpy(blob.data() + (lay.cta - lay.units), cta_start.data(), cta_start.size() * 4);
-  st = stage_to_device(ws + lay.units, blob.data(), blob.size(), stream);
+  if (n == 0) return cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+  // the cleared error word, the units and the CTA starts travel in one copy
+  // (they are adjacent at the head of the workspace)
+  std::vector<uint8_t> blob(lay.empty - lay.err, 0);
+  std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
+  std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
+  st = stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
   if (st != JFA_OK) return st;
 
   FwdArgs a;
@@ -402,7 +402,6 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   const BwdLayout lay = bwd_layout(n, n_cta, c.q_rows, c.o_rows, num_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
 
   BwdArgs a;
   a.q = q;
@@ -432,16 +431,22 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   a.err = reinterpret_cast<int*>(ws + lay.err);
   a.stream = stream;
 
-  const size_t acc_bytes = static_cast<size_t>(c.q_rows) * num_heads * head_dim * 4;
-  if (acc_bytes && cudaMemsetAsync(a.dq_acc, 0, acc_bytes, stream) != cudaSuccess) return JFA_ERR_CUDA;
   if (n > 0) {
-    std::vector<uint8_t> blob(lay.lse2 - lay.units, 0);
-    std::memcpy(blob.data(), units.data(), units.size() * 4);
-    std::memcpy(blob.data() + (lay.cta - lay.units), cta_start.data(), cta_start.size() * 4);
-    st = stage_to_device(ws + lay.units, blob.data(), blob.size(), stream);
-    if (st != JFA_OK) return st;
-    st = launch_bwd_prep(a);
-    if (st != JFA_OK) return st;
+    // the cleared error word, the units and the CTA starts in one copy, ahead of
+    // the kernels so that they follow one another directly
+    std::vector<uint8_t> blob(lay.lse2 - lay.err, 0);
+    std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
+    std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
+    st = stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
+  } else {
+    st = cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+  }
+  if (st != JFA_OK) return st;
+  // the prepass also zeroes the dQ accumulator, so it runs even with no units
+  // (broadcast-Q with every sequence empty still returns dQ = 0)
+  st = launch_bwd_prep(a, c.dev.num_sms);
+  if (st != JFA_OK) return st;
+  if (n > 0) {
     st = launch_bwd_main(a);
     if (st != JFA_OK) return st;
   }
@@ -463,7 +468,6 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   const BlockLayout lay = block_layout(batch, P);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
   a->q = q;
   a->k = k;
   a->v = v;
@@ -479,11 +483,12 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   a->n_prog = P;
   a->scale = scale;
   a->stream = stream;
-  if (P == 0) return JFA_OK;
-  std::vector<uint8_t> blob(lay.total - lay.bpb, 0);
-  std::memcpy(blob.data(), bpb.data(), bpb.size() * 4);
-  std::memcpy(blob.data() + (lay.prog - lay.bpb), prog.data(), prog.size() * 4);
-  return stage_to_device(ws + lay.bpb, blob.data(), blob.size(), stream);
+  if (P == 0) return cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+  // the cleared error word and both lists in one copy
+  std::vector<uint8_t> blob(lay.total - lay.err, 0);
+  std::memcpy(blob.data() + (lay.bpb - lay.err), bpb.data(), bpb.size() * 4);
+  std::memcpy(blob.data() + (lay.prog - lay.err), prog.data(), prog.size() * 4);
+  return stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
 }
 
 extern "C" int block_attn_fwd(const void* q, const void* k, const void* v, void* o, const int32_t* offsets_dev,

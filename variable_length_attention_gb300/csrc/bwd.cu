@@ -9,7 +9,8 @@
 // Broadcast-Q sums dQ of the shared Q over every sequence.
 //
 // Kernels, in launch order:
-//   prep_kernel   Di = rowsum(dO o O) and L * log2(e) per (row, head)
+//   prep_kernel   Di = rowsum(dO o O) and L * log2(e) per (row, head); zeroes the
+//                 fp32 dQ accumulator
 //   bwd_kernel    persistent, one CTA per SM, one work unit = one valid block of
 //                 128 keys of one (sequence, head); it loops over the 128-row query
 //                 tiles that attend to those keys, keeps dK and dV in TMEM and
@@ -41,6 +42,8 @@
 // Masks: keys past the sequence end and query rows past it are zeroed per thread
 // (a key flag and L = +inf), so only the causal diagonal tile needs an
 // element-wise mask, and it is peeled into its own code path.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -555,36 +558,63 @@ done:
 
 // Di[h, r] = sum_d dO[r,h,d] O[r,h,d];  lse2[h, r] = L[h, r] log2(e).
 // 16 threads per (row, head) for D = 128 (8 per head for D = 64), 8 bf16 each.
+// Di and L * log2(e) for every (head, row) pair, and a zero fill of the fp32
+// dQ accumulator that the main kernel reduce-adds into.  Pairs are numbered
+// head-major (p = h * rows + r, the layout of L and Di), so consecutive pairs are
+// consecutive rows of one head and the per-pair results are written coalesced;
+// each pair's O and dO rows (D bf16 each) are read by D/8 lanes with 16-byte
+// loads, several pairs per thread in flight.
 template <int D>
 __global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                             const float* __restrict__ lse, float* __restrict__ di, float* __restrict__ lse2,
-                            int rows, int H) {
-  constexpr int TPR = D / 8;
-  const long gid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long pair = gid / TPR;  // (row, head) index = row * H + h
-  const int part = static_cast<int>(gid % TPR);
-  float acc = 0.f;
-  const bool in = pair < static_cast<long>(rows) * H;
-  if (in) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + pair * D + part * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(dout + pair * D + part * 8);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+                            int rows, int H, float4* __restrict__ acc, long acc4) {
+  constexpr int TPP = D / 8;     // lanes per pair
+  constexpr int PPW = 32 / TPP;  // pairs per warp per round
+  constexpr int U = 4;           // rounds whose loads are in flight together
+  const int lane = threadIdx.x & 31, part = lane % TPP;
+  const long warp = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long n_warps = (static_cast<long>(gridDim.x) * blockDim.x) >> 5;
+  const long n_pairs = static_cast<long>(rows) * H;
+  for (long base = warp * PPW * U; base < n_pairs; base += n_warps * PPW * U) {
+    uint4 a[U], b[U];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 fa = __bfloat1622float2(a2[e]);
-      const float2 fb = __bfloat1622float2(b2[e]);
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
+    for (int u = 0; u < U; ++u) {
+      const long pr = base + u * PPW + lane / TPP;
+      if (pr < n_pairs) {
+        const long h = pr / rows, r = pr - h * rows;
+        const size_t at = (static_cast<size_t>(r) * H + h) * D + part * 8;
+        a[u] = *reinterpret_cast<const uint4*>(o + at);
+        b[u] = *reinterpret_cast<const uint4*>(dout + at);
+      } else {
+        a[u] = make_uint4(0, 0, 0, 0);
+        b[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a2[e]);
+        const float2 fb = __bfloat1622float2(b2[e]);
+        s = fmaf(fa.x, fb.x, s);
+        s = fmaf(fa.y, fb.y, s);
+      }
+#pragma unroll
+      for (int off = TPP / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const long pr = base + u * PPW + lane / TPP;
+      if (part == 0 && pr < n_pairs) {
+        di[pr] = s;
+        lse2[pr] = lse[pr] * kLog2e;
+      }
     }
   }
-#pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (in && part == 0) {
-    const int r = static_cast<int>(pair / H), h = static_cast<int>(pair % H);
-    di[static_cast<size_t>(h) * rows + r] = acc;
-    lse2[static_cast<size_t>(h) * rows + r] = lse[static_cast<size_t>(h) * rows + r] * kLog2e;
-  }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < acc4;
+       i += static_cast<long>(gridDim.x) * blockDim.x)
+    acc[i] = z;
 }
 
 __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4, float scale) {
@@ -637,20 +667,26 @@ int launch_main(const BwdArgs& a) {
 
 }  // namespace bwd
 
-int launch_bwd_prep(const BwdArgs& a) {
-  if (a.o_rows == 0) return JFA_OK;
-  const long threads = static_cast<long>(a.o_rows) * a.H * (a.D / 8);
+int launch_bwd_prep(const BwdArgs& a, int num_sms) {
+  const long pairs = static_cast<long>(a.o_rows) * a.H;
+  const long acc4 = static_cast<long>(a.q_rows) * a.H * a.D / 4;
+  if (pairs == 0 && acc4 == 0) return JFA_OK;
   const int block = 256;
-  const long grid = (threads + block - 1) / block;
+  // enough warps for every pair to be visited once where that fits, capped at
+  // 16 resident blocks per SM; larger problems loop
+  const long per_block = (block / 32) * (32 / (a.D / 8)) * 4;
+  long grid = std::max((pairs + per_block - 1) / per_block, (acc4 + block - 1) / block);
+  grid = std::min<long>(std::max<long>(grid, 1), 16L * num_sms);
   ProfileScope prof(kKindBwdPrep, a.stream);
+  float4* acc = reinterpret_cast<float4*>(a.dq_acc);
   if (a.D == 128)
-    bwd::prep_kernel<128><<<grid, block, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.o),
-                                                         static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di,
-                                                         a.lse2, a.o_rows, a.H);
+    bwd::prep_kernel<128><<<static_cast<int>(grid), block, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di, a.lse2,
+        a.o_rows, a.H, acc, acc4);
   else
-    bwd::prep_kernel<64><<<grid, block, 0, a.stream>>>(static_cast<const __nv_bfloat16*>(a.o),
-                                                        static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di,
-                                                        a.lse2, a.o_rows, a.H);
+    bwd::prep_kernel<64><<<static_cast<int>(grid), block, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.di, a.lse2,
+        a.o_rows, a.H, acc, acc4);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

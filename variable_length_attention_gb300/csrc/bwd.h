@@ -25,7 +25,7 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
-int launch_bwd_prep(const BwdArgs& a);
+int launch_bwd_prep(const BwdArgs& a, int num_sms);  // also zeroes dq_acc
 int launch_bwd_main(const BwdArgs& a);
 int launch_dq_convert(const BwdArgs& a, int num_sms);
 

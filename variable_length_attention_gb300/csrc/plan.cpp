@@ -50,99 +50,107 @@ int check_offsets(const int32_t* offsets, int batch, int max_len) {
   return JFA_OK;
 }
 
+// Both list planners share one dealing step.  Units arrive in enumeration
+// order with a small integer cost.  A counting sort on the cost (largest first)
+// gives the same order as a stable sort, in linear time: units of equal cost
+// keep their enumeration order.  Sorted index t is dealt in pass p = t / P to
+// slot r = t % P, CTA r on even passes and P-1-r on odd ones, so CTA c holds
+// one unit per pass and the unit of pass p sits at position p of its list.
+template <class Enumerate>
+static int deal_sorted(Enumerate&& each, int64_t n, int n_cta, std::vector<int32_t>* units,
+                       std::vector<int32_t>* cta_start) {
+  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
+  const int64_t P = n_cta, full = n / P, rem = n % P;
+  std::vector<int32_t> start(P + 1, 0);
+  for (int64_t c = 0; c < P; ++c) {
+    // the last, partial pass reaches CTAs 0..rem-1 (even pass) or P-rem..P-1 (odd pass)
+    const bool extra = (full % 2 == 0) ? c < rem : c >= P - rem;
+    start[c + 1] = static_cast<int32_t>(start[c] + full + (extra ? 1 : 0));
+  }
+  if (units) {
+    int32_t max_cost = 0;
+    each([&](int32_t, int32_t, int32_t, int32_t cost) { max_cost = std::max(max_cost, cost); });
+    // bucket k holds cost max_cost - k; its cursor is the (pass, slot) of the
+    // sorted index its next unit takes, advanced without a division per unit
+    const size_t nb = static_cast<size_t>(max_cost) + 1;
+    std::vector<int64_t> first(nb + 1, 0), pass(nb), slot(nb);
+    each([&](int32_t, int32_t, int32_t, int32_t cost) { ++first[max_cost - cost + 1]; });
+    for (size_t k = 1; k <= nb; ++k) first[k] += first[k - 1];
+    for (size_t k = 0; k < nb; ++k) {
+      pass[k] = first[k] / P;
+      slot[k] = first[k] % P;
+    }
+    units->resize(4 * n);  // every entry is written below
+    int32_t* out = units->data();
+    each([&](int32_t b, int32_t h, int32_t m, int32_t cost) {
+      const size_t k = static_cast<size_t>(max_cost - cost);
+      const int64_t p = pass[k], r = slot[k];
+      if (++slot[k] == P) {
+        slot[k] = 0;
+        ++pass[k];
+      }
+      const int64_t c = (p % 2 == 0) ? r : P - 1 - r;
+      int32_t* e = out + 4 * (start[c] + p);
+      e[0] = b;
+      e[1] = h;
+      e[2] = m;
+      e[3] = cost;
+    });
+  }
+  if (cta_start) *cta_start = std::move(start);
+  return static_cast<int>(n);
+}
+
 int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
-  struct U {
-    int32_t b, h, m, cost;
+  // enumeration order: sequence, head, 256-row unit; cost = K/V blocks visited
+  auto each = [&](auto&& fn) {
+    for (int b = 0; b < batch; ++b) {
+      const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+      if (L == 0) continue;
+      const int64_t rows = nq > 0 ? nq : L;
+      const int64_t nm = cdiv(rows, kFwdRows);
+      for (int h = 0; h < H; ++h)
+        for (int64_t m = 0; m < nm; ++m) {
+          int64_t cost;
+          if (causal) {
+            const int64_t last_row = std::min<int64_t>(kFwdRows * (m + 1), rows);
+            cost = cdiv(std::min(last_row, L), kKvBlock);
+          } else {
+            cost = cdiv(L, kKvBlock);
+          }
+          fn(b, h, static_cast<int32_t>(m), static_cast<int32_t>(cost));
+        }
+    }
   };
-  std::vector<U> all;
+  int64_t n = 0;
   for (int b = 0; b < batch; ++b) {
     const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
-    if (L == 0) continue;
-    const int64_t rows = nq > 0 ? nq : L;
-    const int64_t nm = cdiv(rows, kFwdRows);
-    for (int h = 0; h < H; ++h)
-      for (int64_t m = 0; m < nm; ++m) {
-        int64_t cost;
-        if (causal) {
-          const int64_t last_row = std::min<int64_t>(kFwdRows * (m + 1), rows);
-          cost = cdiv(std::min(last_row, L), kKvBlock);
-        } else {
-          cost = cdiv(L, kKvBlock);
-        }
-        all.push_back({b, h, static_cast<int32_t>(m), static_cast<int32_t>(cost)});
-      }
+    if (L > 0) n += static_cast<int64_t>(H) * cdiv(nq > 0 ? nq : L, kFwdRows);
   }
-  std::stable_sort(all.begin(), all.end(), [](const U& x, const U& y) { return x.cost > y.cost; });
-  const int64_t n = static_cast<int64_t>(all.size());
-  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
-  // snake deal: sorted index t -> pass p = t / P, slot r = t % P
-  std::vector<int32_t> cta_of(n), count(n_cta, 0);
-  for (int64_t t = 0; t < n; ++t) {
-    const int64_t p = t / n_cta, r = t % n_cta;
-    const int32_t c = static_cast<int32_t>((p % 2 == 0) ? r : n_cta - 1 - r);
-    cta_of[t] = c;
-    ++count[c];
-  }
-  std::vector<int32_t> start(n_cta + 1, 0);
-  for (int c = 0; c < n_cta; ++c) start[c + 1] = start[c] + count[c];
-  if (units) {
-    units->assign(4 * n, 0);
-    std::vector<int32_t> pos(start.begin(), start.end() - 1);
-    for (int64_t t = 0; t < n; ++t) {
-      const int64_t i = pos[cta_of[t]]++;
-      (*units)[4 * i + 0] = all[t].b;
-      (*units)[4 * i + 1] = all[t].h;
-      (*units)[4 * i + 2] = all[t].m;
-      (*units)[4 * i + 3] = all[t].cost;
-    }
-  }
-  if (cta_start) *cta_start = start;
-  return static_cast<int>(n);
+  return deal_sorted(each, n, n_cta, units, cta_start);
 }
 
 int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
-  struct U {
-    int32_t b, h, n, cost;
-  };
-  std::vector<U> all;
-  for (int b = 0; b < batch; ++b) {
-    const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
-    const int64_t rows = nq > 0 ? nq : L;
-    const int64_t q_tiles = cdiv(rows, kKvBlock);
-    for (int h = 0; h < H; ++h)
-      for (int64_t blk = 0; blk < cdiv(L, kKvBlock); ++blk)
-        all.push_back({b, h, static_cast<int32_t>(blk), static_cast<int32_t>(causal ? q_tiles - blk : q_tiles)});
-  }
-  const int64_t n = static_cast<int64_t>(all.size());
-  if (units == nullptr && cta_start == nullptr) return static_cast<int>(n);
-  // Equal costs (broadcast-Q) keep the enumeration order; unequal ones (self-
-  // attention, where a unit loops over its sequence's query tiles) are sorted
-  // largest first so the snake deal balances them.
-  std::stable_sort(all.begin(), all.end(), [](const U& x, const U& y) { return x.cost > y.cost; });
-  std::vector<int32_t> cta_of(n), count(n_cta, 0);
-  for (int64_t t = 0; t < n; ++t) {
-    const int64_t p = t / n_cta, r = t % n_cta;
-    const int32_t c = static_cast<int32_t>((p % 2 == 0) ? r : n_cta - 1 - r);
-    cta_of[t] = c;
-    ++count[c];
-  }
-  std::vector<int32_t> start(n_cta + 1, 0);
-  for (int c = 0; c < n_cta; ++c) start[c + 1] = start[c] + count[c];
-  if (units) {
-    units->assign(4 * n, 0);
-    std::vector<int32_t> pos(start.begin(), start.end() - 1);
-    for (int64_t t = 0; t < n; ++t) {
-      const int64_t i = pos[cta_of[t]]++;
-      (*units)[4 * i + 0] = all[t].b;
-      (*units)[4 * i + 1] = all[t].h;
-      (*units)[4 * i + 2] = all[t].n;
-      (*units)[4 * i + 3] = all[t].cost;
+  // enumeration order: sequence, head, 128-key block; cost = query tiles visited.
+  // Equal costs (broadcast-Q) keep this order; unequal ones (self-attention,
+  // where a unit loops over its sequence's query tiles) come largest first so
+  // the snake deal balances them.
+  auto each = [&](auto&& fn) {
+    for (int b = 0; b < batch; ++b) {
+      const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+      const int64_t q_tiles = cdiv(nq > 0 ? nq : L, kKvBlock);
+      const int64_t nblk = cdiv(L, kKvBlock);
+      for (int h = 0; h < H; ++h)
+        for (int64_t blk = 0; blk < nblk; ++blk)
+          fn(b, h, static_cast<int32_t>(blk), static_cast<int32_t>(causal ? q_tiles - blk : q_tiles));
     }
-  }
-  if (cta_start) *cta_start = start;
-  return static_cast<int>(n);
+  };
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b)
+    n += static_cast<int64_t>(H) * cdiv(static_cast<int64_t>(offsets[b + 1]) - offsets[b], kKvBlock);
+  return deal_sorted(each, n, n_cta, units, cta_start);
 }
 
 int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<int32_t>* bpb,

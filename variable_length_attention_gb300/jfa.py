@@ -73,7 +73,7 @@ def load(path: str | None = None):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _host_offsets(offsets, offsets_host):
@@ -83,8 +83,16 @@ def _host_offsets(offsets, offsets_host):
     return h
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    """Handle of the current CUDA stream of the current device (the direct
+    query where this torch has it: it skips building a Stream object)."""
+    if _raw_stream is not None and _cur_device is not None:
+        return _raw_stream(_cur_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(name, st):
@@ -125,13 +133,14 @@ def _check_problem(q, k, v, offsets, offs_h, nq, *, o=None, dout=None, lse=None,
 
 
 def _workspace(op, offs_h, batch, nq, H, D, causal, bq, workspace, device):
-    need = load().jfa_workspace_size(op, offs_h.ctypes.data_as(ctypes.c_void_p), batch, nq, H, D, int(causal),
-                                     int(bq))
-    if need == 0 and batch >= 0:
-        need = 256
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-    return workspace, need
+    """The caller's workspace as given (the library checks its size and returns
+    JFA_ERR_WORKSPACE_TOO_SMALL), or a new one of the size the library asks for."""
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace: must be a contiguous CUDA tensor")
+        return workspace
+    need = load().jfa_workspace_size(op, offs_h.ctypes.data, batch, nq, H, D, int(causal), int(bq))
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=device)
 
 
 def jfa_workspace_size(op, offsets_host, batch, nq_broadcast, num_heads, head_dim, causal, broadcast_q):
@@ -169,10 +178,10 @@ def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0
     if not return_lse:
         lse = None
     _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
-    workspace, need = _workspace(JFA_OP_FWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    workspace = _workspace(JFA_OP_FWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
     st = L.jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
-                   offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv, D,
-                   float(scale), int(causal), int(bq), _ptr(workspace), workspace.numel(), _stream())
+                   offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast), H, Hkv, D,
+                   float(scale), int(causal), int(bq), workspace.data_ptr(), workspace.nbytes, _stream())
     _check("jfa_fwd", st)
     return out, lse
 
@@ -194,10 +203,10 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, 
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv)
-    workspace, need = _workspace(JFA_OP_BWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    workspace = _workspace(JFA_OP_BWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
     st = L.jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                   _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast),
-                   H, Hkv, D, float(scale), int(causal), int(bq), _ptr(workspace), workspace.numel(), _stream())
+                   _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast),
+                   H, Hkv, D, float(scale), int(causal), int(bq), workspace.data_ptr(), workspace.nbytes, _stream())
     _check("jfa_bwd", st)
     return dq, dk, dv
 
@@ -214,9 +223,9 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
         scale = 1.0 / math.sqrt(D)
     out = torch.empty_like(q) if out is None else out
     _check_problem(q, k, v, offsets, offs_h, 0, o=out)
-    workspace, need = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
-    st = L.block_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p),
-                          batch, int(max_len), H, D, float(scale), _ptr(workspace), workspace.numel(), _stream())
+    workspace = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    st = L.block_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(offsets), offs_h.ctypes.data,
+                          batch, int(max_len), H, D, float(scale), workspace.data_ptr(), workspace.nbytes, _stream())
     _check("block_attn_fwd", st)
     return out
 
@@ -236,10 +245,10 @@ def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check_problem(q, k, v, offsets, offs_h, 0, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
-    workspace, need = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    workspace = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     st = L.block_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(offsets), offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), H, D,
-                          float(scale), _ptr(workspace), workspace.numel(), _stream())
+                          _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), H, D,
+                          float(scale), workspace.data_ptr(), workspace.nbytes, _stream())
     _check("block_attn_bwd", st)
     return dq, dk, dv
 
@@ -328,7 +337,7 @@ def jfa_fwd_noalloc(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_bro
         out = torch.empty((o_rows, H, D), dtype=torch.bfloat16, device=q.device)
     _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
     st = L.jfa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
-                           offs_h.ctypes.data_as(ctypes.c_void_p), batch, int(max_len), int(nq_broadcast), H, Hkv,
+                           offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast), H, Hkv,
                            D, float(scale), int(causal), int(bq), _stream())
     _check("jfa_fwd_noalloc", st)
     return out, lse
