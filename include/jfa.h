@@ -213,14 +213,20 @@ int jfa_get_schedule(void);
 
 /*
  * Optional kernel timing (no counterpart on the pages; measurement support).
- * jfa_profile_enable(1) starts bracketing every library kernel launch with CUDA
- * events on its stream (and forgets earlier records); jfa_profile_enable(0)
- * stops it.  jfa_profile_read(kind, &ms, &n) synchronises on the recorded
- * events and returns the summed device time and the launch count of one kernel
- * kind: 0 forward, 1 backward prepass (Di), 2 backward main, 3 dQ convert,
- * 4 block forward, 5 block backward, 6 empty-sequence fill.
+ * jfa_profile_enable(1) starts counting every library kernel launch and
+ * bracketing it with CUDA events on its stream (and forgets earlier records);
+ * jfa_profile_enable(0) stops it.  jfa_profile_select(mask) limits the events
+ * to the kinds whose bit is set in mask (launches of the other kinds are still
+ * counted; the initial mask selects every kind; a mask outside [0, 2^7)
+ * returns JFA_ERR_INVALID_ARG), so a measurement can time one kernel without
+ * adding events around the rest.  jfa_profile_read(kind, &ms, &n) synchronises
+ * on the recorded events and returns the summed device time (0 for an
+ * unselected kind) and the launch count of one kernel kind: 0 forward,
+ * 1 backward prepass (Di), 2 backward main, 3 dQ convert, 4 block forward,
+ * 5 block backward, 6 empty-sequence fill.
  */
 int jfa_profile_enable(int on);
+int jfa_profile_select(int kind_mask);
 int jfa_profile_read(int kind, double* total_ms, int* launches);
 
 #ifdef __cplusplus

@@ -241,9 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row maximum: 4 independent partial maxima, two new values per step
+        float pm[4];
 #pragma unroll
-        for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 4; ++i) pm[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int c = 8; c < BN; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pm[i] = fmax3(pm[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), pm[3]);
         const float m_new = fmaxf(m_run, mx * sl2);
         if (m_new > m_run + kRescaleThreshold) {
           if (j > 0) {
@@ -262,16 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m_run = m_new;
         }
-        float sum = 0.f;
+        float ps[2] = {0.f, 0.f};  // 2 partial row sums
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
           const float p0 = ex2(fmaf(s[c], sl2, -m_run));
           const float p1 = ex2(fmaf(s[c + 1], sl2, -m_run));
-          sum += p0 + p1;
+          ps[(c / 2) & 1] += p0 + p1;
           pk[c / 2] = pack_bf16(p0, p1);
         }
-        l_run += sum;
+        l_run += ps[0] + ps[1];
         tmem_st32(tS + 0, pk);
         tmem_st32(tS + 32, pk + 32);
         tmem_wait_st();

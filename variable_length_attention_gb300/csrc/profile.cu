@@ -1,7 +1,9 @@
 // profile.cu -- optional per-kernel timing.  When enabled, every launch of a
-// library kernel is bracketed by two CUDA events recorded on the launch stream;
-// jfa_profile_read() synchronises on them and returns the summed device time and
-// the launch count per kernel kind.  Disabled (the default) it costs one branch.
+// library kernel is counted and, if its kind is selected (all kinds unless
+// jfa_profile_select() narrowed them), bracketed by two CUDA events recorded on
+// the launch stream; jfa_profile_read() synchronises on them and returns the
+// summed device time and the launch count per kernel kind.  Disabled (the
+// default) it costs one branch.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,13 +19,17 @@ struct Pair {
 };
 std::mutex g_mu;
 bool g_on = false;
+int g_mask = (1 << kNumKernelKinds) - 1;  // kinds whose launches get events
 std::vector<Pair> g_pool;
 std::vector<Pair> g_used[kNumKernelKinds];
+int g_count[kNumKernelKinds] = {};
 }  // namespace
 
 ProfileScope::ProfileScope(int kind, cudaStream_t stream) : kind_(kind), stream_(stream) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_on || kind < 0 || kind >= kNumKernelKinds) return;
+  ++g_count[kind];
+  if (!(g_mask & (1 << kind))) return;
   Pair p;
   if (!g_pool.empty()) {
     p = g_pool.back();
@@ -58,6 +64,14 @@ extern "C" int jfa_profile_enable(int on) {
     for (auto& p : v) g_pool.push_back(p);
     v.clear();
   }
+  for (int& c : g_count) c = 0;
+  return JFA_OK;
+}
+
+extern "C" int jfa_profile_select(int kind_mask) {
+  if (kind_mask < 0 || kind_mask >= (1 << kNumKernelKinds)) return JFA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_mask = kind_mask;
   return JFA_OK;
 }
 
@@ -72,6 +86,6 @@ extern "C" int jfa_profile_read(int kind, double* total_ms, int* launches) {
     t += ms;
   }
   *total_ms = t;
-  *launches = static_cast<int>(g_used[kind].size());
+  *launches = g_count[kind];
   return JFA_OK;
 }

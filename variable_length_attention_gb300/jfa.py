@@ -41,6 +41,7 @@ SIGNATURES = {
     "jfa_set_schedule": (_I, [_I]),
     "jfa_get_schedule": (_I, []),
     "jfa_profile_enable": (_I, [_I]),
+    "jfa_profile_select": (_I, [_I]),
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
 KERNEL_KINDS = {"fwd": 0, "bwd_prep": 1, "bwd_main": 2, "dq_convert": 3, "block_fwd": 4, "block_bwd": 5,
@@ -306,6 +307,17 @@ def jfa_get_schedule() -> int:
 def jfa_profile_enable(on: bool = True):
     """Start (or stop) bracketing every library kernel launch with CUDA events."""
     _check("jfa_profile_enable", load().jfa_profile_enable(int(on)))
+
+
+def jfa_profile_select(kinds=None):
+    """Limit the events to these kernel kinds (names or numbers; None = all)."""
+    if kinds is None:
+        mask = (1 << len(KERNEL_KINDS)) - 1
+    else:
+        mask = 0
+        for k in kinds:
+            mask |= 1 << (KERNEL_KINDS[k] if isinstance(k, str) else int(k))
+    _check("jfa_profile_select", load().jfa_profile_select(mask))
 
 
 def jfa_profile_read(kind) -> tuple[float, int]:
