@@ -59,6 +59,13 @@ namespace bwd {
 constexpr int BQ = 128;  // query rows per tile
 constexpr int BK = 128;  // keys per unit
 constexpr int kThreads = 512;
+// Registers per thread after setmaxnreg: the two P/dS warpgroups, the dQ/dK/dV
+// drain warpgroup, the MMA/loader warpgroup.  The sum must not exceed the
+// launch allocation (128 per thread at 512 threads); the launcher checks the
+// compiled count.
+constexpr int kRegPds = 128, kRegDrain = 160, kRegIssue = 96;
+constexpr int kRegTotal = 2 * 128 * kRegPds + 128 * kRegDrain + 128 * kRegIssue;
+static_assert(kRegTotal <= kThreads * 128, "register split exceeds the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -202,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8) {
     // -------------------------------------------------------- P^T and dS^T
     // register split 128 / 128 / 160 / 96 over the four warpgroups (65,536 total)
-    setmaxnreg_inc<128>();
+    setmaxnreg_inc<kRegPds>();
     const int wg = warp >> 2;              // query half
     const int k = threadIdx.x & 127;       // key row == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // -------------------------------------------------------- dQ reduction
-    setmaxnreg_inc<160>();
+    setmaxnreg_inc<kRegDrain>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0, dkv_ph = 0;
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 256) bulk_wait_all();
   } else {
-    setmaxnreg_dec<96>();
+    setmaxnreg_dec<kRegIssue>();
     if (warp == 12) {
       if (lane == 0) {
         // ------------------------------------------------------ MMA issuer
@@ -641,6 +648,9 @@ int launch_main(const BwdArgs& a) {
   auto kern = bwd_kernel<D, CAUSAL>;
   static bool attr_set = false;
   if (!attr_set) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return JFA_ERR_CUDA;
+    if (fa.numRegs * kThreads < kRegTotal) return JFA_ERR_UNSUPPORTED;  // the split could never be granted
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
       return JFA_ERR_CUDA;
     attr_set = true;

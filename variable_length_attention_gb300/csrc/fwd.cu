@@ -40,6 +40,13 @@ namespace fwd {
 constexpr int BM = 128;  // rows per query tile
 constexpr int BN = 128;  // keys per K/V block
 constexpr int kThreads = 512;
+// Registers per thread after the warpgroups' setmaxnreg: two softmax
+// warpgroups, the epilogue warpgroup, the MMA/loader warpgroup.  Their sum must
+// not exceed what the CTA is launched with (128 per thread at 512 threads), or
+// setmaxnreg.inc would wait forever; the launcher checks the compiled count.
+constexpr int kRegSoftmax = 176, kRegEpilogue = 64, kRegIssue = 96;
+constexpr int kRegTotal = 2 * 128 * kRegSoftmax + 128 * kRegEpilogue + 128 * kRegIssue;
+static_assert(kRegTotal <= kThreads * 128, "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<176>();
+    setmaxnreg_inc<kRegSoftmax>();
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = threadIdx.x & 127;       // TMEM lane == row of the tile
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -251,7 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) pm[i] = fmax3(pm[i], s[c + 2 * i], s[c + 2 * i + 1]);
         const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]), pm[3]);
         const float m_new = fmaxf(m_run, mx * sl2);
-        if (m_new > m_run + kRescaleThreshold) {
+        // The decision is made per warp (any lane over the threshold moves the
+        // whole warp's maxima), because the TMEM accesses below must be
+        // executed by all 32 lanes together; moving a maximum that grew by
+        // less is exact all the same.
+        if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
           if (j > 0) {
             const float alpha = ex2(m_run - m_new);
             l_run *= alpha;
@@ -268,16 +279,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m_run = m_new;
         }
-        float ps[2] = {0.f, 0.f};  // 2 partial row sums
+        // s * scale * log2(e) - m two columns per instruction, and the row sum
+        // kept as two paired partial sums
+        const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_run, -m_run);
+        uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
-          const float p0 = ex2(fmaf(s[c], sl2, -m_run));
-          const float p1 = ex2(fmaf(s[c + 1], sl2, -m_run));
-          ps[(c / 2) & 1] += p0 + p1;
+          float x0, x1;
+          f32x2_split(ffma2(f32x2(s[c], s[c + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          ps2[(c / 2) & 1] = fadd2(ps2[(c / 2) & 1], f32x2(p0, p1));
           pk[c / 2] = pack_bf16(p0, p1);
         }
-        l_run += ps[0] + ps[1];
+        {
+          float a0, a1, b0, b1;
+          f32x2_split(ps2[0], a0, a1);
+          f32x2_split(ps2[1], b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
+        }
         tmem_st32(tS + 0, pk);
         tmem_st32(tS + 32, pk + 32);
         tmem_wait_st();
@@ -294,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ epilogue
-    setmaxnreg_dec<64>();
+    setmaxnreg_dec<kRegEpilogue>();
     const int row = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t phase = 0;
@@ -340,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       phase ^= 1;
     }
   } else {
-    setmaxnreg_dec<96>();
+    setmaxnreg_dec<kRegIssue>();
     if (warp == 12 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
@@ -515,6 +535,9 @@ int launch_impl(const FwdArgs& a) {
   auto kern = fwd_kernel<D, CAUSAL>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return JFA_ERR_CUDA;
+    if (fa.numRegs * kThreads < kRegTotal) return JFA_ERR_UNSUPPORTED;  // the split could never be granted
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
       return JFA_ERR_CUDA;
     attr_set = true;
