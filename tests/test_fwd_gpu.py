@@ -79,3 +79,40 @@ def test_repeatable_and_no_lse():
     torch.cuda.synchronize()
     assert none is None
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_growth(causal):
+    """Scores that climb along the keys, for some rows and not others: the running
+    maximum of those rows grows by more than 2^8 several times, so the O rescale
+    path runs, with rows of one warp taking different decisions ("TLX Block
+    Attention", section 2.1: the correction factor when m grows)."""
+    import oracle
+    from tests.parity import rel_l2, to64
+    lengths = [700, 300, 129]
+    H, D = 2, 64
+    offs_h = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(offs_h[-1])
+    g = torch.Generator().manual_seed(4242 + int(causal))
+    q = torch.randn(T, H, D, generator=g)
+    k = torch.randn(T, H, D, generator=g)
+    v = torch.randn(T, H, D, generator=g)
+    q[:, :, 0] = torch.where(torch.arange(T) % 2 == 0, 3.0, 0.0)[:, None]  # every other row climbs
+    for b in range(len(lengths)):
+        j = torch.arange(lengths[b], dtype=torch.float32)
+        k[offs_h[b]:offs_h[b + 1], :, 0] = (0.07 * j)[:, None]
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    scale = 1.0 / np.sqrt(D)
+    offs = torch.from_numpy(offs_h).cuda()
+    o, lse = V.jfa_fwd(q.cuda(), k.cuda(), v.cuda(), offs, offs_h, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref, _ = oracle.attn_fwd(to64(q), to64(k), to64(v), offs_h, scale=scale, causal=causal)
+    o_g, lse_g = to64(o), to64(lse)
+    res = {"o_max_abs": float(np.max(np.abs(o_g - o_ref))), "o_rel_l2": rel_l2(o_g, o_ref),
+           "lse_max_abs": float(np.max(np.abs(lse_g - lse_ref))), "lse_inf_match": True,
+           "finite": bool(np.all(np.isfinite(o_g)))}
+    # the growth is real: for a climbing row near the end of the first sequence, the
+    # maximum over all its keys exceeds the first block's by more than two steps of 2^8
+    s_row = to64(k[:lengths[0] - 1, 0]) @ to64(q[lengths[0] - 2, 0]) * scale
+    assert (s_row.max() - s_row[:128].max()) * np.log2(np.e) > 16.0
+    assert_fwd_ok(res)
