@@ -225,6 +225,19 @@ int jfa_get_schedule(void);
  * 1 backward prepass (Di), 2 backward main, 3 dQ convert, 4 block forward,
  * 5 block backward, 6 empty-sequence fill.
  */
+/*
+ * Failure-path self-test (no counterpart on the pages; failure detection).
+ * Launches on `stream` one CTA that waits, through the same bounded mbarrier
+ * wait every kernel of this library uses, on a barrier that nothing completes.
+ * The wait gives up after its limit (2 s), the CTA records
+ * JFA_ERR_DEVICE_TIMEOUT in the error word at the start of `workspace` (device
+ * memory, at least 4 bytes, owned by the caller) and exits; no fault, no trap,
+ * and the context stays usable.  Returns JFA_ERR_INVALID_ARG for a null or too
+ * small workspace, JFA_ERR_CUDA if the launch fails, else JFA_OK; read the
+ * outcome with jfa_device_status(workspace, stream).
+ */
+int jfa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
 int jfa_profile_enable(int on);
 int jfa_profile_select(int kind_mask);
 int jfa_profile_read(int kind, double* total_ms, int* launches);

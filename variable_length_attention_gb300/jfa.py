@@ -41,6 +41,7 @@ SIGNATURES = {
     "jfa_set_schedule": (_I, [_I]),
     "jfa_get_schedule": (_I, []),
     "jfa_profile_enable": (_I, [_I]),
+    "jfa_selftest_wait_timeout": (_I, [_P, _S, _P]),
     "jfa_profile_select": (_I, [_I]),
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
@@ -302,6 +303,15 @@ def jfa_set_schedule(mode):
 
 def jfa_get_schedule() -> int:
     return load().jfa_get_schedule()
+
+
+def jfa_selftest_wait_timeout(workspace) -> None:
+    """Launch the bounded-wait self-test into ``workspace`` (a CUDA uint8 tensor);
+    jfa_device_status(workspace) then reports JFA_ERR_DEVICE_TIMEOUT."""
+    if not workspace.is_cuda:
+        raise ValueError("workspace: must be a CUDA tensor")
+    _check("jfa_selftest_wait_timeout",
+           load().jfa_selftest_wait_timeout(workspace.data_ptr(), workspace.nbytes, _stream()))
 
 
 def jfa_profile_enable(on: bool = True):
