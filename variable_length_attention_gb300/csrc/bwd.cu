@@ -144,7 +144,7 @@ struct Bars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty;
-  uint64_t stg_full, stg_free;  // dQ staging: rows written by all 128 drain threads / read out by TMA
+  uint64_t stg_full[2], stg_free[2];  // dQ staging slots: rows written by the 128 drain threads / read out by TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -190,8 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_empty, 4);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 4);
-    mbar_init(&bars->stg_full, 128);
-    mbar_init(&bars->stg_free, 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&bars->stg_full[s2], 128);
+      mbar_init(&bars->stg_free[s2], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<kRegDrain>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t ph = 0, q_it = 0, full_ph = 0, free_ph = 0, dkv_ph = 0;
+    uint32_t ph = 0, q_it = 0, dkv_ph = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
@@ -356,41 +358,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
         // Stage the rows in shared memory and reduce-add them into the fp32
-        // accumulator with TMA, 64 columns (two 32-column swizzled boxes) per
-        // round (aixai.ru summary, "dQ epilogue": staged writeback).  Rows past
-        // the end of the query set are exactly zero (their P is zero), so adding
-        // them is harmless, and TMA clips rows past the end of the tensor.
+        // accumulator with TMA (aixai.ru summary, "dQ epilogue": staged
+        // writeback): one 32-column swizzled box per round, alternating between
+        // two 16 KB slots, so the rows of round g are written while TMA still
+        // reads round g-1; one box is read at a time (more in flight slowed the
+        // TMA loads that share the engine).  Rows past the end of the query set
+        // are exactly zero (their P is zero), so adding them is harmless, and
+        // TMA clips rows past the end of the tensor.
         uint8_t* stage = smem + C::OFF_STG;
+        const uint32_t stage_u32 = smem_u32(stage);
         const int y = u.q_base + BQ * i;
+        uint32_t g = q_it * (D / 32);  // rounds so far (the same count in every drain thread)
 #pragma unroll
-        for (int rnd = 0; rnd < D / 64; ++rnd) {
-          if (rnd > 0 || q_it > 0) {  // the previous round's boxes must have been read out
+        for (int rnd = 0; rnd < D / 32; ++rnd, ++g) {
+          const uint32_t slot = g & 1;
+          if (g >= 2) {  // slot last read by the TMA of round g-2
             if (threadIdx.x == 256) {
-              bulk_wait_read_all();
-              mbar_arrive(&bars->stg_free);
+              bulk_wait_read_all_but_newest();
+              mbar_arrive(&bars->stg_free[slot]);
             }
-            if (!mbar_wait(&bars->stg_free, free_ph, ab)) goto done;
-            free_ph ^= 1;
+            if (!mbar_wait(&bars->stg_free[slot], ((g >> 1) - 1) & 1, ab)) goto done;
           }
+          const uint32_t row = stage_u32 + slot * 16384 + r * 128;
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            uint8_t* row = stage + b * 16384 + r * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int c = 64 * rnd + 32 * b + 4 * j;
-              const uint32_t addr = smem_u32(row + ((j ^ (r & 7)) << 4));
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[c]), "r"(v[c + 1]),
-                           "r"(v[c + 2]), "r"(v[c + 3])
-                           : "memory");
-            }
+          for (int j = 0; j < 8; ++j) {
+            const int c = 32 * rnd + 4 * j;
+            const uint32_t addr = row + ((j ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[c]), "r"(v[c + 1]),
+                         "r"(v[c + 2]), "r"(v[c + 3])
+                         : "memory");
           }
           fence_proxy_async_smem();
-          mbar_arrive(&bars->stg_full);
-          if (!mbar_wait(&bars->stg_full, full_ph, ab)) goto done;
-          full_ph ^= 1;
+          mbar_arrive(&bars->stg_full[slot]);
+          if (!mbar_wait(&bars->stg_full[slot], (g >> 1) & 1, ab)) goto done;
           if (threadIdx.x == 256) {
-            tma_reduce_add_2d(&tm_dq, stage, u.h * D + 64 * rnd, y);
-            tma_reduce_add_2d(&tm_dq, stage + 16384, u.h * D + 64 * rnd + 32, y);
+            bulk_wait_read_all();  // one box being read at a time
+            tma_reduce_add_2d(&tm_dq, stage + slot * 16384, u.h * D + 32 * rnd, y);
             bulk_commit_group();
           }
         }
