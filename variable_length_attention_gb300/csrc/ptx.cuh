@@ -276,18 +276,16 @@ __device__ __forceinline__ void clc_try_cancel(void* resp16, uint64_t* bar) {
 }
 // Decode a response: returns the x index of the cancelled CTA, or -1 if none was.
 __device__ __forceinline__ int clc_cancelled_x(const void* resp16) {
-  uint32_t ok = 0, x = 0, y = 0, z = 0;
+  uint32_t ok = 0, x = 0;
   asm volatile(
       "{\n .reg .pred p;\n .reg .b128 r;\n"
-      " ld.shared.b128 r, [%4];\n"
+      " ld.shared.b128 r, [%2];\n"
       " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
-      " selp.u32 %3, 1, 0, p;\n"
-      " @p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, %1, %2, _}, r;\n}\n"
-      : "=r"(x), "=r"(y), "=r"(z), "=r"(ok)
+      " selp.u32 %1, 1, 0, p;\n"
+      " @p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, _, _, _}, r;\n}\n"
+      : "=r"(x), "=r"(ok)
       : "r"(smem_u32(resp16))
       : "memory");
-  (void)y;
-  (void)z;
   return ok ? static_cast<int>(x) : -1;
 }
 
