@@ -66,18 +66,24 @@ __device__ __forceinline__ Blk locate(const Params& p, int g) {
   return r;
 }
 
+// Operands come in two rings: Q and K of a tile together (released as soon as
+// its score GEMM has read them) and V on its own (released after the PV GEMM),
+// so more bytes are in flight from HBM than with whole Q/K/V stages.
 template <int D>
 struct FwdCfg {
   static constexpr int TILE = 128 * D * 2;         // 128 rows x D, bf16
   static constexpr int CHUNK = 128 * 128;          // 64 columns x 128 rows
-  static constexpr int STAGE = 3 * TILE;           // Q, K, V
-  static constexpr int NST = D == 128 ? 2 : 4;
-  static constexpr int OFF_BAR = NST * STAGE;
+  static constexpr int NQK = 2;                    // Q+K slots
+  static constexpr int NV = D == 128 ? 3 : 6;      // V slots (D=64: 160 KB in all measured
+                                                   // faster than filling the 227 KB)
+  static constexpr int OFF_V = NQK * 2 * TILE;
+  static constexpr int OFF_BAR = OFF_V + NV * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct FwdBars {
-  uint64_t full[4], empty[4];
+  uint64_t qk_full[2], qk_empty[2], v_full[6], v_empty[6];
   uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -100,13 +106,18 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::OFF_BAR);
+  static_assert(sizeof(FwdBars) <= 256, "barrier block");
   const int warp = warp_id(), lane = lane_id();
   const int t0 = p.prog_start[blockIdx.x], t1 = p.prog_start[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+    for (int s = 0; s < C::NQK; ++s) {
+      mbar_init(&bars->qk_full[s], 1);
+      mbar_init(&bars->qk_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -130,50 +141,85 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- loader
-    for (int t = t0; t < t1; ++t) {
-      const int i = t - t0, st = i % C::NST;
-      if (!mbar_wait(&bars->empty[st], ((i / C::NST) & 1) ^ 1, ab)) break;
-      const int pair = t / p.H, h = t % p.H;
-      const Blk a = locate(p, 2 * pair);
-      Blk b = locate(p, 2 * pair + 1);
-      if (b.len == 0) b = a;  // nothing there: reload block a, masked later
-      uint8_t* base = smem + st * C::STAGE;
-      mbar_expect_tx(&bars->full[st], C::STAGE);
-      load_half<D>(&tm_q, &bars->full[st], base, 0, h, a.row0);
-      load_half<D>(&tm_q, &bars->full[st], base, 1, h, b.row0);
-      load_half<D>(&tm_k, &bars->full[st], base + C::TILE, 0, h, a.row0);
-      load_half<D>(&tm_k, &bars->full[st], base + C::TILE, 1, h, b.row0);
-      load_half<D>(&tm_v, &bars->full[st], base + 2 * C::TILE, 0, h, a.row0);
-      load_half<D>(&tm_v, &bars->full[st], base + 2 * C::TILE, 1, h, b.row0);
+    // In the order the tensor core consumes them: QK(0), then QK(i+1), V(i).
+    // Consecutive tiles share their pair of blocks across the heads, so the
+    // block search runs once per pair, not per load.
+    const int n = t1 - t0;
+    int cached_pair = -1;
+    Blk ca{0, 0}, cb{0, 0};
+    auto rows = [&](int i, Blk& a, Blk& b, int& h) {
+      const int t = t0 + i, pair = t / p.H;
+      h = t % p.H;
+      if (pair != cached_pair) {
+        cached_pair = pair;
+        ca = locate(p, 2 * pair);
+        cb = locate(p, 2 * pair + 1);
+        if (cb.len == 0) cb = ca;  // nothing there: reload block a, masked later
+      }
+      a = ca;
+      b = cb;
+    };
+    auto load_qk = [&](int i) -> bool {
+      const int st = i % C::NQK;
+      if (!mbar_wait(&bars->qk_empty[st], ((i / C::NQK) & 1) ^ 1, ab)) return false;
+      Blk a, b;
+      int h;
+      rows(i, a, b, h);
+      uint8_t* base = smem + st * 2 * C::TILE;
+      mbar_expect_tx(&bars->qk_full[st], 2 * C::TILE);
+      load_half<D>(&tm_q, &bars->qk_full[st], base, 0, h, a.row0);
+      load_half<D>(&tm_q, &bars->qk_full[st], base, 1, h, b.row0);
+      load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 0, h, a.row0);
+      load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 1, h, b.row0);
+      return true;
+    };
+    auto load_v = [&](int i) -> bool {
+      const int st = i % C::NV;
+      if (!mbar_wait(&bars->v_empty[st], ((i / C::NV) & 1) ^ 1, ab)) return false;
+      Blk a, b;
+      int h;
+      rows(i, a, b, h);
+      uint8_t* base = smem + C::OFF_V + st * C::TILE;
+      mbar_expect_tx(&bars->v_full[st], C::TILE);
+      load_half<D>(&tm_v, &bars->v_full[st], base, 0, h, a.row0);
+      load_half<D>(&tm_v, &bars->v_full[st], base, 1, h, b.row0);
+      return true;
+    };
+    if (n > 0 && load_qk(0)) {
+      for (int i = 0; i < n; ++i) {
+        if (i + 1 < n && !load_qk(i + 1)) break;
+        if (!load_v(i)) break;
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, D, 0, 1);
     const uint32_t sb = smem_u32(smem);
     auto issue_s = [&](int i) {
-      const int st = i % C::NST, b = i & 1;
-      const uint32_t q = sb + st * C::STAGE, k = q + C::TILE;
+      const int st = i % C::NQK, b = i & 1;
+      const uint32_t q = sb + st * 2 * C::TILE, k = q + C::TILE;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
         mma_ss(tmem + 256 * b, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_s, kk > 0);
       }
       mma_commit(&bars->s_full[b]);
+      mma_commit(&bars->qk_empty[st]);  // Q and K are read: the slot may refill
     };
     auto issue_pv = [&](int i) {
-      const int st = i % C::NST, b = i & 1;
-      const uint32_t v = sb + st * C::STAGE + 2 * C::TILE;
+      const int st = i % C::NV, b = i & 1;
+      const uint32_t v = sb + C::OFF_V + st * C::TILE;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ts(tmem + 256 * b + 128, tmem + 256 * b + 8 * kk, sdesc_sw128(v + kk * 2048, C::CHUNK, 1024), id_o,
                kk > 0);
       mma_commit(&bars->o_full[b]);
-      mma_commit(&bars->empty[st]);
+      mma_commit(&bars->v_empty[st]);
     };
     const int n = t1 - t0;
     for (int i = 0; i <= n; ++i) {
       if (i < n) {  // S of tile i, once its operands landed and its TMEM buffer is free
-        if (!mbar_wait(&bars->full[i % C::NST], (i / C::NST) & 1, ab)) break;
+        if (!mbar_wait(&bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
         if (!mbar_wait(&bars->t_free[i & 1], ((i >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after();
         issue_s(i);
@@ -181,6 +227,7 @@ __global__ void __launch_bounds__(384, 1)
       if (i > 0) {  // PV of tile i-1
         const int j = i - 1;
         if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, ab)) break;
+        if (!mbar_wait(&bars->v_full[j % C::NV], (j / C::NV) & 1, ab)) break;
         tc_fence_after();
         issue_pv(j);
       }
@@ -269,21 +316,25 @@ done:
 }
 
 // ------------------------------------------------------------------ backward
+// Operands by lifetime: Q and K (read until the last GEMM) in a 2-slot ring, so
+// the next tile's pair loads during this tile; V and dO (last read by the dV
+// GEMM) in one slot that refills from the middle of the tile; P and then dS
+// share one buffer (dS is written once the dV GEMM has read P).
 template <int D>
 struct BwdCfg {
   static constexpr int TILE = 128 * D * 2;
   static constexpr int CHUNK = 128 * 128;
-  static constexpr int STAGE = 4 * TILE;            // Q, K, V, dO
-  static constexpr int NST = D == 128 ? 1 : 2;
-  static constexpr int OFF_P = NST * STAGE;         // P  [128 q][128 keys] bf16
-  static constexpr int OFF_DS = OFF_P + 32768;      // dS [128 q][128 keys] bf16
-  static constexpr int OFF_BAR = OFF_DS + 32768;
+  static constexpr int NQK = 2;
+  static constexpr int OFF_V = NQK * 2 * TILE;
+  static constexpr int OFF_DO = OFF_V + TILE;
+  static constexpr int OFF_PDS = OFF_DO + TILE;     // P, then dS: [128 q][128 keys] bf16
+  static constexpr int OFF_BAR = OFF_PDS + 32768;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 
 struct BwdBars {
-  uint64_t full[2], empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full, acc_full, t_free;
+  uint64_t qk_full[2], qk_empty[2], vdo_full, vdo_empty;
+  uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -312,12 +363,15 @@ __global__ void __launch_bounds__(256, 1)
   constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+    for (int s = 0; s < C::NQK; ++s) {
+      mbar_init(&bars->qk_full[s], 1);
+      mbar_init(&bars->qk_empty[s], 1);
     }
+    mbar_init(&bars->vdo_full, 1);
+    mbar_init(&bars->vdo_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_used, 1);
     mbar_init(&bars->p_full, 4);
     mbar_init(&bars->ds_full, 4);
     mbar_init(&bars->acc_full, 1);
@@ -338,32 +392,65 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- loader
-    for (int t = t0; t < t1; ++t) {
-      const int i = t - t0, st = i % C::NST;
-      if (!mbar_wait(&bars->empty[st], ((i / C::NST) & 1) ^ 1, ab)) break;
-      const int pair = t / p.H, h = t % p.H;
-      const Blk a = locate(p, 2 * pair);
-      Blk b = locate(p, 2 * pair + 1);
-      if (b.len == 0) b = a;
-      uint8_t* base = smem + st * C::STAGE;
-      mbar_expect_tx(&bars->full[st], C::STAGE);
-      const CUtensorMap* maps[4] = {&tm_q, &tm_k, &tm_v, &tm_do};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        load_half<D>(maps[m], &bars->full[st], base + m * C::TILE, 0, h, a.row0);
-        load_half<D>(maps[m], &bars->full[st], base + m * C::TILE, 1, h, b.row0);
+    // Order: QK(0), VdO(0), then QK(i+1) (its slot was freed by tile i-1) and
+    // VdO(i+1) (free once tile i's dV has run).  The block search runs once per
+    // pair of blocks, shared by the pair's heads.
+    const int n = t1 - t0;
+    int cached_pair = -1;
+    Blk ca{0, 0}, cb{0, 0};
+    auto rows = [&](int i, Blk& a, Blk& b, int& h) {
+      const int t = t0 + i, pair = t / p.H;
+      h = t % p.H;
+      if (pair != cached_pair) {
+        cached_pair = pair;
+        ca = locate(p, 2 * pair);
+        cb = locate(p, 2 * pair + 1);
+        if (cb.len == 0) cb = ca;
       }
+      a = ca;
+      b = cb;
+    };
+    auto load_qk = [&](int i) -> bool {
+      const int st = i % C::NQK;
+      if (!mbar_wait(&bars->qk_empty[st], ((i / C::NQK) & 1) ^ 1, ab)) return false;
+      Blk a, b;
+      int h;
+      rows(i, a, b, h);
+      uint8_t* base = smem + st * 2 * C::TILE;
+      mbar_expect_tx(&bars->qk_full[st], 2 * C::TILE);
+      load_half<D>(&tm_q, &bars->qk_full[st], base, 0, h, a.row0);
+      load_half<D>(&tm_q, &bars->qk_full[st], base, 1, h, b.row0);
+      load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 0, h, a.row0);
+      load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 1, h, b.row0);
+      return true;
+    };
+    auto load_vdo = [&](int i) -> bool {
+      if (!mbar_wait(&bars->vdo_empty, (i & 1) ^ 1, ab)) return false;
+      Blk a, b;
+      int h;
+      rows(i, a, b, h);
+      mbar_expect_tx(&bars->vdo_full, 2 * C::TILE);
+      load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 0, h, a.row0);
+      load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 1, h, b.row0);
+      load_half<D>(&tm_do, &bars->vdo_full, smem + C::OFF_DO, 0, h, a.row0);
+      load_half<D>(&tm_do, &bars->vdo_full, smem + C::OFF_DO, 1, h, b.row0);
+      return true;
+    };
+    if (n > 0 && load_qk(0) && load_vdo(0)) {
+      for (int i = 0; i + 1 < n; ++i)
+        if (!load_qk(i + 1) || !load_vdo(i + 1)) break;
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t id_s = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
     const uint32_t id_kv = idesc_bf16(128, D, 1, 1);    // dV = P^T dO, dK = dS^T Q
     const uint32_t id_q = idesc_bf16(128, D, 0, 1);     // dQ = dS K
-    const uint32_t sP = smem_u32(smem + C::OFF_P), sDS = smem_u32(smem + C::OFF_DS);
+    const uint32_t sP = smem_u32(smem + C::OFF_PDS), sDS = sP;
+    const uint32_t v = smem_u32(smem + C::OFF_V), dO = smem_u32(smem + C::OFF_DO);
     for (int i = 0; i < t1 - t0; ++i) {
-      const int st = i % C::NST;
-      const uint32_t q = smem_u32(smem + st * C::STAGE), k = q + C::TILE, v = q + 2 * C::TILE, dO = q + 3 * C::TILE;
-      if (!mbar_wait(&bars->full[st], (i / C::NST) & 1, ab)) break;
+      const int st = i % C::NQK;
+      const uint32_t q = smem_u32(smem + st * 2 * C::TILE), k = q + C::TILE;
+      if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
       if (!mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
       tc_fence_after();
 #pragma unroll
@@ -372,6 +459,8 @@ __global__ void __launch_bounds__(256, 1)
         mma_ss(tmem + COL_S, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_s, kk > 0);
       }
       mma_commit(&bars->s_full);
+      if (!mbar_wait(&bars->vdo_full, i & 1, ab)) break;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
@@ -385,6 +474,8 @@ __global__ void __launch_bounds__(256, 1)
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tmem + COL_DV, sdesc_sw128(sP + kk * 2048, C::CHUNK, 1024), sdesc_sw128(dO + kk * 2048, C::CHUNK, 1024),
                id_kv, kk > 0);
+      mma_commit(&bars->vdo_empty);  // V and dO are read: the next tile's may load
+      mma_commit(&bars->p_used);     // P is read: the dS phase may overwrite it
       // dK = dS^T Q into the dP columns, dQ = dS K into the S columns
       if (!mbar_wait(&bars->ds_full, i & 1, ab)) break;
       tc_fence_after();
@@ -399,7 +490,7 @@ __global__ void __launch_bounds__(256, 1)
                kk > 0);
       }
       mma_commit(&bars->acc_full);
-      mma_commit(&bars->empty[st]);
+      mma_commit(&bars->qk_empty[st]);
     }
     mma_commit(&bars->drain);
     const uint64_t tw = global_timer_ns();
@@ -410,8 +501,8 @@ __global__ void __launch_bounds__(256, 1)
     const int r = threadIdx.x & 127;
     const int half = r >> 6, rr = r & 63;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint8_t* sP = smem + C::OFF_P;
-    uint8_t* sDS = smem + C::OFF_DS;
+    uint8_t* sP = smem + C::OFF_PDS;
+    uint8_t* sDS = sP;  // the same buffer: dS goes in once the dV GEMM has read P
     const float sl2 = p.scale_log2;
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
     for (int i = 0; i < t1 - t0; ++i) {
@@ -468,15 +559,14 @@ __global__ void __launch_bounds__(256, 1)
         float di = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) di = fmaf(pr[c], __uint_as_float(dr[c]), di);
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2)
+          w[c / 2] = pack_bf16(pr[c] * (__uint_as_float(dr[c]) - di), pr[c + 1] * (__uint_as_float(dr[c + 1]) - di));
+        if (!mbar_wait(&bars->p_used, i & 1, ab)) goto done;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * j + 2 * e;
-            w[e] = pack_bf16(pr[c] * (__uint_as_float(dr[c]) - di), pr[c + 1] * (__uint_as_float(dr[c + 1]) - di));
-          }
-          st_row_piece(sDS, r, half, j, w);
+          st_row_piece(sDS, r, half, j, w + 4 * j);
           st_row_piece(sDS, r, 1 - half, j, zero);
         }
       }
