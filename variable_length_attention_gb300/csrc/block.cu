@@ -335,6 +335,7 @@ struct BwdCfg {
 struct BwdBars {
   uint64_t qk_full[2], qk_empty[2], vdo_full, vdo_empty;
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
+  uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -352,7 +353,8 @@ template <int D>
 __global__ void __launch_bounds__(256, 1)
     block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const Params p) {
+                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const Params p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -372,6 +374,8 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_used, 1);
+    mbar_init(&bars->stg_full, 128);
+    mbar_init(&bars->stg_free, 1);
     mbar_init(&bars->p_full, 4);
     mbar_init(&bars->ds_full, 4);
     mbar_init(&bars->acc_full, 1);
@@ -505,6 +509,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* sDS = sP;  // the same buffer: dS goes in once the dV GEMM has read P
     const float sl2 = p.scale_log2;
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
+    uint32_t stg_full_ph = 0, stg_free_ph = 0;
     for (int i = 0; i < t1 - t0; ++i) {
       const int t = t0 + i;
       const int pair = t / p.H, h = t % p.H;
@@ -574,39 +579,118 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full);
-      // epilogue: row r is query r for dQ and key r for dK, dV (same block, same token)
-      if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
-      tc_fence_after();
-      {
-        const bool valid = rr < blk.len;
-        const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
-#pragma unroll 1
-        for (int which = 0; which < 3; ++which) {
-          const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
-          const float mul = which == 2 ? 1.0f : p.scale;
-          __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_addr + col + c, v);
-            tmem_wait_ld();
-            reg_fence<32>(v);
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-            if (valid) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      if constexpr (D == 128) {
+        // epilogue: row r is query r for dQ and key r for dK, dV (same block, same token).
+        // Each result is staged as bf16 rows in the P/dS buffer (free once dK and dQ
+        // have read dS) and written by TMA, one 64-row half at a time; a half whose
+        // block is shorter than 64 rows is written row by row instead, so no rows
+        // of the next block are touched.
+        // thread 128 (row 0, block a) issues the stores; it also needs block b
+        const Blk blk_a = blk, blk_b = threadIdx.x == 128 ? locate(p, 2 * pair + 1) : blk;
+        if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
+        tc_fence_after();
+        {
+          const bool valid = rr < blk.len;
+          const bool full_half = blk.len == kBlk;
+          const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+  #pragma unroll 1
+          for (int which = 0; which < 3; ++which) {
+            const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
+            const float mul = which == 2 ? 1.0f : p.scale;
+            const CUtensorMap* tm_out = which == 0 ? &tm_dq : (which == 1 ? &tm_dk : &tm_dv);
+            __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+            if (which > 0) {  // the previous result's boxes must have been read out
+              if (threadIdx.x == 128) {
+                bulk_wait_read_all();
+                mbar_arrive(&bars->stg_free);
+              }
+              if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
+              stg_free_ph ^= 1;
+            }
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_addr + col + c, v);
+              tmem_wait_ld();
+              reg_fence<32>(v);
+              uint32_t w[16];
+  #pragma unroll
+              for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+              // columns c..c+31: pieces (c%64)/8 .. (c%64)/8+3 of the 64-column box c/64
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) st_row_piece(sP, r, c / 64, (c % 64) / 8 + e, w + 4 * e);
+              if (valid && !full_half) {
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              }
+            }
+            if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->t_free);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->stg_full);
+            if (!mbar_wait(&bars->stg_full, stg_full_ph, ab)) goto done;
+            stg_full_ph ^= 1;
+            if (threadIdx.x == 128) {
+  #pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const Blk bk = hf == 0 ? blk_a : blk_b;
+                if (bk.len != kBlk) continue;
+  #pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc)
+                  tma_store_2d(tm_out, smem + C::OFF_PDS + cc * 16384 + hf * 8192, h * D + 64 * cc, bk.row0);
+              }
+              bulk_commit_group();
             }
           }
+          // the next tile's P goes into the same buffer: wait for the last boxes
+          if (threadIdx.x == 128) {
+            bulk_wait_read_all();
+            mbar_arrive(&bars->stg_free);
+          }
+          if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
+          stg_free_ph ^= 1;
+        }
+      } else {
+        // epilogue (D=64): row r is query r for dQ and key r for dK, dV; each thread
+        // writes its rows directly (at this head size the staged path measured slower)
+        if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
+        tc_fence_after();
+        {
+          const bool valid = rr < blk.len;
+          const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+  #pragma unroll 1
+          for (int which = 0; which < 3; ++which) {
+            const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
+            const float mul = which == 2 ? 1.0f : p.scale;
+            __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_addr + col + c, v);
+              tmem_wait_ld();
+              reg_fence<32>(v);
+              uint32_t w[16];
+  #pragma unroll
+              for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+              if (valid) {
+  #pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->t_free);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->t_free);
     }
+    if (threadIdx.x == 128) bulk_wait_all();  // every store has landed before the CTA exits
   }
 done:
   __syncwarp();
@@ -654,12 +738,15 @@ template <int D>
 int launch_bwd_impl(const BlockArgs& a) {
   using C = BwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   const uint64_t inner = static_cast<uint64_t>(a.H) * D;
   int st = make_map_2d(&tq, a.q, inner, a.rows, 64, kBlk);
   if (st == JFA_OK) st = make_map_2d(&tk, a.k, inner, a.rows, 64, kBlk);
   if (st == JFA_OK) st = make_map_2d(&tv, a.v, inner, a.rows, 64, kBlk);
   if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tdq, a.dq, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, inner, a.rows, 64, kBlk);
+  if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, inner, a.rows, 64, kBlk);
   if (st != JFA_OK) return st;
   static bool attr = false;
   if (!attr) {
@@ -682,7 +769,7 @@ int launch_bwd_impl(const BlockArgs& a) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   ProfileScope prof(kKindBlockBwd, a.stream);
-  block_bwd_kernel<D><<<a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, p);
+  block_bwd_kernel<D><<<a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

@@ -133,6 +133,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
       "r"(smem_u32(src)), "r"(x), "r"(y)
       : "memory");
 }
+// 2D tiled store from shared memory into global memory, tracked as a bulk
+// async-group of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the issuing thread's bulk groups have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
