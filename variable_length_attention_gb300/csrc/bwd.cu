@@ -145,6 +145,7 @@ struct Bars {
   uint64_t q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty;
   uint64_t stg_full[2], stg_free[2];  // dQ staging slots: rows written by the 128 drain threads / read out by TMA
+  uint64_t kvst_full, kvst_free;      // the same buffer holding a bf16 dK or dV tile for a TMA store
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -154,7 +155,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dq, const Params p) {
+               const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+               const __grid_constant__ CUtensorMap tm_dv, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023) != 0) {  // the layout below needs 1024-byte alignment
@@ -190,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_empty, 4);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 4);
+    mbar_init(&bars->kvst_full, 128);
+    mbar_init(&bars->kvst_free, 1);
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(&bars->stg_full[s2], 128);
       mbar_init(&bars->stg_free[s2], 1);
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<kRegDrain>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t ph = 0, q_it = 0, dkv_ph = 0;
+    uint32_t ph = 0, q_it = 0, dkv_ph = 0, kvst_full_ph = 0, kvst_free_ph = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
@@ -317,10 +321,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
           dkv_ph ^= 1;
           tc_fence_after();
+          // A block of 128 valid keys goes out through the staging buffer and TMA
+          // stores (one warp store instruction would otherwise touch 32 rows); a
+          // shorter tail block is written row by row, so the next sequence's rows
+          // are untouched.  The buffer is taken over from the dQ reduction once its
+          // boxes have been read.  Causal attention keeps the row stores: its query
+          // loads are DRAM-heavy and the stores' TMA traffic measured slower there.
+          const bool full_blk = !CAUSAL && BK * (u.n + 1) <= u.L;
           const bool key_ok = BK * u.n + r < u.L;
           const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.H + u.h) * D;
+          const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
 #pragma unroll 1
           for (int which = 0; which < 2; ++which) {
+            if (full_blk) {  // the buffer holds nothing TMA still reads
+              if (threadIdx.x == 256) {
+                bulk_wait_read_all();
+                mbar_arrive(&bars->kvst_free);
+              }
+              if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
+              kvst_free_ph ^= 1;
+            }
             const uint32_t tAcc = tmem + lane_addr + (which == 0 ? C::COL_DV : C::COL_DK);
             const float mul = which == 0 ? 1.0f : p.scale;
             __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row;
@@ -334,16 +354,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
-              if (key_ok) {
+              if (full_blk) {
+                // row r of 64-column box c/64, 16-byte pieces (c%64)/8 .. +3, 128-byte swizzle
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t addr =
+                      stage32 + (c / 64) * 16384 + r * 128 + ((((c % 64) / 8 + e) ^ (r & 7)) << 4);
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * e]),
+                               "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
+                               : "memory");
+                }
+              } else if (key_ok) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                   st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
               }
             }
+            if (which == 1) {  // dV and dK are out of TMEM: the next unit's MMAs may start
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->dkv_empty);
+            }
+            if (full_blk) {
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->kvst_full);
+              if (!mbar_wait(&bars->kvst_full, kvst_full_ph, ab)) goto done;
+              kvst_full_ph ^= 1;
+              if (threadIdx.x == 256) {
+#pragma unroll
+                for (int b2 = 0; b2 < D / 64; ++b2)
+                  tma_store_2d(which == 0 ? &tm_dv : &tm_dk, smem + C::OFF_STG + b2 * 16384, u.h * D + 64 * b2,
+                               u.kv0 + BK * u.n);
+                bulk_commit_group();
+              }
+            }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->dkv_empty);
+          if (full_blk) {  // hand the buffer back to the dQ reduction
+            if (threadIdx.x == 256) {
+              bulk_wait_read_all();
+              mbar_arrive(&bars->kvst_free);
+            }
+            if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
+            kvst_free_ph ^= 1;
+          }
         }
         if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
         ph ^= 1;
@@ -647,6 +700,9 @@ int launch_main(const BwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BQ);
   CUtensorMap tdq;  // fp32 dQ accumulator, 32-column boxes for the staged reduce-add
   if (st == JFA_OK) st = make_map_2d_f32(&tdq, a.dq_acc, static_cast<uint64_t>(a.H) * D, a.q_rows, 32, BQ);
+  CUtensorMap tdk, tdv;  // dK, dV outputs: 64-column boxes of one 128-key block
+  if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
   if (st != JFA_OK) return st;
   auto kern = bwd_kernel<D, CAUSAL>;
   static bool attr_set = false;
@@ -674,7 +730,7 @@ int launch_main(const BwdArgs& a) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   ProfileScope prof(kKindBwdMain, a.stream);
-  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, p);
+  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
