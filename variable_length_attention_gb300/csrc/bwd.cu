@@ -43,6 +43,7 @@
 // (a key flag and L = +inf), so only the causal diagonal tile needs an
 // element-wise mask, and it is peeled into its own code path.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -237,30 +238,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->s_full, ph, ab)) goto done;
         tc_fence_after();
         const bool diag = CAUSAL && i == u.n;
-        // P^T first: the dV MMA can start while dS^T is being formed
+        // P^T first: the dV MMA can start while dS^T is being formed.  Only the
+        // causal diagonal tile carries the element mask (the choice is the same
+        // for the whole warp, as the TMEM accesses need).
         float pf[64];
+        auto p_phase = [&](auto diag_tile) {
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          uint32_t sr[32];
-          tmem_ld32(tS + 32 * pass, sr);
-          tmem_wait_ld();
-          reg_fence<32>(sr);
-          uint32_t pw[16];
+          for (int pass = 0; pass < 2; ++pass) {
+            uint32_t sr[32];
+            tmem_ld32(tS + 32 * pass, sr);
+            tmem_wait_ld();
+            reg_fence<32>(sr);
+            uint32_t pw[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * pass + c);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int c = 0; c < 32; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse_s + 32 * pass + c);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pe = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, -lv[e]));
-              if (diag && (64 * wg + 32 * pass + c + e) < k) pe = 0.f;
-              pf[32 * pass + c + e] = key_ok ? pe : 0.f;
+              for (int e = 0; e < 4; ++e) {
+                float pe = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, -lv[e]));
+                if constexpr (decltype(diag_tile)::value) {
+                  if ((64 * wg + 32 * pass + c + e) < k) pe = 0.f;
+                }
+                pf[32 * pass + c + e] = key_ok ? pe : 0.f;
+              }
+              pw[c / 2] = pack_bf16(pf[32 * pass + c], pf[32 * pass + c + 1]);
+              pw[c / 2 + 1] = pack_bf16(pf[32 * pass + c + 2], pf[32 * pass + c + 3]);
             }
-            pw[c / 2] = pack_bf16(pf[32 * pass + c], pf[32 * pass + c + 1]);
-            pw[c / 2 + 1] = pack_bf16(pf[32 * pass + c + 2], pf[32 * pass + c + 3]);
+            tmem_st16(tP + 16 * pass, pw);
           }
-          tmem_st16(tP + 16 * pass, pw);
-        }
+        };
+        if (diag)
+          p_phase(std::true_type{});
+        else
+          p_phase(std::false_type{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
