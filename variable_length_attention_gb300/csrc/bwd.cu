@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
       const bool key_ok = BK * u.n + k < u.L;
+      const bool all_keys_ok = __all_sync(0xffffffffu, key_ok);  // the same in the whole warp
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
         const int st = q_it & 1;
         const float* lse_s = s_lse + st * 128 + 64 * wg;
@@ -239,10 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool diag = CAUSAL && i == u.n;
         // P^T first: the dV MMA can start while dS^T is being formed.  Only the
-        // causal diagonal tile carries the element mask (the choice is the same
-        // for the whole warp, as the TMEM accesses need).
+        // causal diagonal tile carries the element mask, and only warps with keys
+        // past the sequence end the key select (both choices are the same for the
+        // whole warp, as the TMEM accesses need).
         float pf[64];
-        auto p_phase = [&](auto diag_tile) {
+        auto p_phase = [&](auto diag_tile, auto key_mask) {
 #pragma unroll
           for (int pass = 0; pass < 2; ++pass) {
             uint32_t sr[32];
@@ -260,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (decltype(diag_tile)::value) {
                   if ((64 * wg + 32 * pass + c + e) < k) pe = 0.f;
                 }
-                pf[32 * pass + c + e] = key_ok ? pe : 0.f;
+                if constexpr (decltype(key_mask)::value) pe = key_ok ? pe : 0.f;
+                pf[32 * pass + c + e] = pe;
               }
               pw[c / 2] = pack_bf16(pf[32 * pass + c], pf[32 * pass + c + 1]);
               pw[c / 2 + 1] = pack_bf16(pf[32 * pass + c + 2], pf[32 * pass + c + 3]);
@@ -269,9 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         if (diag)
-          p_phase(std::true_type{});
+          p_phase(std::true_type{}, std::true_type{});
+        else if (!all_keys_ok)  // a tail block: some keys of this warp lie past the sequence end
+          p_phase(std::false_type{}, std::true_type{});
         else
-          p_phase(std::false_type{});
+          p_phase(std::false_type{}, std::false_type{});
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
