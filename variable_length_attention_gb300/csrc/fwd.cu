@@ -58,7 +58,8 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSTAGE * TILE_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 4096;      // barriers, stats, TMEM address
+  static constexpr int OFF_STG = OFF_BAR + 4096;         // after barriers, stats, TMEM address:
+  static constexpr int SMEM_BYTES = OFF_STG + BM * 128;  // O staging, one 64-column bf16 box
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;   // slack for 1024-byte alignment
 };
 
@@ -138,6 +139,7 @@ struct Bars {
   int sched_unit[4];
   float stat_m[2][BM];
   float stat_l[2][BM];
+  uint64_t ostg_full, ostg_free;  // O staging box: rows written by the epilogue / read out by TMA
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -161,7 +163,7 @@ __device__ __forceinline__ int sched_pop(Bars* bars, uint32_t it, const Abort& a
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const Params p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -192,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->q_empty, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->ostg_full, BM);
+    mbar_init(&bars->ostg_free, 1);
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -317,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_dec<kRegEpilogue>();
     const int row = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t phase = 0;
+    uint32_t phase = 0, sf_ph = 0, sr_ph = 0;
+    const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
     for (uint32_t it = 0;; ++it) {
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
@@ -332,33 +337,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->st_empty[t]);
         const int qi = 2 * BM * u.m + BM * t + row;
         const bool valid = qi < u.rows;
+        // A tile of 128 valid rows leaves through the staging box and TMA stores
+        // (a warp store instruction would otherwise touch 32 rows); a tail tile is
+        // written row by row, so no row past the end is touched.
+        const bool full_tile = 2 * BM * u.m + BM * t + BM <= u.rows;
         const int orow = u.o_row0 + BM * t + row;
         const float inv_l = 1.0f / l_fin;
         __nv_bfloat16* dst = p.o + (static_cast<size_t>(orow) * p.H + u.h) * D;
         const uint32_t tO = tmem + lane_addr + 256 + t * 128;
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c, ov);
-          tmem_wait_ld();
-          reg_fence<32>(ov);
-          uint32_t pk[16];
+        for (int rnd = 0; rnd < D / 64; ++rnd) {
+          if (full_tile) {  // the box is free once TMA has read the previous one
+            if (threadIdx.x == 256) {
+              bulk_wait_read_all();
+              mbar_arrive(&bars->ostg_free);
+            }
+            if (!mbar_wait(&bars->ostg_free, sf_ph, ab)) goto done;
+            sf_ph ^= 1;
+          }
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {  // 16 columns at a time
+            const int c = 64 * rnd + 16 * q4;
+            uint32_t ov[16];
+            tmem_ld16(tO + c, ov);
+            tmem_wait_ld();
+            reg_fence<16>(ov);
+            uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-          if (valid) {
+            for (int i = 0; i < 8; ++i)
+              pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (full_tile) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_global_v4(dst + c + 8 * i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 2; ++i) {
+                const uint32_t addr = stage32 + row * 128 + (((2 * q4 + i) ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * i]),
+                             "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3])
+                             : "memory");
+              }
+            } else if (valid) {
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                st_global_v4(dst + c + 8 * i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          if (rnd == D / 64 - 1) {  // all of O is out of TMEM
+            tc_fence_before();
+            mbar_arrive(&bars->o_empty[t]);
+          }
+          if (full_tile) {
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->ostg_full);
+            if (!mbar_wait(&bars->ostg_full, sr_ph, ab)) goto done;
+            sr_ph ^= 1;
+            if (threadIdx.x == 256) {
+              tma_store_2d(&tm_o, smem + C::OFF_STG, u.h * D + 64 * rnd, u.o_row0 + BM * t);
+              bulk_commit_group();
+            }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bars->o_empty[t]);
         if (valid && p.lse != nullptr)
           p.lse[static_cast<size_t>(u.h) * p.o_rows + orow] = (m_fin + log2f(l_fin)) * 0.69314718055994531f;
       }
       phase ^= 1;
     }
+    if (threadIdx.x == 256) bulk_wait_all();  // every store has landed before the CTA exits
   } else {
     setmaxnreg_dec<kRegIssue>();
     if (warp == 12 && lane == 0) {
@@ -531,6 +573,8 @@ int launch_impl(const FwdArgs& a) {
   int st = make_map_2d(&tq, a.q, static_cast<uint64_t>(a.H) * D, a.q_rows, 64, BM);
   if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BN);
   if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BN);
+  CUtensorMap to;  // O, for the epilogue's TMA stores of full tiles
+  if (st == JFA_OK) st = make_map_2d(&to, a.o, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BM);
   if (st != JFA_OK) return st;
   auto kern = fwd_kernel<D, CAUSAL>;
   static bool attr_set = false;  // per instantiation
@@ -557,7 +601,7 @@ int launch_impl(const FwdArgs& a) {
   p.n_units = a.n_units;
   p.use_clc = a.use_clc;
   ProfileScope prof(kKindFwd, a.stream);
-  kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, p);
+  kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
