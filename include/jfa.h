@@ -36,8 +36,10 @@
  *  - Causal masking (key j visible to query i iff j <= i inside a sequence) is
  *    supported for self-attention only.
  *  - head_dim must be 64 or 128 (the pages allow up to 128 [C "feature scope"];
- *    this library builds those two).  GQA is forward-only: the backward needs
- *    num_kv_heads == num_heads [C "feature scope"].
+ *    this library builds those two).  Grouped-query attention (GQA) is
+ *    supported forward and backward.  The pages' own implementation limits
+ *    the backward to one group [C "feature scope"]; here dk and dv of key/value
+ *    head g sum the gradients of all its query heads.
  *  - offsets_dev is the device copy of the offsets; offsets_host the host copy,
  *    from which all scheduling is planned on the CPU with no device sync
  *    [B 5].  Both must hold the same values; only offsets_host is validated.
@@ -66,7 +68,7 @@ extern "C" {
 typedef enum {
   JFA_OK = 0,
   JFA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned pointer */
-  JFA_ERR_UNSUPPORTED = 2,          /* head_dim not 64/128, GQA backward, causal+broadcast,
+  JFA_ERR_UNSUPPORTED = 2,          /* head_dim not 64/128, causal+broadcast,
                                        num_heads % num_kv_heads != 0 */
   JFA_ERR_BAD_OFFSETS = 3,          /* offsets[0] != 0, decreasing, or a length > max_len */
   JFA_ERR_WORKSPACE_TOO_SMALL = 4,
@@ -99,9 +101,12 @@ int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, co
  * dq (bf16, like q), dk and dv (bf16, like k):
  *   P = exp(scale q k^T - lse), dV = P^T dO, dP = dO V^T, Di = rowsum(dO o O),
  *   dS = P o (dP - Di), dQ = scale dS K, dK = scale dS^T Q.
- * Requires num_kv_heads == num_heads.  In broadcast-Q mode dq is summed over all
- * sequences.  Only valid 128-key blocks are listed; they are sorted by cost
- * and snake-dealt to the CTAs (see jfa_plan_bwd).
+ * With GQA, dk and dv of key/value head g are the sums over query heads
+ * g*G .. g*G+G-1 (G = num_heads / num_kv_heads), formed in one CTA without
+ * atomics.  In broadcast-Q mode dq is summed over all sequences.  Only valid
+ * 128-key blocks of each (sequence, key/value head) are listed; they are sorted
+ * by cost and snake-dealt to the CTAs (see jfa_plan_bwd, called with
+ * num_kv_heads).
  */
 int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
@@ -157,6 +162,8 @@ size_t jfa_fwd_noalloc_capacity(void);
  * jfa_workspace_size -- device workspace in bytes that `op` needs for this
  * problem (plans, per-row Di, the fp32 dQ accumulator, an error word).
  * Returns 0 on invalid arguments.  Queries the current device's SM count.
+ * num_heads is the number of query heads; for a GQA backward the size is an
+ * upper bound (the call plans over the fewer key/value heads).
  */
 size_t jfa_workspace_size(int op, const int32_t* offsets_host, int batch, int nq_broadcast, int num_heads,
                           int head_dim, int causal, int broadcast_q);
@@ -180,8 +187,10 @@ int jfa_device_status(const void* workspace, void* stream);
  *   jfa_plan_fwd: unit = 256 query rows (b, h, m); cost = 128-key blocks
  *     visited; stable sort by cost descending; snake deal over n_cta.
  *   jfa_plan_bwd: unit = one valid 128-key block (b, h, n), enumerated b, h, n
- *     (n innermost); cost = 128-row query tiles visited; stable sort by cost
- *     descending, snake deal (equal costs keep the enumeration order).
+ *     (n innermost); cost = 128-row query tiles visited per query head; stable
+ *     sort by cost descending, snake deal (equal costs keep the enumeration
+ *     order).  h runs over the key/value heads: jfa_bwd passes num_kv_heads
+ *     here, and each unit then visits the tiles of its G query heads.
  */
 int jfa_plan_fwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal, int n_cta,
                  int32_t* units, int32_t* cta_start);

@@ -71,12 +71,18 @@ def test_bad_offsets(offsets):
     assert _fwd(offsets, max_len=100) == 3
 
 
-def test_bwd_rejects_gqa_before_device_work():
+@pytest.mark.parametrize("H,Hkv,causal,bq,status", [
+    (3, 2, 0, 0, 2),   # query heads not a multiple of key/value heads
+    (4, 2, 1, 1, 2),   # causal broadcast-Q is undefined
+    (4, 0, 0, 0, 1),   # no key/value heads
+])
+def test_bwd_argument_errors_before_device_work(H, Hkv, causal, bq, status):
+    # every case returns before the device is touched, so the fake pointers are never used
     lib = J.load()
     h = np.array([0, 10, 20], dtype=np.int32)
     st = lib.jfa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, h.ctypes.data_as(ctypes.c_void_p),
-                     2, 10, 0, 4, 2, 64, 0.125, 0, 0, FAKE, 1 << 20, None)
-    assert st == 2
+                     2, 10, 16 if bq else 0, H, Hkv, 64, 0.125, causal, bq, FAKE, 1 << 20, None)
+    assert st == status
 
 
 def test_planner_hooks_reject_bad_input():

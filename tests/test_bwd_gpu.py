@@ -50,17 +50,45 @@ def test_dense_full_size():
     assert_bwd_ok(check_bwd(w, sel=sample_units(w.batch, w.num_heads, 4, seed=13)))
 
 
-def test_gqa_backward_is_rejected():
-    w = W.custom([100, 50], 4, 64, num_kv_heads=2)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv,D", [(4, 2, 64), (4, 1, 128), (8, 2, 128)])
+def test_gqa(H, Hkv, D, causal):
+    # dK and dV of a key/value head sum the gradients of its H/Hkv query heads;
+    # sequences of several key blocks and query tiles, ragged tails, a 1-token one
+    w = W.custom([300, 1, 129, 700, 256], H, D, num_kv_heads=Hkv, causal=causal,
+                 seed_base=900 + 10 * H + Hkv + D + int(causal))
+    assert_bwd_ok(check_bwd(w))
+
+
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_gqa_broadcast(Hkv):
+    # broadcast-Q with groups: dQ of each query head sums over all sequences,
+    # dK/dV of each key/value head over its group; an empty sequence included
+    w = W.custom([200, 0, 77, 513, 129], 4, 128, num_kv_heads=Hkv, nq=192, seed_base=950 + Hkv)
+    assert_bwd_ok(check_bwd(w))
+
+
+def test_gqa_group_sum_identity():
+    # the grouped call equals the ungrouped call on K/V repeated per query head,
+    # with dK/dV summed over each group (checked on the GPU results themselves)
+    w = W.custom([300, 129, 513], 4, 128, num_kv_heads=2, seed_base=960)
     (q, k, v, do), offs, _ = gpu_inputs(w)
     o, lse = V.jfa_fwd(q, k, v, offs, w.offsets)
-    with pytest.raises(V.jfa.JfaError) as e:
-        V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets)
-    assert e.value.status == 2
+    dq, dk, dv = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets)
+    kr, vr = k.repeat_interleave(2, dim=1).contiguous(), v.repeat_interleave(2, dim=1).contiguous()
+    o2, lse2 = V.jfa_fwd(q, kr, vr, offs, w.offsets)
+    dq2, dk2, dv2 = V.jfa_bwd(q, kr, vr, o2, do, lse2, offs, w.offsets)
+    torch.cuda.synchronize()
+    T = int(w.offsets[-1])
+    dk2 = dk2.float().view(T, 2, 2, 128).sum(2)
+    dv2 = dv2.float().view(T, 2, 2, 128).sum(2)
+    for a, b in ((dq.float(), dq2.float()), (dk.float(), dk2), (dv.float(), dv2)):
+        assert ((a - b).norm() / b.norm()).item() < 1e-2
 
 
-def test_backward_repeatable_except_dq_order():
-    w = W.custom([700, 33, 300], 2, 128, seed_base=800)
+@pytest.mark.parametrize("Hkv", [2, 1])
+def test_backward_repeatable_except_dq_order(Hkv):
+    w = W.custom([700, 33, 300], 2, 128, num_kv_heads=Hkv, seed_base=800)
     (q, k, v, do), offs, _ = gpu_inputs(w)
     o, lse = V.jfa_fwd(q, k, v, offs, w.offsets)
     g1 = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets)

@@ -290,6 +290,8 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
   }
   if (op == JFA_OP_BWD) {
     if (head_dim != 64 && head_dim != 128) return 0;
+    // planned over all query heads: an upper bound when the call groups them
+    // (grouped-query attention plans over the fewer K/V heads)
     const int n = plan_bwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
     const int q_rows = broadcast_q ? nq : offsets_host[batch];
     const int o_rows = broadcast_q ? batch * nq : offsets_host[batch];
@@ -387,7 +389,6 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
                            head_dim, scale, causal, broadcast_q, &c);
   if (st != JFA_OK) return st;
-  if (num_kv_heads != num_heads) return JFA_ERR_UNSUPPORTED;  // backward needs a single query group
   if (c.o_rows > 0 && (dout == nullptr || lse == nullptr || dq == nullptr)) return JFA_ERR_INVALID_ARG;
   if (c.kv_rows > 0 && (dk == nullptr || dv == nullptr)) return JFA_ERR_INVALID_ARG;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
@@ -395,10 +396,11 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   if (st != JFA_OK) return st;
 
   std::vector<int32_t> units, cta_start;
-  const int n_probe = plan_bwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+  // units run over the K/V heads; each loops over its group's query heads
+  const int n_probe = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, 1, nullptr, nullptr);
   const int n_cta = plan_ctas(c.dev, n_probe);
   int n = 0;
-  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_heads, nq, causal, n_cta, &units, &cta_start);
+  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, n_cta, &units, &cta_start);
   const BwdLayout lay = bwd_layout(n, n_cta, c.q_rows, c.o_rows, num_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -418,6 +420,7 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   a.kv_rows = c.kv_rows;
   a.o_rows = c.o_rows;
   a.H = num_heads;
+  a.Hkv = num_kv_heads;
   a.D = head_dim;
   a.nq = nq;
   a.scale = scale;

@@ -6,13 +6,16 @@
 //   P  = exp(scale Q K^T - L)            (recomputed, no stored P)
 //   dV = P^T dO,  dP = dO V^T,  Di = rowsum(dO o O),  dS = P o (dP - Di)
 //   dQ = scale dS K,  dK = scale dS^T Q
-// Broadcast-Q sums dQ of the shared Q over every sequence.
+// Broadcast-Q sums dQ of the shared Q over every sequence.  With grouped-query
+// attention (G = H / Hkv query heads per K/V head) dK and dV of a K/V head sum
+// the contributions of all G query heads of its group.
 //
 // Kernels, in launch order:
 //   prep_kernel   Di = rowsum(dO o O) and L * log2(e) per (row, head); zeroes the
 //                 fp32 dQ accumulator
 //   bwd_kernel    persistent, one CTA per SM, one work unit = one valid block of
-//                 128 keys of one (sequence, head); it loops over the 128-row query
+//                 128 keys of one (sequence, K/V head); it loops over the query
+//                 heads of the head's group and, per head, the 128-row query
 //                 tiles that attend to those keys, keeps dK and dV in TMEM and
 //                 adds each tile's dQ into an fp32 accumulator
 //   dq_convert    dQ = scale * accumulator -> bf16
@@ -102,12 +105,12 @@ struct Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* err;
-  int H, nq, o_rows;
+  int H, Hkv, G, nq, o_rows;  // G = H / Hkv query heads per K/V head
   float scale, scale_log2;
 };
 
 struct Unit {
-  int b, h, n;
+  int b, h, n;         // h: the K/V head; its query heads are h*G .. h*G+G-1
   int kv0, L;          // first key row of the sequence, its length
   int rows;            // query rows (L, or nq in broadcast mode)
   int i0, i1;          // query tiles [i0, i1)
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit u = decode<CAUSAL>(p, ui);
       const bool key_ok = BK * u.n + k < u.L;
       const bool all_keys_ok = __all_sync(0xffffffffu, key_ok);  // the same in the whole warp
+      for (int hg = 0; hg < p.G; ++hg)
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
         const int st = q_it & 1;
         const float* lse_s = s_lse + st * 128 + 64 * wg;
@@ -329,9 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0, q_it = 0, dkv_ph = 0, kvst_full_ph = 0, kvst_free_ph = 0;
     for (int ui = u_begin; ui < u_end; ++ui) {
       const Unit u = decode<CAUSAL>(p, ui);
+      for (int hg = 0; hg < p.G; ++hg)
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
         const uint32_t tQ = tmem + lane_addr + region_s(q_it);  // dQ sits where this tile's S^T was
-        if (i + 1 == u.i1) {
+        if (hg + 1 == p.G && i + 1 == u.i1) {
           // unit done: dV and dK leave TMEM first (the next unit's first dV/dK
           // MMAs wait for them); one thread per key row
           if (!mbar_wait(&bars->dkv_full, dkv_ph, ab)) goto done;
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // loads are DRAM-heavy and the stores' TMA traffic measured slower there.
           const bool full_blk = !CAUSAL && BK * (u.n + 1) <= u.L;
           const bool key_ok = BK * u.n + r < u.L;
-          const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.H + u.h) * D;
+          const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.Hkv + u.h) * D;
           const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
 #pragma unroll 1
           for (int which = 0; which < 2; ++which) {
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars->stg_full[slot], (g >> 1) & 1, ab)) goto done;
           if (threadIdx.x == 256) {
             bulk_wait_read_all();  // one box being read at a time
-            tma_reduce_add_2d(&tm_dq, stage + slot * 16384, u.h * D + 32 * rnd, y);
+            tma_reduce_add_2d(&tm_dq, stage + slot * 16384, (u.h * p.G + hg) * D + 32 * rnd, y);
             bulk_commit_group();
           }
         }
@@ -500,7 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars->kv_full, kv_ph, ab)) goto mma_done;
           kv_ph ^= 1;
           if (!issue_s(q_it)) goto mma_done;  // the unit's first tile
+          for (int hg = 0; hg < p.G; ++hg)
           for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+            const bool first = hg == 0 && i == u.i0;          // the unit's first tile
+            const bool last = hg + 1 == p.G && i + 1 == u.i1;  // and its last
             const uint32_t st = q_it & 1;
             const uint32_t sQ = smem_u32(smem + C::OFF_Q + st * C::TILE);
             const uint32_t sDO = smem_u32(smem + C::OFF_DO);
@@ -509,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // was, which holds the previous tile's dQ until the drain has read it.
             const uint32_t rs = region_s(q_it), rd = 128 - rs;
             // dP^T = V dO^T, once the previous dQ has left TMEM
-            if (i > u.i0 || ui > u_begin) {
+            if (!first || ui > u_begin) {
               if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
               dq_ph ^= 1;
             }
@@ -522,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(&bars->dp_full);
             // dV += P^T dO  (A from TMEM)
-            if (i == u.i0) {
+            if (first) {
               if (!mbar_wait(&bars->dkv_empty, dkv_ph ^ 1, ab)) goto mma_done;
               dkv_ph ^= 1;
             }
@@ -532,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t pcol = (kk < 4) ? 8 * kk : 64 + 8 * (kk - 4);
               mma_ts(tmem + C::COL_DV, tmem + rs + pcol, sdesc_sw128(sDO + kk * 2048, C::CHUNK, 1024), id_kv,
-                     (i > u.i0 || kk > 0) ? 1u : 0u);
+                     (!first || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->do_empty);  // dV was dO's last reader: the next dO may load
             if (!mbar_wait(&bars->ds_full, ph, ab)) goto mma_done;
@@ -546,13 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss(tmem + rs, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024),
                      id_q, kk > 0);
             mma_commit(&bars->dq_full);
-            if (i + 1 < u.i1 && !issue_s(q_it + 1)) goto mma_done;
-            if (i + 1 == u.i1) mma_commit(&bars->kv_empty);  // K and V are done: the next unit's may load
+            if (!last && !issue_s(q_it + 1)) goto mma_done;
+            if (last) mma_commit(&bars->kv_empty);  // K and V are done: the next unit's may load
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
               mma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(sQ + kk * 2048, C::CHUNK, 1024),
-                     id_kv, (i > u.i0 || kk > 0) ? 1u : 0u);
+                     id_kv, (!first || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars->ds_empty);
             mma_commit(&bars->q_empty[st]);
@@ -581,14 +589,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n);
           }
         }
+        for (int hg = 0; hg < p.G && ok; ++hg)
         for (int i = u.i0; i < u.i1; ++i, ++q_it) {
+          const int hq = u.h * p.G + hg;  // query head
           const uint32_t st = q_it & 1;
           if (!mbar_wait(&bars->q_empty[st], ((q_it >> 1) & 1) ^ 1, ab)) {
             ok = false;
             break;
           }
           // L and Di of the tile's 128 query rows (rows past the end: L = +inf so P = 0)
-          const size_t lbase = static_cast<size_t>(u.h) * p.o_rows + u.o_base + BQ * i;
+          const size_t lbase = static_cast<size_t>(hq) * p.o_rows + u.o_base + BQ * i;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int r = 4 * lane + e;
@@ -601,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&bars->q_full[st], C::TILE);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_load_2d(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, u.h * D + c * 64, u.q_base + BQ * i);
+              tma_load_2d(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, hq * D + c * 64, u.q_base + BQ * i);
           } else {
             mbar_arrive(&bars->q_full[st]);
           }
@@ -614,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&bars->do_full, C::TILE);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_load_2d(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, u.h * D + c * 64,
+              tma_load_2d(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, hq * D + c * 64,
                           u.o_base + BQ * i);
           }
         }
@@ -711,14 +721,14 @@ int launch_main(const BwdArgs& a) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv, tdo;
   int st = make_map_2d(&tq, a.q, static_cast<uint64_t>(a.H) * D, a.q_rows, 64, BQ);
-  if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
-  if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tk, a.k, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tv, a.v, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st == JFA_OK) st = make_map_2d(&tdo, a.dout, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BQ);
   CUtensorMap tdq;  // fp32 dQ accumulator, 32-column boxes for the staged reduce-add
   if (st == JFA_OK) st = make_map_2d_f32(&tdq, a.dq_acc, static_cast<uint64_t>(a.H) * D, a.q_rows, 32, BQ);
   CUtensorMap tdk, tdv;  // dK, dV outputs: 64-column boxes of one 128-key block
-  if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
-  if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.H) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
+  if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st != JFA_OK) return st;
   auto kern = bwd_kernel<D, CAUSAL>;
   static bool attr_set = false;
@@ -741,6 +751,8 @@ int launch_main(const BwdArgs& a) {
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
   p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
   p.nq = a.nq;
   p.o_rows = a.o_rows;
   p.scale = a.scale;

@@ -12,7 +12,7 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   const int32_t* offsets_dev;
   int q_rows, kv_rows, o_rows;
-  int H, D, nq;
+  int H, Hkv, D, nq;  // query heads, K/V heads (H % Hkv == 0)
   float scale;
   int causal;
   const int32_t* units;

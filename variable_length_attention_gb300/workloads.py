@@ -138,7 +138,8 @@ def block(head_dim: int = 128, batch: int = 1152, seq_len: int = 4032) -> Worklo
 
 def dense(gqa: bool = False) -> Workload:
     """B=8 sequences of 8192 tokens in jagged layout, H=16, head_dim 128;
-    the GQA variant has 4 K/V heads and is forward-only."""
+    the GQA variant has 4 K/V heads and is timed forward-only, the configuration
+    it stands for being a forward one."""
     return Workload(f"dense_B8_L8192_H16{'_KV4' if gqa else ''}_D128", "jagged",
                     np.full(8, 8192, dtype=np.int64), 16, 4 if gqa else 16, 128,
                     seed_base=5000, bwd=not gqa)
