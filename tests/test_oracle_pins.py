@@ -252,10 +252,13 @@ def test_gradients_finite_differences(causal, H, Hkv):
     _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng)
 
 
-def test_broadcast_gradients_finite_differences():
-    rng = np.random.default_rng(30)
+@pytest.mark.parametrize("H,Hkv,lengths", [(2, 2, [4, 2, 5]), (4, 2, [4, 0, 5]), (4, 1, [3, 6])])
+def test_broadcast_gradients_finite_differences(H, Hkv, lengths):
+    # grouped heads: dK/dV of a key/value head collect every query head of its
+    # group and every query row; dQ of the shared Q every sequence
+    rng = np.random.default_rng(30 + H + Hkv)
     nq = 3
-    offs, q, k, v, do = _problem(rng, [4, 2, 5], 2, 2, 4, nq=nq)
+    offs, q, k, v, do = _problem(rng, lengths, H, Hkv, 4, nq=nq)
 
     def fwd(q, k, v):
         return oracle.attn_fwd(q, k, v, offs, scale=0.5, nq=nq)[0]
