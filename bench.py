@@ -298,34 +298,67 @@ def main():
     value = job_throughput(step_flops, args.steps, total_ms, ws)
 
     # ---------------------------------------------------------------- e2e through host buffers
+    # Every step uploads its inputs from pinned host memory (q, k, v, dO and the
+    # offsets), runs, and reads its results back (O, dQ, dK, dV) into pinned host
+    # memory.  The copies run on two copy streams and the kernels on the compute
+    # stream, with two slots of device inputs and outputs: step i+1's upload and
+    # step i-1's read-back overlap step i's kernels, and a slot is reused only
+    # after both its kernels and its read-back are done.  The timed region spans
+    # the first upload to the last read-back.
     e2e = None
     host_in = job["host_inputs"]
     if host_in is not None:
-        outs = job["outputs"]
-        o_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        h2d = sum(t.numel() * t.element_size() for t in host_in) + job["offsets_bytes"]
-        d2h = sum(t.numel() * t.element_size() for t in o_h)
+        s2 = job["new_slot"]()
+        d_in = [job["dev_inputs"], [torch.empty_like(t) for t in job["dev_inputs"]]]
+        outs = [job["outputs"](0), job["outputs"](s2)]
+        o_h = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs[0]] for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in o_h[0])
+        comp = torch.cuda.current_stream(dev)
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ran = [torch.cuda.Event(), torch.cuda.Event()]   # the slot's last step has run
+        read = [torch.cuda.Event(), torch.cuda.Event()]  # the slot's last results are on the host
+        loaded = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            step([t.to(dev, non_blocking=True) for t in host_in])
-            for dst, src in zip(o_h, outs):
-                dst.copy_(src, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        barrier()
-        e_ms = []
-        for i in range(args.steps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            e2e_step()
-            b.record()
+        def e2e_run(n):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(comp)
+            up.wait_stream(comp)
+            down.wait_stream(comp)
+            for i in range(n):
+                s = i & 1
+                slot = 0 if s == 0 else s2
+                with torch.cuda.stream(up):
+                    if i >= 2:
+                        up.wait_event(ran[s])  # its inputs are no longer read
+                    for d, h in zip(d_in[s], host_in):
+                        d.copy_(h, non_blocking=True)
+                    loaded[s].record(up)
+                comp.wait_event(loaded[s])
+                if i >= 2:
+                    comp.wait_event(read[s])  # its outputs have been read back
+                job["step"](d_in[s], slot)
+                ran[s].record(comp)
+                with torch.cuda.stream(down):
+                    down.wait_event(ran[s])
+                    for h, d in zip(o_h[s], outs[s]):
+                        h.copy_(d, non_blocking=True)
+                    read[s].record(down)
+            comp.wait_stream(up)
+            comp.wait_stream(down)
+            t1.record(comp)
             torch.cuda.synchronize()
-            e_ms.append(a.elapsed_time(b))
-        e_total = max_over_ranks(float(sum(e_ms)), ws)
+            return t0.elapsed_time(t1)
+
+        e2e_run(2)
+        barrier()
+        e_total = max_over_ranks(float(e2e_run(args.steps)), ws)
         e2e = {"value": job_throughput(step_flops, args.steps, e_total, ws), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_total / args.steps,
+               "overlap": "uploads and read-backs on two copy streams overlap the neighbouring steps' kernels "
+                          "(two slots of device buffers); inputs copied from host every step "
+                          f"({h2d / 2**20:.0f} MiB, larger than L2)"}
 
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, peak_src = _peaks()
@@ -365,48 +398,60 @@ def main():
 
 
 def build_job(args, dev):
-    """Inputs, outputs and the step function of one workload."""
+    """Inputs, outputs and the step function of one workload.
+
+    ``step(inputs, slot)`` runs one step on the current stream, writing the
+    outputs of ``slot``; ``new_slot()`` allocates a further set of outputs (and
+    workspaces) and returns its index, so that consecutive steps can keep their
+    results apart while earlier ones are still being read back."""
     import variable_length_attention_gb300 as V
     from variable_length_attention_gb300 import workloads as W
-
-    def nbytes(ts):
-        return sum(t.numel() * t.element_size() for t in ts)
 
     if args.workload in ("jagged", "broadcast", "dense"):
         wls = {"jagged": [W.jagged(False), W.jagged(True)], "broadcast": [W.broadcast()],
                "dense": [W.dense(False), W.dense(True)]}[args.workload]
         w = wls[0]
-        host = [t.pin_memory() for t in w.tensors("cpu")]
-        dev_in = [t.to(dev) for t in host]
         offs_h = w.offsets
-        offs = torch.from_numpy(offs_h).to(dev)
-        calls, outputs = [], []
-        for wl in wls:
-            kv_heads = wl.num_kv_heads
-            extra = None
-            if kv_heads != w.num_kv_heads:  # GQA forward: its own K, V with fewer heads
-                g = wl.tensors("cpu")
-                extra = [g[1].to(dev), g[2].to(dev)]
-            o = torch.empty((wl.o_rows, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
-            lse = torch.empty((wl.num_heads, wl.o_rows), dtype=torch.float32, device=dev)
-            grads = None
-            if wl.bwd:
-                grads = (torch.empty_like(dev_in[0]), torch.empty_like(dev_in[1]), torch.empty_like(dev_in[2]))
-                outputs += [o, *grads]
-            else:
-                outputs.append(o)
-            need = max(V.jfa_workspace_size(0, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
-                                            wl.nq > 0),
-                       V.jfa_workspace_size(1, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
-                                            wl.nq > 0) if wl.bwd else 0)
-            calls.append((wl, o, lse, grads, extra, torch.empty(need, dtype=torch.uint8, device=dev)))
-
+        # step inputs: q, k, v, dO, then the K, V of a GQA forward (fewer heads) if
+        # the workload has one, then the offsets
+        host = list(w.tensors("cpu"))
+        gqa = [wl for wl in wls if wl.num_kv_heads != w.num_kv_heads]
+        if gqa:
+            g = gqa[0].tensors("cpu")
+            host += [g[1], g[2]]
+        host.append(torch.from_numpy(offs_h.copy()))
+        host = [t.pin_memory() for t in host]
+        dev_in = [t.to(dev) for t in host]
         max_len = w.max_len  # the caller's bound on sequence length, as the interface takes it
 
-        def step(inp):
-            q, k, v, do = inp
-            for wl, o, lse, grads, extra, wsb in calls:
-                kk, vv = (extra[0], extra[1]) if extra is not None else (k, v)
+        def make_slot():
+            calls, outputs = [], []
+            for wl in wls:
+                o = torch.empty((wl.o_rows, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+                lse = torch.empty((wl.num_heads, wl.o_rows), dtype=torch.float32, device=dev)
+                grads = None
+                if wl.bwd:
+                    grads = (torch.empty_like(dev_in[0]), torch.empty_like(dev_in[1]), torch.empty_like(dev_in[2]))
+                    outputs += [o, *grads]
+                else:
+                    outputs.append(o)
+                need = max(V.jfa_workspace_size(0, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
+                                                wl.nq > 0),
+                           V.jfa_workspace_size(1, offs_h, wl.batch, wl.nq, wl.num_heads, wl.head_dim, wl.causal,
+                                                wl.nq > 0) if wl.bwd else 0)
+                calls.append((wl, o, lse, grads, torch.empty(need, dtype=torch.uint8, device=dev)))
+            return calls, outputs
+
+        slots = [make_slot()]
+
+        def new_slot():
+            slots.append(make_slot())
+            return len(slots) - 1
+
+        def step(inp, slot=0):
+            q, k, v, do, offs = inp[0], inp[1], inp[2], inp[3], inp[-1]
+            for wl, o, lse, grads, wsb in slots[slot][0]:
+                kk, vv = (inp[4], inp[5]) if wl.num_kv_heads != w.num_kv_heads else (k, v)
                 V.jfa_fwd(q, kk, vv, offs, offs_h, max_len=max_len, causal=wl.causal, nq_broadcast=wl.nq, out=o,
                           lse=lse, workspace=wsb)
                 if grads is not None:
@@ -422,22 +467,29 @@ def build_job(args, dev):
                "tokens": w.total_tokens, "max_len": w.max_len}
         if w.nq:
             cfg["nq_broadcast"] = w.nq
-        return {"step": step, "dev_inputs": dev_in, "host_inputs": host, "outputs": outputs,
-                "offsets_bytes": offs_h.nbytes, "flops": flops, "bytes": {}, "dominant": "bwd_main",
-                "bound": "tensor", "config": cfg}
+        return {"step": step, "new_slot": new_slot, "outputs": lambda slot: slots[slot][1], "dev_inputs": dev_in,
+                "host_inputs": host, "flops": flops, "bytes": {}, "dominant": "bwd_main", "bound": "tensor",
+                "config": cfg}
 
     # block-diagonal: inputs drawn on the device (the full workload is 4.8 GB per tensor)
     w = W.block(args.head_dim, batch=args.block_batch)
-    dev_in = list(w.tensors(str(dev)))
     offs_h = w.offsets
-    offs = torch.from_numpy(offs_h).to(dev)
-    o = torch.empty_like(dev_in[0])
-    grads = [torch.empty_like(dev_in[i]) for i in range(3)]
-    wsb = torch.empty(V.jfa_workspace_size(2, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
-                      dtype=torch.uint8, device=dev)
+    dev_in = list(w.tensors(str(dev))) + [torch.from_numpy(offs_h.copy()).to(dev)]
+    slots = []
 
-    def step(inp):
-        q, k, v, do = inp
+    def new_slot():
+        o = torch.empty_like(dev_in[0])
+        grads = [torch.empty_like(dev_in[i]) for i in range(3)]
+        wsb = torch.empty(V.jfa_workspace_size(2, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
+                          dtype=torch.uint8, device=dev)
+        slots.append((o, grads, wsb))
+        return len(slots) - 1
+
+    new_slot()
+
+    def step(inp, slot=0):
+        q, k, v, do, offs = inp
+        o, grads, wsb = slots[slot]
         V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=o, workspace=wsb)
         V.block_attn_bwd(q, k, v, o, do, offs, offs_h, max_len=w.max_len, dq=grads[0], dk=grads[1], dv=grads[2],
                          workspace=wsb)
@@ -447,8 +499,9 @@ def build_job(args, dev):
     host = None
     if 4 * t_bytes <= (4 << 30):  # e2e only when the inputs fit a modest pinned host buffer
         host = [t.cpu().pin_memory() for t in dev_in]
-    return {"step": step, "dev_inputs": dev_in, "host_inputs": host, "outputs": [o] + grads,
-            "offsets_bytes": offs_h.nbytes, "flops": {"block_fwd": float(f), "block_bwd": float(b)},
+    return {"step": step, "new_slot": new_slot, "outputs": lambda slot: [slots[slot][0]] + slots[slot][1],
+            "dev_inputs": dev_in, "host_inputs": host,
+            "flops": {"block_fwd": float(f), "block_bwd": float(b)},
             "bytes": {"block_fwd": 4.0 * t_bytes, "block_bwd": 7.0 * t_bytes}, "dominant": "block_bwd",
             "bound": "hbm",
             "config": {"workload": w.name + " fwd+bwd", "batch": w.batch, "heads": w.num_heads,
