@@ -48,6 +48,8 @@ def _args():
                     help="jagged (default) is the headline step; the others are diagnostic lines")
     ap.add_argument("--block-batch", type=int, default=1152)
     ap.add_argument("--head-dim", type=int, default=128)
+    ap.add_argument("--copy-streams", type=int, default=4,
+                    help="copy streams per direction in the end-to-end measurement")
     return ap.parse_args()
 
 
@@ -315,37 +317,45 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in o_h[0])
         comp = torch.cuda.current_stream(dev)
-        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ran = [torch.cuda.Event(), torch.cuda.Event()]   # the slot's last step has run
-        read = [torch.cuda.Event(), torch.cuda.Event()]  # the slot's last results are on the host
-        loaded = [torch.cuda.Event(), torch.cuda.Event()]
+        n_cs = max(1, args.copy_streams)  # tensors are dealt round-robin over the copy streams
+        ups = [torch.cuda.Stream(dev) for _ in range(n_cs)]
+        downs = [torch.cuda.Stream(dev) for _ in range(n_cs)]
+        ran = [torch.cuda.Event(), torch.cuda.Event()]  # the slot's last step has run
+        loaded = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]
+        read = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]  # results on the host
 
         def e2e_run(n):
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t0.record(comp)
-            up.wait_stream(comp)
-            down.wait_stream(comp)
+            for st in ups + downs:
+                st.wait_stream(comp)
             for i in range(n):
                 s = i & 1
                 slot = 0 if s == 0 else s2
-                with torch.cuda.stream(up):
-                    if i >= 2:
-                        up.wait_event(ran[s])  # its inputs are no longer read
-                    for d, h in zip(d_in[s], host_in):
-                        d.copy_(h, non_blocking=True)
-                    loaded[s].record(up)
-                comp.wait_event(loaded[s])
+                pairs_in = list(zip(d_in[s], host_in))
+                for c, st in enumerate(ups):
+                    with torch.cuda.stream(st):
+                        if i >= 2:
+                            st.wait_event(ran[s])  # the slot's inputs are no longer read
+                        for d, h in pairs_in[c::n_cs]:
+                            d.copy_(h, non_blocking=True)
+                        loaded[s][c].record(st)
+                for ev in loaded[s]:
+                    comp.wait_event(ev)
                 if i >= 2:
-                    comp.wait_event(read[s])  # its outputs have been read back
+                    for ev in read[s]:  # the slot's outputs have been read back
+                        comp.wait_event(ev)
                 job["step"](d_in[s], slot)
                 ran[s].record(comp)
-                with torch.cuda.stream(down):
-                    down.wait_event(ran[s])
-                    for h, d in zip(o_h[s], outs[s]):
-                        h.copy_(d, non_blocking=True)
-                    read[s].record(down)
-            comp.wait_stream(up)
-            comp.wait_stream(down)
+                pairs_out = list(zip(o_h[s], outs[s]))
+                for c, st in enumerate(downs):
+                    with torch.cuda.stream(st):
+                        st.wait_event(ran[s])
+                        for h, d in pairs_out[c::n_cs]:
+                            h.copy_(d, non_blocking=True)
+                        read[s][c].record(st)
+            for st in ups + downs:
+                comp.wait_stream(st)
             t1.record(comp)
             torch.cuda.synchronize()
             return t0.elapsed_time(t1)
@@ -355,8 +365,8 @@ def main():
         e_total = max_over_ranks(float(e2e_run(args.steps)), ws)
         e2e = {"value": job_throughput(step_flops, args.steps, e_total, ws), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e_total / args.steps,
-               "overlap": "uploads and read-backs on two copy streams overlap the neighbouring steps' kernels "
+               "ms_per_step": e_total / args.steps, "copy_streams_per_direction": n_cs,
+               "overlap": "uploads and read-backs on their own copy streams overlap the neighbouring steps' kernels "
                           "(two slots of device buffers); inputs copied from host every step "
                           f"({h2d / 2**20:.0f} MiB, larger than L2)"}
 
