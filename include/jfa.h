@@ -221,6 +221,18 @@ int jfa_set_schedule(int mode);
 int jfa_get_schedule(void);
 
 /*
+ * The same two modes for the jagged backward's persistent kernel, whose units
+ * are 128-key blocks [R "Tile balancing and Cluster Launch Control"]: 0 static
+ * plan (units sorted by cost, snake-dealt over one CTA per SM), 1 Cluster Launch
+ * Control (one CTA per unit in cost order; a CTA that finishes a unit takes
+ * over the unit of a CTA not yet launched).  Initially JFA_SCHED_BWD ("static"
+ * or "clc") if set, else Cluster Launch Control; jfa_set_bwd_schedule() changes it for
+ * subsequent calls (process-wide).  Returns JFA_ERR_INVALID_ARG for another mode.
+ */
+int jfa_set_bwd_schedule(int mode);
+int jfa_get_bwd_schedule(void);
+
+/*
  * Optional kernel timing (no counterpart on the pages; measurement support).
  * jfa_profile_enable(1) starts counting every library kernel launch and
  * bracketing it with CUDA events on its stream (and forgets earlier records);

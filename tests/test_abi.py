@@ -85,6 +85,20 @@ def test_bwd_argument_errors_before_device_work(H, Hkv, causal, bq, status):
     assert st == status
 
 
+@pytest.mark.parametrize("which", ["schedule", "bwd_schedule"])
+def test_schedule_switches(which):
+    # host-side state only: no device work
+    lib = J.load()
+    set_, get_ = getattr(lib, f"jfa_set_{which}"), getattr(lib, f"jfa_get_{which}")
+    old = get_()
+    try:
+        assert set_(2) == 1 and set_(-1) == 1 and get_() == old
+        for mode in (1, 0):
+            assert set_(mode) == 0 and get_() == mode
+    finally:
+        set_(old)
+
+
 def test_planner_hooks_reject_bad_input():
     lib = J.load()
     h = np.array([1, 5], dtype=np.int32)

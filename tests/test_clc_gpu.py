@@ -1,12 +1,14 @@
-"""The jagged forward under Cluster Launch Control scheduling: same results as
-the static plan (parity with the oracle, and bit-identical outputs, since each
-unit is computed by one CTA in the same way whichever CTA takes it)."""
+"""The jagged forward and backward under Cluster Launch Control scheduling: same
+results as the static plan (parity with the oracle, and bit-identical outputs
+where each output is owned by one unit, since a unit is computed by one CTA in
+the same way whichever CTA takes it; the backward's dQ sums units in arrival
+order)."""
 import pytest
 import torch
 
 import variable_length_attention_gb300 as V
 from variable_length_attention_gb300 import workloads as W
-from tests.parity import assert_fwd_ok, check_fwd, gpu_inputs, sample_units
+from tests.parity import assert_bwd_ok, assert_fwd_ok, check_bwd, check_fwd, gpu_inputs, sample_units
 
 pytestmark = pytest.mark.gpu
 
@@ -38,3 +40,35 @@ def test_clc_full_size_matches_static(clc_mode):
     V.jfa_set_schedule("clc")
     res, _ = check_fwd(w, sel=sample_units(w.batch, w.num_heads, 8, seed=5))
     assert_fwd_ok(res)
+
+
+@pytest.fixture
+def bwd_clc_mode():
+    old = V.jfa_get_bwd_schedule()
+    V.jfa_set_bwd_schedule("clc")
+    yield
+    V.jfa_set_bwd_schedule(old)
+
+
+@pytest.mark.parametrize("w", [W.tiny(), W.custom([1, 63, 129, 257, 513, 1000], 2, 128, causal=True, seed_base=42),
+                               W.custom([5, 0, 130, 700], 2, 64, nq=300, seed_base=43),
+                               W.custom([300, 129, 700], 4, 128, num_kv_heads=2, seed_base=44)],
+                         ids=["tiny", "causal_edges", "broadcast", "gqa"])
+def test_bwd_clc_parity(bwd_clc_mode, w):
+    assert_bwd_ok(check_bwd(w))
+
+
+def test_bwd_clc_full_size_matches_static(bwd_clc_mode):
+    # causal: units of very different costs, so CTAs take over many units
+    w = W.jagged(True)
+    (q, k, v, do), offs, _ = gpu_inputs(w)
+    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=True)
+    g_clc = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets, causal=True)
+    V.jfa_set_bwd_schedule("static")
+    g_st = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets, causal=True)
+    torch.cuda.synchronize()
+    V.jfa_set_bwd_schedule("clc")
+    # dK and dV are owned by one unit each: bit-identical; dQ sums in arrival order
+    assert torch.equal(g_clc[1], g_st[1]) and torch.equal(g_clc[2], g_st[2])
+    assert (g_clc[0].float() - g_st[0].float()).abs().max().item() < 1e-2
+    assert_bwd_ok(check_bwd(w, sel=sample_units(w.batch, w.num_heads, 8, seed=6)))

@@ -230,6 +230,19 @@ int sched_mode() {
   return m;
 }
 
+static std::atomic<int> g_bwd_sched_mode{-1};
+
+int bwd_sched_mode() {
+  int m = g_bwd_sched_mode.load(std::memory_order_relaxed);
+  if (m < 0) {
+    const char* e = std::getenv("JFA_SCHED_BWD");
+    m = (e != nullptr && std::strcmp(e, "static") == 0) ? 0
+        : (e != nullptr && std::strcmp(e, "clc") == 0 ? 1 : kDefaultBwdSched);
+    g_bwd_sched_mode.store(m, std::memory_order_relaxed);
+  }
+  return m;
+}
+
 // ---------------------------------------------------------------- helpers for noalloc.cu
 // The same argument checks as jfa_fwd, then the device query; fills the row
 // counts and the SM count.
@@ -399,8 +412,10 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   // units run over the K/V heads; each loops over its group's query heads
   const int n_probe = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, 1, nullptr, nullptr);
   const int n_cta = plan_ctas(c.dev, n_probe);
+  const int clc = bwd_sched_mode();
   int n = 0;
-  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, n_cta, &units, &cta_start);
+  // Cluster Launch Control takes the units in plain cost order (the plan dealt to one CTA)
+  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, clc ? 1 : n_cta, &units, &cta_start);
   const BwdLayout lay = bwd_layout(n, n_cta, c.q_rows, c.o_rows, num_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -428,6 +443,8 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
   a.n_cta = n_cta;
+  a.n_units = n;
+  a.use_clc = clc;
   a.lse2 = reinterpret_cast<float*>(ws + lay.lse2);
   a.di = reinterpret_cast<float*>(ws + lay.di);
   a.dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc);
@@ -534,6 +551,14 @@ extern "C" int jfa_set_schedule(int mode) {
 }
 
 extern "C" int jfa_get_schedule(void) { return sched_mode(); }
+
+extern "C" int jfa_set_bwd_schedule(int mode) {
+  if (mode != 0 && mode != 1) return JFA_ERR_INVALID_ARG;
+  g_bwd_sched_mode.store(mode, std::memory_order_relaxed);
+  return JFA_OK;
+}
+
+extern "C" int jfa_get_bwd_schedule(void) { return bwd_sched_mode(); }
 
 extern "C" int jfa_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return JFA_ERR_INVALID_ARG;

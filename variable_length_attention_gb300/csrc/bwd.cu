@@ -33,9 +33,13 @@
 //                    accumulator with TMA (aixai.ru summary, "dQ epilogue": staged
 //                    writeback and early TMEM release)
 //   warp 12          tcgen05 MMA issuer
-//   warp 13          loader: K, V by TMA once per unit; per query tile Q by TMA into
-//                    a 2-deep ring (with L, Di into shared memory) and dO into a
-//                    single buffer (dV, its last reader, runs early in each tile)
+//   warp 13          loader and scheduler: publishes each unit index to the other
+//                    roles through a 4-slot ring (the CTA's slice of the static
+//                    plan, or under Cluster Launch Control its own unit and then
+//                    those of CTAs whose launch it cancels); K, V by TMA once per
+//                    unit; per query tile Q by TMA into a 2-deep ring (with L, Di
+//                    into shared memory) and dO into a single buffer (dV, its last
+//                    reader, runs early in each tile)
 // TMEM: two 128-column regions that S^T and dP^T swap every tile (P^T overwrites
 // columns 0-31 and 64-95 of S^T's region; that tile's dQ then reuses the region),
 // dV [256,256+D), dK [256+D, 256+2D).
@@ -85,7 +89,7 @@ struct Cfg {
   static constexpr int OFF_DS = OFF_DO + TILE;               // dS^T [128 keys][128 queries] bf16
   static constexpr int OFF_STG = OFF_DS + 128 * 128 * 2;     // dQ staging: two 32-column fp32 boxes
   static constexpr int OFF_BAR = OFF_STG + 2 * 128 * 128;
-  static constexpr int OFF_LD = OFF_BAR + 256;                    // per-stage L and Di, 128 floats each
+  static constexpr int OFF_LD = OFF_BAR + 384;                    // per-stage L and Di, 128 floats each
   static constexpr int SMEM_BYTES = OFF_LD + NQS * 1024;
   // No alignment slack: at head_dim 128 this is within 1 KB of the 227 KB limit.
   // The kernel checks that dynamic shared memory starts 1024-byte aligned.
@@ -107,6 +111,8 @@ struct Params {
   int* err;
   int H, Hkv, G, nq, o_rows;  // G = H / Hkv query heads per K/V head
   float scale, scale_log2;
+  int use_clc;  // 1: one CTA per unit in cost order, CTAs take over units of CTAs not yet launched
+  int n_units;
 };
 
 struct Unit {
@@ -151,9 +157,16 @@ struct Bars {
   uint64_t stg_full[2], stg_free[2];  // dQ staging slots: rows written by the 128 drain threads / read out by TMA
   uint64_t kvst_full, kvst_free;      // the same buffer holding a bf16 dK or dV tile for a TMA store
   uint64_t drain;
+  // unit schedule: the loader publishes each unit index (or -1 at the end) to
+  // the other roles through this ring
+  uint64_t sched_full[4], sched_empty[4], clc_bar;
+  int4 clc_resp;
+  int sched_unit[4];
   uint32_t tmem_base;
   int abort_flag;
 };
+
+constexpr int kSchedConsumers = 13;  // 8 P/dS warps + 4 drain warps + the MMA thread
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -169,14 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint8_t* smem = smem_raw;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
-  static_assert(sizeof(Bars) <= 256, "barrier block");
+  static_assert(sizeof(Bars) <= 384, "barrier block");
   float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LD);  // [NQS][128]
   float* s_di = s_lse + C::NQS * 128;                          // [NQS][128]
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int u_begin = p.cta_start[blockIdx.x];
-  const int u_end = p.cta_start[blockIdx.x + 1];
+  const int u_begin = p.use_clc ? 0 : p.cta_start[blockIdx.x];
+  const int u_end = p.use_clc ? 0 : p.cta_start[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -203,6 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->stg_free[s2], 1);
     }
     mbar_init(&bars->drain, 1);
+    for (int s3 = 0; s3 < 4; ++s3) {
+      mbar_init(&bars->sched_full[s3], 1);
+      mbar_init(&bars->sched_empty[s3], kSchedConsumers);
+    }
+    mbar_init(&bars->clc_bar, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -226,7 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sDS = smem + C::OFF_DS + wg * C::CHUNK + k * 128;  // row k of this half's box
     const float sl2 = p.scale_log2;
     uint32_t ph = 0, ds_ph = 0, q_it = 0;
-    for (int ui = u_begin; ui < u_end; ++ui) {
+    for (uint32_t it = 0;; ++it) {
+      const int ui = sched_pop(bars, it, ab, true);
+      if (ui == -2) goto done;
+      if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
       const bool key_ok = BK * u.n + k < u.L;
       const bool all_keys_ok = __all_sync(0xffffffffu, key_ok);  // the same in the whole warp
@@ -331,7 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t ph = 0, q_it = 0, dkv_ph = 0, kvst_full_ph = 0, kvst_free_ph = 0;
-    for (int ui = u_begin; ui < u_end; ++ui) {
+    for (uint32_t it = 0;; ++it) {
+      const int ui = sched_pop(bars, it, ab, true);
+      if (ui == -2) goto done;
+      if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
       for (int hg = 0; hg < p.G; ++hg)
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
@@ -500,7 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->s_full);
           return true;
         };
-        for (int ui = u_begin; ui < u_end; ++ui) {
+        for (uint32_t it = 0;; ++it) {
+          const int ui = sched_pop(bars, it, ab, false);
+          if (ui == -2) goto mma_done;
+          if (ui < 0) break;
           const Unit u = decode<CAUSAL>(p, ui);
           if (!mbar_wait(&bars->kv_full, kv_ph, ab)) goto mma_done;
           kv_ph ^= 1;
@@ -517,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // was, which holds the previous tile's dQ until the drain has read it.
             const uint32_t rs = region_s(q_it), rd = 128 - rs;
             // dP^T = V dO^T, once the previous dQ has left TMEM
-            if (!first || ui > u_begin) {
+            if (!first || it > 0) {
               if (!mbar_wait(&bars->dq_empty, dq_ph, ab)) goto mma_done;
               dq_ph ^= 1;
             }
@@ -574,11 +601,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 13) {
-      // ------------------------------------------------------ loader (whole warp)
+      // ------------------------------------------------------ loader and scheduler (whole warp)
+      // Static plan: this CTA's slice of the list.  Cluster Launch Control: the
+      // CTA starts with its own index and, while loading a unit, asks the
+      // hardware for a CTA that has not launched yet and takes over its unit
+      // (aixai.ru summary, "Tile balancing and Cluster Launch Control").
       uint32_t kv_ph = 0, q_it = 0;
       bool ok = true;
-      for (int ui = u_begin; ui < u_end && ok; ++ui) {
-        const Unit u = decode<CAUSAL>(p, ui);
+      int cur = p.use_clc ? static_cast<int>(blockIdx.x) : (u_begin < u_end ? u_begin : -1);
+      for (uint32_t it = 0; ok; ++it) {
+        const int slot = it & 3;
+        if (!mbar_wait(&bars->sched_empty[slot], ((it >> 2) & 1) ^ 1, ab)) break;
+        if (lane == 0) {
+          bars->sched_unit[slot] = cur;
+          mbar_arrive(&bars->sched_full[slot]);
+          if (cur >= 0 && p.use_clc) {
+            mbar_expect_tx(&bars->clc_bar, 16);
+            clc_try_cancel(&bars->clc_resp, &bars->clc_bar);
+          }
+        }
+        if (cur < 0) break;
+        const Unit u = decode<CAUSAL>(p, cur);
         if (!mbar_wait(&bars->kv_empty, kv_ph ^ 1, ab)) break;
         kv_ph ^= 1;
         if (lane == 0) {
@@ -627,6 +670,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, hq * D + c * 64,
                           u.o_base + BQ * i);
           }
+        }
+        if (!ok) break;
+        if (p.use_clc) {
+          // lane 0 alone reads the response (before it issues the next request
+          // into the same buffer) and hands it to the warp
+          int got = 1, nxt = -1;
+          if (lane == 0) {
+            got = mbar_wait(&bars->clc_bar, it & 1, ab) ? 1 : 0;
+            if (got) nxt = clc_cancelled_x(&bars->clc_resp);
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) break;
+          cur = __shfl_sync(0xffffffffu, nxt, 0);
+          if (cur >= p.n_units) cur = -1;
+        } else {
+          cur = cur + 1 < u_end ? cur + 1 : -1;
         }
       }
       if (*ab.flag) {
@@ -757,8 +815,10 @@ int launch_main(const BwdArgs& a) {
   p.o_rows = a.o_rows;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.use_clc = a.use_clc;
+  p.n_units = a.n_units;
   ProfileScope prof(kKindBwdMain, a.stream);
-  kern<<<a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+  kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

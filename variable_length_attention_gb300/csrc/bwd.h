@@ -18,6 +18,8 @@ struct BwdArgs {
   const int32_t* units;
   const int32_t* cta_start;
   int n_cta;
+  int n_units;
+  int use_clc;    // 1: grid of n_units CTAs under Cluster Launch Control (units in cost order)
   float* lse2;    // workspace [H, o_rows]
   float* di;      // workspace [H, o_rows]
   float* dq_acc;  // workspace [q_rows, H, D]

@@ -146,19 +146,6 @@ struct Bars {
 
 constexpr int kSchedConsumers = 13;  // MMA thread + 8 softmax warps + 4 epilogue warps
 
-// Next unit index from the schedule ring; -1 at the end, -2 if the CTA aborts.
-__device__ __forceinline__ int sched_pop(Bars* bars, uint32_t it, const Abort& ab, bool per_warp) {
-  const int slot = it & 3;
-  if (!mbar_wait(&bars->sched_full[slot], (it >> 2) & 1, ab)) return -2;
-  const int ui = *reinterpret_cast<volatile int*>(&bars->sched_unit[slot]);
-  if (per_warp) {
-    __syncwarp();
-    if (lane_id() == 0) mbar_arrive(&bars->sched_empty[slot]);
-  } else {
-    mbar_arrive(&bars->sched_empty[slot]);
-  }
-  return ui;
-}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)

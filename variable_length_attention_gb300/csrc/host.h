@@ -55,5 +55,9 @@ int launch_fwd(const FwdArgs& a);
 // kDefaultSched; jfa_set_schedule() changes it.
 constexpr int kDefaultSched = 1;  // measured faster on every jagged workload
 int sched_mode();
+// The same choice for the jagged backward: JFA_SCHED_BWD, else kDefaultBwdSched;
+// jfa_set_bwd_schedule() changes it.
+constexpr int kDefaultBwdSched = 1;  // measured faster on the jagged, broadcast-Q and dense backward
+int bwd_sched_mode();
 
 }  // namespace jfa

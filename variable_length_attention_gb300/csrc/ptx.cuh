@@ -297,6 +297,26 @@ __device__ __forceinline__ int clc_cancelled_x(const void* resp16) {
   return ok ? static_cast<int>(x) : -1;
 }
 
+// ------------------------------------------------------------------ unit schedule ring
+// A persistent kernel's scheduling thread publishes each work-unit index (-1 at
+// the end) into a 4-slot ring that every consumer role of the CTA reads.
+// `Bars` holds sched_full[4] (one arrival: the publisher), sched_empty[4] (one
+// arrival per consumer warp or thread) and sched_unit[4].
+// Returns the next unit index; -1 at the end, -2 if the CTA aborts.
+template <class Bars>
+__device__ __forceinline__ int sched_pop(Bars* bars, uint32_t it, const Abort& ab, bool per_warp) {
+  const int slot = it & 3;
+  if (!mbar_wait(&bars->sched_full[slot], (it >> 2) & 1, ab)) return -2;
+  const int ui = *reinterpret_cast<volatile int*>(&bars->sched_unit[slot]);
+  if (per_warp) {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(&bars->sched_empty[slot]);
+  } else {
+    mbar_arrive(&bars->sched_empty[slot]);
+  }
+  return ui;
+}
+
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));

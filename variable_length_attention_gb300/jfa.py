@@ -40,6 +40,8 @@ SIGNATURES = {
     "jfa_fwd_noalloc_capacity": (_S, []),
     "jfa_set_schedule": (_I, [_I]),
     "jfa_get_schedule": (_I, []),
+    "jfa_set_bwd_schedule": (_I, [_I]),
+    "jfa_get_bwd_schedule": (_I, []),
     "jfa_profile_enable": (_I, [_I]),
     "jfa_selftest_wait_timeout": (_I, [_P, _S, _P]),
     "jfa_profile_select": (_I, [_I]),
@@ -303,6 +305,17 @@ def jfa_set_schedule(mode):
 
 def jfa_get_schedule() -> int:
     return load().jfa_get_schedule()
+
+
+def jfa_set_bwd_schedule(mode):
+    """Work distribution of the jagged backward: 0 / "static" (host plan, one
+    CTA per SM) or 1 / "clc" (Cluster Launch Control)."""
+    m = {"static": 0, "clc": 1}.get(mode, mode)
+    _check("jfa_set_bwd_schedule", load().jfa_set_bwd_schedule(int(m)))
+
+
+def jfa_get_bwd_schedule() -> int:
+    return load().jfa_get_bwd_schedule()
 
 
 def jfa_selftest_wait_timeout(workspace) -> None:
