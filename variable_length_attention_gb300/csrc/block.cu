@@ -711,13 +711,14 @@ int launch_fwd_impl(const BlockArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tk, a.k, inner, a.rows, 64, kBlk);
   if (st == JFA_OK) st = make_map_2d(&tv, a.v, inner, a.rows, 64, kBlk);
   if (st != JFA_OK) return st;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
-      return JFA_ERR_CUDA;
-    attr = true;
-  }
+  static PerDeviceOnce setup;  // per instantiation
+  st = setup.run([]() -> int {
+    return cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+                   cudaSuccess
+               ? JFA_OK
+               : JFA_ERR_CUDA;
+  });
+  if (st != JFA_OK) return st;
   Params p{};
   p.offsets = a.offsets_dev;
   p.bpb = a.bpb;
@@ -748,13 +749,14 @@ int launch_bwd_impl(const BlockArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, inner, a.rows, 64, kBlk);
   if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, inner, a.rows, 64, kBlk);
   if (st != JFA_OK) return st;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
-      return JFA_ERR_CUDA;
-    attr = true;
-  }
+  static PerDeviceOnce setup;  // per instantiation
+  st = setup.run([]() -> int {
+    return cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+                   cudaSuccess
+               ? JFA_OK
+               : JFA_ERR_CUDA;
+  });
+  if (st != JFA_OK) return st;
   Params p{};
   p.offsets = a.offsets_dev;
   p.bpb = a.bpb;

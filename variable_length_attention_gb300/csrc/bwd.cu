@@ -789,15 +789,16 @@ int launch_main(const BwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st != JFA_OK) return st;
   auto kern = bwd_kernel<D, CAUSAL>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce setup;  // per instantiation
+  st = setup.run([&]() -> int {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return JFA_ERR_CUDA;
     if (fa.numRegs * kThreads < kRegTotal) return JFA_ERR_UNSUPPORTED;  // the split could never be granted
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
       return JFA_ERR_CUDA;
-    attr_set = true;
-  }
+    return JFA_OK;
+  });
+  if (st != JFA_OK) return st;
   Params p;
   p.units = reinterpret_cast<const int4*>(a.units);
   p.cta_start = a.cta_start;

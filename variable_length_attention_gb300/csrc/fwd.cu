@@ -564,15 +564,16 @@ int launch_impl(const FwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&to, a.o, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BM);
   if (st != JFA_OK) return st;
   auto kern = fwd_kernel<D, CAUSAL>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
+  static PerDeviceOnce setup;  // per instantiation
+  st = setup.run([&]() -> int {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return JFA_ERR_CUDA;
     if (fa.numRegs * kThreads < kRegTotal) return JFA_ERR_UNSUPPORTED;  // the split could never be granted
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
       return JFA_ERR_CUDA;
-    attr_set = true;
-  }
+    return JFA_OK;
+  });
+  if (st != JFA_OK) return st;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;

@@ -4,11 +4,36 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/jfa.h"
 
 namespace jfa {
+
+// One-time setup of a kernel on each device (its dynamic shared-memory limit,
+// the register check).  Attributes set with cudaFuncSetAttribute belong to the
+// current device, so a process that drives several GPUs sets them on each.  The
+// flags are atomic: first calls racing on several threads all run the setup,
+// which is idempotent.
+class PerDeviceOnce {
+ public:
+  // Runs `setup` (which returns a jfa status) unless it has already succeeded
+  // on the current device.
+  template <class F>
+  int run(F&& setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+    if (bit != 0 && (done_.load(std::memory_order_acquire) & bit) != 0) return JFA_OK;
+    const int st = setup();
+    if (st == JFA_OK && bit != 0) done_.fetch_or(bit, std::memory_order_release);
+    return st;
+  }
+
+ private:
+  std::atomic<uint64_t> done_{0};
+};
 
 struct DeviceInfo {
   int device = -1;
