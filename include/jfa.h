@@ -69,7 +69,8 @@ typedef enum {
   JFA_OK = 0,
   JFA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned pointer */
   JFA_ERR_UNSUPPORTED = 2,          /* head_dim not 64/128, causal+broadcast,
-                                       num_heads % num_kv_heads != 0 */
+                                       num_heads % num_kv_heads != 0, more than
+                                       2^31 - 1 broadcast output rows */
   JFA_ERR_BAD_OFFSETS = 3,          /* offsets[0] != 0, decreasing, or a length > max_len */
   JFA_ERR_WORKSPACE_TOO_SMALL = 4,
   JFA_ERR_ARCH = 5,                 /* current device is not compute capability 10.x */

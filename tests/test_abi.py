@@ -66,6 +66,16 @@ def test_fwd_argument_errors(kwargs, status):
     assert _fwd([0, 17, 40], **kwargs) == status
 
 
+def test_broadcast_row_count_overflow_rejected():
+    # batch * nq broadcast output rows past the 32-bit row index range: rejected
+    # before any device work (the empty sequences need no data)
+    lib = J.load()
+    h = np.zeros(70001, dtype=np.int32)
+    st = lib.jfa_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, h.ctypes.data_as(ctypes.c_void_p), 70000, 0, 40000,
+                     2, 2, 64, 0.125, 0, 1, FAKE, 1 << 20, None)
+    assert st == 2
+
+
 @pytest.mark.parametrize("offsets", [[5, 10], [0, 10, 4], [0, -1]])
 def test_bad_offsets(offsets):
     assert _fwd(offsets, max_len=100) == 3

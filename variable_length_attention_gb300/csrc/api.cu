@@ -207,6 +207,8 @@ static int validate_common(const void* q, const void* k, const void* v, const vo
   if (broadcast_q && nq <= 0) return JFA_ERR_INVALID_ARG;
   const int st = check_offsets(offsets_host, batch, max_len);
   if (st != JFA_OK) return st;
+  // row indices are 32-bit: the broadcast output's batch * nq rows must fit
+  if (broadcast_q && static_cast<int64_t>(batch) * nq > INT32_MAX) return JFA_ERR_UNSUPPORTED;
   c->kv_rows = offsets_host[batch];
   c->q_rows = broadcast_q ? nq : c->kv_rows;
   c->o_rows = broadcast_q ? batch * nq : c->kv_rows;
@@ -297,6 +299,7 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
   DeviceInfo dev;
   if (current_device(&dev) != JFA_OK) return 0;
   const int nq = broadcast_q ? nq_broadcast : 0;
+  if (broadcast_q && (nq <= 0 || static_cast<int64_t>(batch) * nq > INT32_MAX)) return 0;
   if (op == JFA_OP_FWD) {
     const int n = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
     return fwd_layout(n, plan_ctas(dev, n), batch).total;
