@@ -11,7 +11,9 @@
 // even passes, right to left on odd ones -- so every CTA receives a mix of long
 // and short work (aixai.ru summary, "Tile balancing and Cluster Launch Control").
 //
-// Backward: a unit is one valid 128-key block of one (sequence, head).  The
+// Backward: a unit is one valid 128-key block of one (sequence, key/value
+// head); with grouped-query attention it visits the query tiles of every query
+// head of its group, so the heads enumerated here are the key/value heads.  The
 // pages describe the backward tiles as near-equal in cost with a varying count,
 // so only valid blocks are listed and they are dealt round-robin, in an order
 // where neighbouring tiles reuse the same data in L2 (same source, same
@@ -133,7 +135,8 @@ int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
 
 int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
-  // enumeration order: sequence, head, 128-key block; cost = query tiles visited.
+  // enumeration order: sequence, head (key/value head), 128-key block; cost =
+  // query tiles visited per query head.
   // Equal costs (broadcast-Q) keep this order; unequal ones (self-attention,
   // where a unit loops over its sequence's query tiles) come largest first so
   // the snake deal balances them.
