@@ -8,6 +8,7 @@ happens in Python: if the library cannot be loaded, every call raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 import threading
@@ -104,9 +105,23 @@ def _check(name, st):
         raise JfaError(name, st)
 
 
-def _expect(name, t, shape, dtype=torch.bfloat16):
+def _on_tensor_device(fn):
+    """Run a call under the CUDA device of its first tensor argument, as a torch
+    op does: the library launches on the current device and its current
+    stream, so calling with tensors of another device would otherwise launch
+    kernels on the wrong GPU."""
+    @functools.wraps(fn)
+    def call(first, *args, **kwargs):
+        if isinstance(first, torch.Tensor) and first.is_cuda:
+            with torch.cuda.device(first.device):
+                return fn(first, *args, **kwargs)
+        return fn(first, *args, **kwargs)  # the argument checks reject it
+    return call
+
+
+def _expect(name, t, shape, dtype=torch.bfloat16, device=None):
     """The C ABI sees only pointers; check here that each tensor really is the
-    contiguous device buffer the call will read or write."""
+    contiguous device buffer the call will read or write, on the call's device."""
     if t is None:
         return
     if tuple(t.shape) != tuple(shape):
@@ -115,6 +130,8 @@ def _expect(name, t, shape, dtype=torch.bfloat16):
         raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, but the call runs on {device}")
 
 
 def _check_problem(q, k, v, offsets, offs_h, nq, *, o=None, dout=None, lse=None, dq=None, dk=None, dv=None):
@@ -125,15 +142,16 @@ def _check_problem(q, k, v, offsets, offs_h, nq, *, o=None, dout=None, lse=None,
     q_rows = nq if nq > 0 else T
     o_rows = batch * nq if nq > 0 else T
     _expect("q", q, (q_rows, H, D))
-    _expect("k", k, (T, Hkv, D))
-    _expect("v", v, (T, Hkv, D))
-    _expect("offsets", offsets, (batch + 1,), torch.int32)
-    _expect("o", o, (o_rows, H, D))
-    _expect("dout", dout, (o_rows, H, D))
-    _expect("lse", lse, (H, o_rows), torch.float32)
-    _expect("dq", dq, (q_rows, H, D))
-    _expect("dk", dk, (T, Hkv, D))
-    _expect("dv", dv, (T, Hkv, D))
+    dev = q.device
+    _expect("k", k, (T, Hkv, D), device=dev)
+    _expect("v", v, (T, Hkv, D), device=dev)
+    _expect("offsets", offsets, (batch + 1,), torch.int32, device=dev)
+    _expect("o", o, (o_rows, H, D), device=dev)
+    _expect("dout", dout, (o_rows, H, D), device=dev)
+    _expect("lse", lse, (H, o_rows), torch.float32, device=dev)
+    _expect("dq", dq, (q_rows, H, D), device=dev)
+    _expect("dk", dk, (T, Hkv, D), device=dev)
+    _expect("dv", dv, (T, Hkv, D), device=dev)
 
 
 def _workspace(op, offs_h, batch, nq, H, D, causal, bq, workspace, device):
@@ -142,6 +160,8 @@ def _workspace(op, offs_h, batch, nq, H, D, causal, bq, workspace, device):
     if workspace is not None:
         if not workspace.is_cuda or not workspace.is_contiguous():
             raise ValueError("workspace: must be a contiguous CUDA tensor")
+        if workspace.device != device:
+            raise ValueError(f"workspace: on {workspace.device}, but the call runs on {device}")
         return workspace
     need = load().jfa_workspace_size(op, offs_h.ctypes.data, batch, nq, H, D, int(causal), int(bq))
     return torch.empty(max(need, 256), dtype=torch.uint8, device=device)
@@ -157,10 +177,12 @@ def jfa_status_string(status: int) -> str:
     return load().jfa_status_string(status).decode()
 
 
+@_on_tensor_device
 def jfa_device_status(workspace) -> int:
     return load().jfa_device_status(_ptr(workspace), _stream())
 
 
+@_on_tensor_device
 def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False, scale=None,
             out=None, lse=None, return_lse=True, workspace=None):
     """Forward.  Returns (o, lse); lse is None if return_lse is False."""
@@ -190,6 +212,7 @@ def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0
     return out, lse
 
 
+@_on_tensor_device
 def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False,
             scale=None, dq=None, dk=None, dv=None, workspace=None):
     """Backward.  Returns (dq, dk, dv)."""
@@ -215,6 +238,7 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, 
     return dq, dk, dv
 
 
+@_on_tensor_device
 def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=None, out=None, workspace=None):
     """Block-diagonal (64-token blocks) forward.  Returns o."""
     L = load()
@@ -234,6 +258,7 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
     return out
 
 
+@_on_tensor_device
 def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None, scale=None, dq=None, dk=None,
                    dv=None, workspace=None):
     """Block-diagonal backward.  Returns (dq, dk, dv)."""
@@ -318,6 +343,7 @@ def jfa_get_bwd_schedule() -> int:
     return load().jfa_get_bwd_schedule()
 
 
+@_on_tensor_device
 def jfa_selftest_wait_timeout(workspace) -> None:
     """Launch the bounded-wait self-test into ``workspace`` (a CUDA uint8 tensor);
     jfa_device_status(workspace) then reports JFA_ERR_DEVICE_TIMEOUT."""
@@ -351,6 +377,7 @@ def jfa_profile_read(kind) -> tuple[float, int]:
     return ms.value, n.value
 
 
+@_on_tensor_device
 def jfa_fwd_noalloc(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False,
                     scale=None, out=None, lse=None):
     """jfa_fwd without a workspace, for callers that cannot allocate device
