@@ -6,6 +6,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import variable_length_attention_gb300 as V
 from variable_length_attention_gb300 import jfa as J
@@ -142,3 +143,16 @@ def test_binding_rejects_mismatched_shapes():
         J._check_problem(q, k, k, offs, offs.numpy(), 0)
     with pytest.raises(ValueError, match="CUDA"):  # right shapes, but host tensors
         J._check_problem(q, k, k, offs, offs.numpy(), 256)
+
+
+@pytest.mark.parametrize("by_keyword", [False, True])
+def test_binding_rejects_host_tensors(by_keyword):
+    # the entry points run under their tensors' CUDA device; host tensors are
+    # rejected by the argument checks before the library is called
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    offs = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        if by_keyword:
+            V.jfa_fwd(q=q, k=q, v=q, offsets=offs, offsets_host=[0, 4])
+        else:
+            V.jfa_fwd(q, q, q, offs, [0, 4])

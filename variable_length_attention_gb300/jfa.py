@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import functools
+import inspect
 import math
 import os
 import threading
@@ -110,12 +111,15 @@ def _on_tensor_device(fn):
     op does: the library launches on the current device and its current
     stream, so calling with tensors of another device would otherwise launch
     kernels on the wrong GPU."""
+    first_name = next(iter(inspect.signature(fn).parameters))
+
     @functools.wraps(fn)
-    def call(first, *args, **kwargs):
+    def call(*args, **kwargs):
+        first = args[0] if args else kwargs.get(first_name)
         if isinstance(first, torch.Tensor) and first.is_cuda:
             with torch.cuda.device(first.device):
-                return fn(first, *args, **kwargs)
-        return fn(first, *args, **kwargs)  # the argument checks reject it
+                return fn(*args, **kwargs)
+        return fn(*args, **kwargs)  # the argument checks reject a tensor that is not on a GPU
     return call
 
 
