@@ -105,3 +105,27 @@ def test_worked_example_block_prefix():
     bpb, ps = V.block_plan(offs, 4, 148)
     assert bpb[1] == 63 and bpb[-1] == 1152 * 63
     assert ps[-1] == (1152 * 63 + 1) // 2 * 4
+
+
+def _balance(per_cta):
+    per_cta = np.asarray(per_cta, dtype=np.float64)
+    return per_cta.mean() / per_cta.max()
+
+
+@pytest.mark.parametrize("w,fwd_min,bwd_min", [(W.jagged(False), 0.90, 0.95), (W.jagged(True), 0.90, 0.95),
+                                               (W.broadcast(), 0.85, 0.99), (W.dense(), 0.99, 0.99)],
+                         ids=["jagged", "jagged_causal", "broadcast", "dense"])
+def test_static_plans_balance_cost(w, fwd_min, bwd_min):
+    # per-CTA summed unit cost over 152 CTAs (mean / max; 1 = perfect), and the
+    # backward's sorted snake deal against plain round-robin in enumeration order
+    for fn, lo in ((V.jfa_plan_fwd, fwd_min), (V.jfa_plan_bwd, bwd_min)):
+        u, s = fn(w.offsets, w.num_heads, 152, nq=w.nq, causal=w.causal)
+        units = u.reshape(-1, 4)
+        cost = units[:, 3].astype(np.int64)
+        snake = _balance([cost[s[c]:s[c + 1]].sum() for c in range(len(s) - 1)])
+        assert snake >= lo, (fn.__name__, snake)
+        if fn is V.jfa_plan_bwd:
+            order = np.lexsort((units[:, 2], units[:, 1], units[:, 0]))  # enumeration order b, h, n
+            rr = np.zeros(152, dtype=np.int64)
+            np.add.at(rr, np.arange(len(order)) % 152, cost[order])
+            assert snake >= _balance(rr) - 1e-12
