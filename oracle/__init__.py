@@ -46,11 +46,18 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _lib_path() -> str:
+    """The compiled oracle.  tests/test_oracle_mutants.py alone sets
+    JFA_ORACLE_MUTANT_LIB, to run the pins against copies of the oracle with a
+    deliberate mistake planted in them and check that the pins fail."""
+    return os.environ.get("JFA_ORACLE_MUTANT_LIB") or build()
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(_lib_path())
             dp = ctypes.POINTER(ctypes.c_double)
             ip = ctypes.POINTER(ctypes.c_int32)
             bp = ctypes.c_void_p

@@ -152,6 +152,60 @@ def test_equal_values_rows():
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_equal_keys_give_uniform_weights(causal):
+    # All keys of a (sequence, kv head) equal: every score of a row is the same,
+    # so P is uniform over the visible keys (O = mean of those V rows, LSE =
+    # scale q.k + log(count)), and dQ_i = scale * (sum_j dS_ij) k = 0 because
+    # each row of dS sums to zero (which needs Di = sum_j P_ij dP_ij exactly).
+    rng = np.random.default_rng(12)
+    offs, q, k, v, do = _problem(rng, [6, 1, 4], 4, 2, 8)
+    for a, e in zip(offs[:-1], offs[1:]):
+        k[a:e] = k[a]
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.6, causal=causal)
+    dq, _, _, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.6, causal=causal)
+    for a, e in zip(offs[:-1], offs[1:]):
+        for i in range(e - a):
+            n = i + 1 if causal else e - a
+            for h in range(4):
+                g = h // 2
+                np.testing.assert_allclose(o[a + i, h], v[a:a + n, g].mean(axis=0), atol=1e-13)
+                np.testing.assert_allclose(lse[h, a + i], 0.6 * q[a + i, h] @ k[a, g] + math.log(n), atol=1e-13)
+    np.testing.assert_allclose(dq, 0, atol=1e-13)
+
+
+def test_causal_boundary_rows():
+    # Causal: the first query of a sequence sees only key 0, so its P is 1, its
+    # dS is 0 and dQ_0 = 0; the last key is seen only by the last query, so
+    # dV_last = P_last,last dO_last with P_last,last = exp(scale q.k - LSE) from
+    # the forward's log-sum-exp.
+    rng = np.random.default_rng(13)
+    offs, q, k, v, do = _problem(rng, [5, 3, 7], 4, 2, 8)
+    _, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.7, causal=True)
+    dq, _, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.7, causal=True)
+    for a, e in zip(offs[:-1], offs[1:]):
+        np.testing.assert_allclose(dq[a], 0, atol=1e-14)
+        last = e - 1
+        for g in range(2):
+            want = sum(math.exp(0.7 * q[last, h] @ k[last, g] - lse[h, last]) * do[last, h] for h in (2 * g, 2 * g + 1))
+            np.testing.assert_allclose(dv[last, g], want, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_backward_equals_repeated_kv(causal):
+    # Grouped-query attention is attention with each K/V head shared by its G
+    # query heads: the grouped gradients equal those of the ungrouped problem on
+    # K/V repeated per query head, with dK/dV summed over each group.
+    rng = np.random.default_rng(14)
+    offs, q, k, v, do = _problem(rng, [6, 2, 9], 6, 2, 4)
+    g = oracle.attn_bwd(q, k, v, do, offs, scale=0.5, causal=causal)
+    kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    r = oracle.attn_bwd(q, kr, vr, do, offs, scale=0.5, causal=causal)
+    np.testing.assert_allclose(g[0], r[0], atol=1e-13)
+    for grouped, repeated in ((g[1], r[1]), (g[2], r[2])):
+        np.testing.assert_allclose(grouped, repeated.reshape(-1, 2, 3, 4).sum(axis=2), atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_key_gradients_sum_to_zero(causal):
     # Shifting every key of a sequence by the same vector leaves the softmax
     # unchanged, so the key gradients of each (sequence, kv head) sum to zero.
