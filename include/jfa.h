@@ -86,9 +86,10 @@ typedef enum { JFA_OP_FWD = 0, JFA_OP_BWD = 1, JFA_OP_BLOCK_FWD = 2, JFA_OP_BLOC
  * B 2.1 Listing 1 for the online-softmax recurrence; N for the layout].
  *   o   = softmax(scale * q k^T) v per sequence and head (bf16 out),
  *   lse = log-sum-exp per row (fp32, may be NULL to skip writing it).
- * Work is planned on the host: 256-row query units sorted by K/V length and
- * dealt to one persistent CTA per SM in snake (zigzag) order [R "Tile
- * balancing"].
+ * Work is planned on the host: 256-row query units sorted by K/V length,
+ * taken in that order under Cluster Launch Control (the default) or dealt to
+ * one persistent CTA per SM in snake (zigzag) order under the static schedule
+ * [R "Tile balancing and Cluster Launch Control"; jfa_set_schedule].
  */
 int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
             const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
@@ -105,9 +106,10 @@ int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, co
  * With GQA, dk and dv of key/value head g are the sums over query heads
  * g*G .. g*G+G-1 (G = num_heads / num_kv_heads), formed in one CTA without
  * atomics.  In broadcast-Q mode dq is summed over all sequences.  Only valid
- * 128-key blocks of each (sequence, key/value head) are listed; they are sorted
- * by cost and snake-dealt to the CTAs (see jfa_plan_bwd, called with
- * num_kv_heads).
+ * 128-key blocks of each (sequence, key/value head) are listed, sorted by cost
+ * (see jfa_plan_bwd, called with num_kv_heads); they are taken in that order
+ * under Cluster Launch Control, the default, or snake-dealt to one CTA per SM
+ * under the static schedule (jfa_set_bwd_schedule).
  */
 int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
