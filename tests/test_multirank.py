@@ -67,3 +67,8 @@ def test_reference_arm_under_torchrun_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the same workload description as the measured arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == dict(bench.jagged_family_config("jagged"), parallelism="replicas x2")
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
