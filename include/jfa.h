@@ -50,6 +50,11 @@
  *  - Streams: all device work is enqueued on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream).  Calls return once the work is enqueued.
  *    The host-side offsets are read before the call returns.
+ *  - Not for stream capture: each call plans on the host and copies its plan to
+ *    the device from a small ring of host buffers that later calls reuse, so a
+ *    captured graph would replay with whatever a buffer then holds.  Do not
+ *    call these entry points while `stream` is being captured into a CUDA
+ *    graph.
  *  - Errors: every call returns a jfa_status; nothing is thrown across the ABI.
  *    Argument errors are detected before any work is enqueued.  A kernel whose
  *    internal wait times out records JFA_ERR_DEVICE_TIMEOUT in the workspace,
