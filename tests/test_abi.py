@@ -96,6 +96,52 @@ def test_bwd_argument_errors_before_device_work(H, Hkv, causal, bq, status):
     assert st == status
 
 
+def _bwd(**kw):
+    # jfa_bwd with fake pointers; every case below is rejected before device work
+    lib = J.load()
+    h = np.array([0, 10, 20], dtype=np.int32)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, D=64)
+    a.update(kw)
+    return lib.jfa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], FAKE,
+                       h.ctypes.data_as(ctypes.c_void_p), 2, 10, 0, 2, 2, a["D"], 0.125, 0, 0, FAKE, 1 << 20, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(do=None), 1), (dict(lse=None), 1), (dict(dq=None), 1), (dict(dk=None), 1), (dict(dv=None), 1),
+    (dict(dq=MISALIGNED), 1), (dict(dk=MISALIGNED), 1), (dict(do=MISALIGNED), 1), (dict(D=96), 2),
+])
+def test_bwd_buffer_errors_before_device_work(kwargs, status):
+    assert _bwd(**kwargs) == status
+
+
+def _block(bwd, offsets=(0, 64, 100), D=128, scale=0.1, **kw):
+    lib = J.load()
+    h = np.ascontiguousarray(np.asarray(offsets, dtype=np.int32))
+    batch = len(h) - 1
+    max_len = int(np.max(np.diff(h))) if batch > 0 else 0
+    hp = h.ctypes.data_as(ctypes.c_void_p)
+    a = dict(dq=FAKE, dk=FAKE, dv=FAKE, do=FAKE)
+    a.update(kw)
+    if bwd:
+        return lib.block_attn_bwd(FAKE, FAKE, FAKE, FAKE, a["do"], a["dq"], a["dk"], a["dv"], FAKE, hp, batch, max_len,
+                                  2, D, scale, FAKE, 1 << 20, None)
+    return lib.block_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, hp, batch, max_len, 2, D, scale, FAKE, 1 << 20, None)
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(D=96), 2), (dict(offsets=(0, 64, 30)), 3), (dict(offsets=(4, 64)), 3), (dict(scale=float("nan")), 1),
+    (dict(scale=0.0), 1),
+])
+def test_block_argument_errors_before_device_work(bwd, kwargs, status):
+    assert _block(bwd, **kwargs) == status
+
+
+@pytest.mark.parametrize("kwargs", [dict(dq=None), dict(do=None), dict(dk=MISALIGNED), dict(dv=MISALIGNED)])
+def test_block_bwd_buffer_errors_before_device_work(kwargs):
+    assert _block(True, **kwargs) == 1
+
+
 @pytest.mark.parametrize("which", ["schedule", "bwd_schedule"])
 def test_schedule_switches(which):
     # host-side state only: no device work
