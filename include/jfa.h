@@ -157,14 +157,31 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
  * 60,000 forward units of 256 query rows).  It calls no cudaMalloc, cudaFree or
  * other allocating routine.  All calls share the array: calls that overlap on
  * the GPU (different streams with no ordering) race, and the array keeps the
- * last call's contents.  The first call on each device looks up the array's
- * device address; make it before any stream capture.
+ * last call's contents (each call clears the error word first).  The first call
+ * on each device looks up the array's device address; make it before any
+ * stream capture.  The plan is copied from pageable host memory, so each call
+ * returns only once the work already queued on `stream` has finished.
  */
 int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
                     const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
                     int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* stream);
 /* Size in bytes of jfa_fwd_noalloc's static scratch array. */
 size_t jfa_fwd_noalloc_capacity(void);
+/*
+ * jfa_fwd_noalloc_status -- the counterpart of jfa_device_status for
+ * jfa_fwd_noalloc: synchronises `stream` and returns JFA_OK, or
+ * JFA_ERR_DEVICE_TIMEOUT if a kernel recorded a failure (a bounded wait that
+ * ran out) in the static array's error word since the last jfa_fwd_noalloc
+ * call on the current device.  Allocates nothing.
+ */
+int jfa_fwd_noalloc_status(void* stream);
+/*
+ * jfa_selftest_wait_timeout_noalloc -- the failure-path self-test (see
+ * jfa_selftest_wait_timeout) with its error word in jfa_fwd_noalloc's static
+ * array: after about 2 s jfa_fwd_noalloc_status() reports
+ * JFA_ERR_DEVICE_TIMEOUT; the next jfa_fwd_noalloc call clears it.
+ */
+int jfa_selftest_wait_timeout_noalloc(void* stream);
 
 /*
  * jfa_workspace_size -- device workspace in bytes that `op` needs for this

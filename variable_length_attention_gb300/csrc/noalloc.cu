@@ -12,7 +12,12 @@
 // the process exits.  Problems whose plan does not fit are rejected with
 // JFA_ERR_TOO_LARGE.  Nothing here calls cudaMalloc, cudaFree, cudaHostAlloc or
 // any other allocating routine; the plan reaches the device with a plain
-// cudaMemcpyAsync from host memory.
+// cudaMemcpyAsync from pageable host memory, so each call returns only after
+// the work already queued on its stream has finished (the copy waits for it).
+//
+// A kernel that gives up a bounded wait records the failure in the array's
+// error word; jfa_fwd_noalloc_status() reads it back, as jfa_device_status()
+// does for a caller's workspace.
 //
 // All calls share the array and it keeps the last call's contents: the error
 // word is cleared on every call, and calls that overlap on the GPU (different
@@ -36,6 +41,7 @@ int fwd_arg_checks(const void* q, const void* k, const void* v, const void* o, c
                    int causal, int broadcast_q, int* q_rows, int* kv_rows, int* o_rows, int* num_sms);
 int launch_fill_empty(const int32_t* empty_dev, int n_empty, int nq, int H, int D, int o_rows, void* o, float* lse,
                       cudaStream_t stream);
+int launch_wait_forever(int* err, cudaStream_t stream);
 
 namespace {
 
@@ -145,3 +151,20 @@ extern "C" int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void
 }
 
 extern "C" size_t jfa_fwd_noalloc_capacity(void) { return kStaticScratchBytes; }
+
+extern "C" int jfa_fwd_noalloc_status(void* stream_) {
+  void* scratch = nullptr;
+  int st = scratch_address(&scratch);
+  if (st != JFA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream_)) != cudaSuccess) return JFA_ERR_CUDA;
+  int err = 0;  // the error word sits at offset 0 of the array
+  if (cudaMemcpy(&err, scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+  return err == 0 ? JFA_OK : JFA_ERR_DEVICE_TIMEOUT;
+}
+
+extern "C" int jfa_selftest_wait_timeout_noalloc(void* stream_) {
+  void* scratch = nullptr;
+  const int st = scratch_address(&scratch);
+  if (st != JFA_OK) return st;
+  return launch_wait_forever(static_cast<int*>(scratch), static_cast<cudaStream_t>(stream_));
+}

@@ -33,13 +33,18 @@ __global__ void wait_forever_kernel(int* err) {
 }
 
 }  // namespace
+
+// Launches the never-completing bounded wait with its error word at `err`
+// (device memory); used by both self-test entry points.
+int launch_wait_forever(int* err, cudaStream_t stream) {
+  if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
+  wait_forever_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
 }  // namespace jfa
 
 extern "C" int jfa_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream_) {
   if (workspace == nullptr || workspace_bytes < sizeof(int)) return JFA_ERR_INVALID_ARG;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  int* err = static_cast<int*>(workspace);
-  if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return JFA_ERR_CUDA;
-  jfa::wait_forever_kernel<<<1, 32, 0, stream>>>(err);
-  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+  return jfa::launch_wait_forever(static_cast<int*>(workspace), static_cast<cudaStream_t>(stream_));
 }

@@ -40,6 +40,8 @@ SIGNATURES = {
     "block_plan": (_I, [_P, _I, _I, _I, _P, _P]),
     "jfa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "jfa_fwd_noalloc_capacity": (_S, []),
+    "jfa_fwd_noalloc_status": (_I, [_P]),
+    "jfa_selftest_wait_timeout_noalloc": (_I, [_P]),
     "jfa_set_schedule": (_I, [_I]),
     "jfa_get_schedule": (_I, []),
     "jfa_set_bwd_schedule": (_I, [_I]),
@@ -407,3 +409,15 @@ def jfa_fwd_noalloc(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_bro
                            D, float(scale), int(causal), int(bq), _stream())
     _check("jfa_fwd_noalloc", st)
     return out, lse
+
+
+def jfa_fwd_noalloc_status() -> int:
+    """Status recorded in jfa_fwd_noalloc's static scratch on the current device
+    (synchronises the current stream): 0 or a JFA_ERR_* code."""
+    return load().jfa_fwd_noalloc_status(_stream())
+
+
+def jfa_selftest_wait_timeout_noalloc() -> None:
+    """The bounded-wait self-test with its error word in jfa_fwd_noalloc's static
+    scratch; jfa_fwd_noalloc_status() then reports JFA_ERR_DEVICE_TIMEOUT."""
+    _check("jfa_selftest_wait_timeout_noalloc", load().jfa_selftest_wait_timeout_noalloc(_stream()))
