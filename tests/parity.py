@@ -27,12 +27,16 @@ def to64(t):
 
 
 def sample_units(batch, H, n, seed=0):
-    """A [batch, H] selection of about n (sequence, head) units, always including
-    the longest and the shortest sequences' units of head 0."""
+    """A [batch, H] selection of at least n (sequence, head) units drawn from a
+    seed, always including the first sequence's head 0 and the last sequence's
+    last head (the two ends of the packed tensors)."""
     rng = np.random.default_rng(seed)
     sel = np.zeros((batch, H), dtype=bool)
     flat = rng.choice(batch * H, size=min(n, batch * H), replace=False)
     sel.reshape(-1)[flat] = True
+    if batch > 0:
+        sel[0, 0] = True
+        sel[batch - 1, H - 1] = True
     return sel
 
 

@@ -46,8 +46,12 @@ def test_broadcast_full_size():
 
 
 def test_dense_full_size():
+    # dQ, dK, dV of a seeded sample of (sequence, head) units, at least 8, the
+    # first and last sequences among them
     w = W.dense(gqa=False)
-    assert_bwd_ok(check_bwd(w, sel=sample_units(w.batch, w.num_heads, 4, seed=13)))
+    sel = sample_units(w.batch, w.num_heads, 8, seed=13)
+    assert sel[0].any() and sel[w.batch - 1].any() and sel.sum() >= 8
+    assert_bwd_ok(check_bwd(w, sel=sel))
 
 
 @pytest.mark.parametrize("causal", [False, True])

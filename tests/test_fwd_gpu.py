@@ -64,6 +64,16 @@ def test_broadcast_full_size():
     assert_fwd_ok(res)
 
 
+def test_dense_full_size():
+    # the dense-equivalent stress shape (B=8 x 8192, H=16, D=128): O and LSE of a
+    # seeded sample of 10 (sequence, head) units, sequences 0 and 7 among them
+    w = W.dense(gqa=False)
+    sel = sample_units(w.batch, w.num_heads, 8, seed=14)
+    assert sel[0].any() and sel[w.batch - 1].any() and sel.sum() >= 8
+    res, _ = check_fwd(w, sel=sel)
+    assert_fwd_ok(res)
+
+
 def test_dense_gqa_full_size():
     w = W.dense(gqa=True)
     res, _ = check_fwd(w, sel=sample_units(w.batch, w.num_heads, 6, seed=4))
