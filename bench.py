@@ -50,6 +50,10 @@ def _args():
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--copy-streams", type=int, default=4,
                     help="copy streams per direction in the end-to-end measurement")
+    ap.add_argument("--passes", type=int, default=0,
+                    help="passes of the hot path per step (0: enough for --min-timed-s)")
+    ap.add_argument("--min-timed-s", type=float, default=5.0,
+                    help="timed region length the pass count is chosen for (clock samples every 200 ms)")
     return ap.parse_args()
 
 
@@ -264,6 +268,29 @@ def run_reference(args, ws, rank):
         dist.destroy_process_group()
 
 
+def _plan_ms(job, reps=50):
+    """Host planning time of one pass of the hot path: the library's own planners
+    (the calls each entry point makes before it enqueues work), on the pass's
+    offsets, timed on the host.  With the host copy of the offsets the plan needs
+    no device synchronisation and overlaps the previous kernels."""
+    import ctypes
+    from variable_length_attention_gb300 import jfa as J
+    lib = J.load()
+    plans = job["plans"]
+    if not plans:
+        return None
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for fn, offs, heads, nq, causal, n_cta in plans:
+            f = getattr(lib, fn)
+            n = f(offs.ctypes.data_as(ctypes.c_void_p), len(offs) - 1, heads, nq, int(causal), 1, None, None)
+            units = np.empty(4 * max(n, 1), dtype=np.int32)
+            start = np.empty(n_cta + 1, dtype=np.int32)
+            f(offs.ctypes.data_as(ctypes.c_void_p), len(offs) - 1, heads, nq, int(causal), n_cta,
+              units.ctypes.data_as(ctypes.c_void_p), start.ctypes.data_as(ctypes.c_void_p))
+    return (time.perf_counter() - t0) * 1e3 / reps
+
+
 def main():
     args = _args()
     ws, rank, local = _dist()
@@ -276,7 +303,7 @@ def main():
     dev = torch.device("cuda", local)
     job = build_job(args, dev)
     step, flush = job["step"], torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
-    step_flops = float(sum(job["flops"].values()))
+    pass_flops = float(sum(job["flops"].values()))
 
     def barrier():
         if ws > 1:
@@ -287,45 +314,98 @@ def main():
     for _ in range(max(args.warmup, 3)):
         step(job["dev_inputs"])
     barrier()
+    # A step is `passes` passes of the hot path, each after an L2 flush, so that
+    # the K timed steps last long enough (--min-timed-s) for the clock sampler to
+    # see the GPU under load; every pass is timed by its own pair of events.
+    if args.passes > 0:
+        passes = args.passes
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            step(job["dev_inputs"])
+        e1.record()
+        torch.cuda.synchronize()
+        est = max(e0.elapsed_time(e1) / 3, 1e-3)
+        passes = max(1, math.ceil(args.min_timed_s * 1e3 / (args.steps * est)))
+        passes = int(max_over_ranks(passes, ws))
     # ---------------------------------------------------------------- timed region (device)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(passes)]
+           for _ in range(args.steps)]
     # inside the timed region only the dominant kernel is bracketed by events
     # (every launch is still counted); the per-kernel breakdown comes from
-    # separate steps afterwards
+    # separate passes afterwards
     V.jfa_profile_select([job["dominant"]])
     V.jfa_profile_enable(True)
+    host_enqueue = 0.0
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
         for i in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps, outside the events
-            evs[i][0].record()
-            step(job["dev_inputs"])
-            evs[i][1].record()
+            for r in range(passes):
+                flush.zero_()  # L2 flush between timed passes, outside the events
+                evs[i][r][0].record()
+                h0 = time.perf_counter()
+                step(job["dev_inputs"])
+                host_enqueue += time.perf_counter() - h0
+                evs[i][r][1].record()
         barrier()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
+    step_ms = [sum(a.elapsed_time(b) for a, b in row) for row in evs]
     prof = {kind: V.jfa_profile_read(kind) for kind in V.jfa.KERNEL_KINDS}
     V.jfa_profile_enable(False)
-    # per-kernel breakdown: the same steps again, every kernel kind timed
+    total_ms = max_over_ranks(float(sum(step_ms)), ws)
+    ms_per_step = total_ms / args.steps
+    median_step = max_over_ranks(float(statistics.median(step_ms)), ws)
+    value = job_throughput(pass_flops * passes, args.steps, total_ms, ws)
+
+    # ---------------------------------------------------------------- per-kernel and per-call breakdown
+    # Outside the timed region: every kernel kind timed by the library over
+    # `steps` passes, then each entry-point call of a pass on its own (CUDA
+    # events around the call; the library's events around its kernels), so the
+    # causal and non-causal variants are reported separately.
+    n_bd = args.steps
     V.jfa_profile_select(None)
     V.jfa_profile_enable(True)
-    for i in range(args.steps):
+    for i in range(n_bd):
         flush.zero_()
         step(job["dev_inputs"])
     barrier()
     breakdown = {kind: V.jfa_profile_read(kind) for kind in V.jfa.KERNEL_KINDS}
     V.jfa_profile_enable(False)
-    total_ms = max_over_ranks(float(sum(step_ms)), ws)
-    ms_per_step = total_ms / args.steps
-    value = job_throughput(step_flops, args.steps, total_ms, ws)
+    calls = {}
+    for c in job["calls"]:
+        ms_call, ms_main = [], []
+        for i in range(n_bd):
+            flush.zero_()
+            V.jfa_profile_select([c["main"]])
+            V.jfa_profile_enable(True)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            c["run"](job["dev_inputs"])
+            b.record()
+            torch.cuda.synchronize()
+            ms_call.append(a.elapsed_time(b))
+            ms_main.append(V.jfa_profile_read(c["main"])[0])
+            V.jfa_profile_enable(False)
+        mc, mm = statistics.median(ms_call), statistics.median(ms_main)
+        ent = {"median_call_ms": mc, "median_kernel_ms": mm, "kernel": c["main"]}
+        if job["bound"] == "tensor":
+            ent["call_tflops"] = c["flops"] / (mc * 1e-3) / 1e12
+            ent["kernel_tflops"] = c["flops"] / (mm * 1e-3) / 1e12 if mm > 0 else None
+        else:
+            ent["call_gbs"] = c["bytes"] / (mc * 1e-3) / 1e9
+            ent["kernel_gbs"] = c["bytes"] / (mm * 1e-3) / 1e9 if mm > 0 else None
+        calls[c["name"]] = ent
+    V.jfa_profile_select(None)
 
     # ---------------------------------------------------------------- e2e through host buffers
-    # Every step uploads its inputs from pinned host memory (q, k, v, dO and the
+    # Every pass uploads its inputs from pinned host memory (q, k, v, dO and the
     # offsets), runs, and reads its results back (O, dQ, dK, dV) into pinned host
-    # memory.  The copies run on two copy streams and the kernels on the compute
-    # stream, with two slots of device inputs and outputs: step i+1's upload and
-    # step i-1's read-back overlap step i's kernels, and a slot is reused only
-    # after both its kernels and its read-back are done.  The timed region spans
-    # the first upload to the last read-back.
+    # memory.  The copies run on their own copy streams and the kernels on the
+    # compute stream, with two slots of device inputs and outputs: pass i+1's
+    # upload and pass i-1's read-back overlap pass i's kernels, and a slot is
+    # reused only after both its kernels and its read-back are done.  The timed
+    # region spans the first upload to the last read-back of `steps` steps of
+    # `passes` passes.
     e2e = None
     host_in = job["host_inputs"]
     if host_in is not None:
@@ -339,7 +419,7 @@ def main():
         n_cs = max(1, args.copy_streams)  # tensors are dealt round-robin over the copy streams
         ups = [torch.cuda.Stream(dev) for _ in range(n_cs)]
         downs = [torch.cuda.Stream(dev) for _ in range(n_cs)]
-        ran = [torch.cuda.Event(), torch.cuda.Event()]  # the slot's last step has run
+        ran = [torch.cuda.Event(), torch.cuda.Event()]  # the slot's last pass has run
         loaded = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]
         read = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]  # results on the host
 
@@ -381,12 +461,12 @@ def main():
 
         e2e_run(2)
         barrier()
-        e_total = max_over_ranks(float(e2e_run(args.steps)), ws)
-        e2e = {"value": job_throughput(step_flops, args.steps, e_total, ws), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+        e_total = max_over_ranks(float(e2e_run(args.steps * passes)), ws)
+        e2e = {"value": job_throughput(pass_flops * passes, args.steps, e_total, ws), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d) * passes, "d2h_bytes_per_step": int(d2h) * passes,
                "ms_per_step": e_total / args.steps, "copy_streams_per_direction": n_cs,
-               "overlap": "uploads and read-backs on their own copy streams overlap the neighbouring steps' kernels "
-                          "(two slots of device buffers); inputs copied from host every step "
+               "overlap": "uploads and read-backs on their own copy streams overlap the neighbouring passes' "
+                          "kernels (two slots of device buffers); inputs copied from host every pass "
                           f"({h2d / 2**20:.0f} MiB, larger than L2)"}
 
     # ---------------------------------------------------------------- roofline of the dominant kernel
@@ -394,27 +474,42 @@ def main():
     kind_ms = {k: v[0] for k, v in breakdown.items()}
     dom = job["dominant"]
     dom_ms, dom_n = prof[dom]
+    n_passes = args.steps * passes
     if job["bound"] == "tensor":
-        achieved = args.steps * job["flops"][dom] / (dom_ms * 1e-3) / 1e12 if dom_ms > 0 else None
+        achieved = n_passes * job["flops"][dom] / (dom_ms * 1e-3) / 1e12 if dom_ms > 0 else None
         peak, unit, psrc = peaks["bf16_tflops"], "TFLOP/s", f"{peak_src} bf16 burst"
     else:
-        achieved = args.steps * job["bytes"][dom] / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
+        achieved = n_passes * job["bytes"][dom] / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
         peak, unit, psrc = peaks["hbm_gbs"], "GB/s", f"{peak_src} HBM copy"
     roofline = {"kernel": dom, "bound": job["bound"], "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": (achieved / peak) if achieved else None, "peak_source": psrc,
                 "traffic": _traffic() if args.workload == "jagged" else None, "launches": dom_n,
                 "avg_launch_ms": dom_ms / max(dom_n, 1), "dominant_by_time": max(kind_ms, key=kind_ms.get)}
-    per_kind = {k: args.steps * f / (kind_ms[k] * 1e-3) / 1e12 for k, f in job["flops"].items() if kind_ms.get(k)}
+    if job["bound"] == "tensor" and achieved:
+        roofline["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
+    per_kind = {k: n_bd * f / (kind_ms[k] * 1e-3) / 1e12 for k, f in job["flops"].items() if kind_ms.get(k)}
     clocks = clk.summary()
+    plan_ms = _plan_ms(job)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "median_ms_per_step": median_step,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(job["config"], parallelism=f"replicas x{ws}",
-                           l2="flushed (256 MiB write) before every timed step, outside the events"),
+                           l2="flushed (256 MiB write) before every timed pass, outside the events"),
+            "passes_per_step": passes,
+            "passes_note": "a step is this many passes of the hot path, each after an L2 flush, so that the "
+                           "timed region lasts long enough for the clock samples",
             "pct_of_peak": value / ws / peaks["bf16_tflops"] * 100.0,
             "kernel_tflops": per_kind,
             "kernel_ms": {k: v for k, v in kind_ms.items() if v > 0},
-            "kernel_ms_note": "per kind, summed over the steps of a second pass after the timed region",
+            "kernel_ms_note": f"per kind, summed over {n_bd} passes after the timed region",
+            "calls": calls,
+            "calls_note": f"each entry-point call of a pass alone, median of {n_bd} after an L2 flush: the whole "
+                          "call (CUDA events around it) and its main kernel (the library's events)",
+            "host_plan_ms": plan_ms,
+            "host_plan_note": "host planning of one pass (every planner call the pass's entry points make), "
+                              "timed on the host; it overlaps the previous kernels",
+            "host_enqueue_ms_per_pass": host_enqueue * 1e3 / n_passes,
             "roofline": roofline, "clocks": clocks, "gpu_launches": int(sum(n for _, n in prof.values())),
             "e2e": e2e}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == "jagged":
@@ -491,9 +586,32 @@ def build_job(args, dev):
         flops = {"fwd": float(sum(f for f, _ in fl)),
                  "bwd_main": float(sum(b for (_, b), wl in zip(fl, wls) if wl.bwd))}
         cfg = jagged_family_config(args.workload)
+
+        def one_call(i, which):
+            def run(inp, slot=0):
+                q, k, v, do, offs = inp[0], inp[1], inp[2], inp[3], inp[-1]
+                wl, o, lse, grads, wsb = slots[slot][0][i]
+                kk, vv = (inp[4], inp[5]) if wl.num_kv_heads != w.num_kv_heads else (k, v)
+                if which == "fwd":
+                    V.jfa_fwd(q, kk, vv, offs, offs_h, max_len=max_len, causal=wl.causal, nq_broadcast=wl.nq,
+                              out=o, lse=lse, workspace=wsb)
+                else:
+                    V.jfa_bwd(q, kk, vv, o, do, lse, offs, offs_h, max_len=max_len, causal=wl.causal,
+                              nq_broadcast=wl.nq, dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+            return run
+
+        calls, plans = [], []
+        for i, (wl, (f_fwd, f_bwd)) in enumerate(zip(wls, fl)):
+            tag = ("_causal" if wl.causal else "") + ("_gqa" if wl.num_kv_heads != wl.num_heads else "")
+            calls.append({"name": "fwd" + tag, "run": one_call(i, "fwd"), "flops": float(f_fwd), "main": "fwd"})
+            plans.append(("jfa_plan_fwd", offs_h, wl.num_heads, wl.nq, wl.causal, 1))
+            if wl.bwd:
+                calls.append({"name": "bwd" + tag, "run": one_call(i, "bwd"), "flops": float(f_bwd),
+                              "main": "bwd_main"})
+                plans.append(("jfa_plan_bwd", offs_h, wl.num_kv_heads, wl.nq, wl.causal, 1))
         return {"step": step, "new_slot": new_slot, "outputs": lambda slot: slots[slot][1], "dev_inputs": dev_in,
                 "host_inputs": host, "flops": flops, "bytes": {}, "dominant": "bwd_main", "bound": "tensor",
-                "config": cfg}
+                "config": cfg, "calls": calls, "plans": plans}
 
     # block-diagonal: inputs drawn on the device (the full workload is 4.8 GB per tensor)
     w = W.block(args.head_dim, batch=args.block_batch)
@@ -520,6 +638,19 @@ def build_job(args, dev):
 
     f, b = W.flops(w)
     t_bytes = dev_in[0].numel() * 2
+
+    def run_fwd(inp, slot=0):
+        q, k, v, do, offs = inp
+        V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=slots[slot][0], workspace=slots[slot][2])
+
+    def run_bwd(inp, slot=0):
+        q, k, v, do, offs = inp
+        o, grads, wsb = slots[slot]
+        V.block_attn_bwd(q, k, v, o, do, offs, offs_h, max_len=w.max_len, dq=grads[0], dk=grads[1], dv=grads[2],
+                         workspace=wsb)
+
+    calls = [{"name": "block_fwd", "run": run_fwd, "flops": float(f), "bytes": 4.0 * t_bytes, "main": "block_fwd"},
+             {"name": "block_bwd", "run": run_bwd, "flops": float(b), "bytes": 7.0 * t_bytes, "main": "block_bwd"}]
     host = None
     if 4 * t_bytes <= (4 << 30):  # e2e only when the inputs fit a modest pinned host buffer
         host = [t.cpu().pin_memory() for t in dev_in]
@@ -527,7 +658,7 @@ def build_job(args, dev):
             "dev_inputs": dev_in, "host_inputs": host,
             "flops": {"block_fwd": float(f), "block_bwd": float(b)},
             "bytes": {"block_fwd": 4.0 * t_bytes, "block_bwd": 7.0 * t_bytes}, "dominant": "block_bwd",
-            "bound": "hbm",
+            "bound": "hbm", "calls": calls, "plans": [],
             "config": {"workload": w.name + " fwd+bwd", "batch": w.batch, "heads": w.num_heads,
                        "head_dim": w.head_dim, "tokens": w.total_tokens, "block": 64}}
 
