@@ -86,6 +86,7 @@ struct Unit {
   int n_plain;      // leading blocks that need no mask
   int n_kv0;        // blocks query tile 0 needs (causal: it skips the unit's last block when
                     // that block lies wholly in its masked future)
+  int nt;           // query tiles of the unit: 1 when the second tile lies wholly past the last row
 };
 
 template <bool CAUSAL>
@@ -107,6 +108,7 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
     u.q_row0 = u.kv0 + 2 * BM * u.m;
     u.o_row0 = u.q_row0;
   }
+  u.nt = 2 * BM * u.m + BM < u.rows ? 2 : 1;
   if (CAUSAL) {
     const int last = min(2 * BM * (u.m + 1), u.rows);
     u.n_kv = (min(last, u.L) + BN - 1) / BN;
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ui == -2) goto done;
       if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
+      if (t >= u.nt) continue;                     // a single-tile unit: nothing for tile 1
       const int qi = 2 * BM * u.m + BM * t + row;  // query index inside the sequence / shared Q
       float m_run = -INFINITY, l_run = 0.f;
       const int n_kv_t = t == 0 ? u.n_kv0 : u.n_kv;
@@ -308,14 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_dec<kRegEpilogue>();
     const int row = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t phase = 0, sf_ph = 0, sr_ph = 0;
+    uint32_t tph0 = 0, tph1 = 0, sf_ph = 0, sr_ph = 0;  // o_full / st_full phase of each tile
     const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
     for (uint32_t it = 0;; ++it) {
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
       if (ui < 0) break;
       const Unit u = decode<CAUSAL>(p, ui);
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < u.nt; ++t) {
+        const uint32_t phase = t == 0 ? tph0 : tph1;
+        if (t == 0)
+          tph0 ^= 1;
+        else
+          tph1 ^= 1;
         if (!mbar_wait(&bars->o_full[t], phase, ab)) goto done;
         if (!mbar_wait(&bars->st_full[t], phase, ab)) goto done;
         tc_fence_after();
@@ -385,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid && p.lse != nullptr)
           p.lse[static_cast<size_t>(u.h) * p.o_rows + orow] = (m_fin + log2f(l_fin)) * 0.69314718055994531f;
       }
-      phase ^= 1;
     }
     if (threadIdx.x == 256) bulk_wait_all();  // every store has landed before the CTA exits
   } else {
@@ -395,39 +402,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_o = idesc_bf16(BM, D, 0, 1);
       const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
-      uint32_t kv_it = 0, u_phase = 0;
+      uint32_t kv_it = 0;
       uint32_t p_phase[2] = {0, 0};
+      uint32_t q_ph[2] = {0, 0};   // q_full parity of each tile's next load
+      uint32_t o_cnt[2] = {0, 0};  // units that have used each O accumulator
+      bool s0_early = false;       // the current unit's first S0 was issued during the previous unit
       auto stage_of = [&](uint32_t it) { return it % C::NSTAGE; };
       auto phase_of = [&](uint32_t it) { return (it / C::NSTAGE) & 1; };
+      // Descriptors are formed once per GEMM and stepped through the K slices by
+      // adding to their start-address field (address / 16, which stays inside
+      // its 14 bits for any shared-memory address), keeping the issuing thread's
+      // register use low.
       auto issue_s = [&](int t, uint32_t stage) {
-        const uint32_t qa = sq + t * C::TILE_BYTES, ka = skv + stage * C::TILE_BYTES;
+        uint64_t qd = sdesc_sw128(sq + t * C::TILE_BYTES, 16, 1024);
+        uint64_t kd = sdesc_sw128(skv + stage * C::TILE_BYTES, 16, 1024);
+        asm volatile("" : "+l"(qd), "+l"(kd));  // formed here, not hoisted out of the unit loop
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32;
-          mma_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                 k > 0);
+          const uint32_t off16 = ((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) >> 4;
+          mma_ss(tmem + t * BN, qd + off16, kd + off16, idesc_s, k > 0);
         }
       };
       auto issue_pv = [&](int t, uint32_t stage, bool acc) {
-        const uint32_t va = skv + stage * C::TILE_BYTES;
+        uint64_t vd = sdesc_sw128(skv + stage * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        asm volatile("" : "+l"(vd));
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tmem + 256 + t * 128, tmem + t * BN + k * 8, sdesc_sw128(va + k * 2048, C::CHUNK_BYTES, 1024),
-                 idesc_o, (acc || k > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + t * 128, tmem + t * BN + k * 8, vd + ((k * 2048) >> 4), idesc_o,
+                 (acc || k > 0) ? 1u : 0u);
+      };
+      // Once tile 0 of the current unit is done, the next unit's first score
+      // GEMM (its tile-0 Q against its first K block) can run while tile 1's last
+      // softmax does, so the tensor core does not idle at the unit boundary.  It
+      // is issued only if the loader has already published that unit and its Q
+      // tile and K block have landed (non-blocking checks: a blocking wait here
+      // could hold up the releases the loader is waiting for); otherwise the next
+      // unit starts as usual.  S0's TMEM columns are free: their P was read by
+      // the tile's last PV, issued before (MMAs run in issue order).
+      auto try_early_s0 = [&](uint32_t sched_it, uint32_t kv_next) {
+        if (s0_early) return;
+        const int slot = sched_it & 3;
+        if (!mbar_try_wait(&bars->sched_full[slot], (sched_it >> 2) & 1)) return;
+        if (*reinterpret_cast<volatile int*>(&bars->sched_unit[slot]) < 0) return;
+        if (!mbar_try_wait(&bars->q_full[0], q_ph[0])) return;
+        if (!mbar_try_wait(&bars->kv_full[stage_of(kv_next)], phase_of(kv_next))) return;
+        tc_fence_after();
+        issue_s(0, stage_of(kv_next));
+        mma_commit(&bars->s_full[0]);
+        s0_early = true;
       };
       for (uint32_t it = 0;; ++it) {
         const int ui = sched_pop(bars, it, ab, false);
         if (ui < 0) break;
         const Unit u = decode<CAUSAL>(p, ui);
-        if (!mbar_wait(&bars->q_full[0], u_phase, ab)) goto mma_done;
-        if (!mbar_wait(&bars->q_full[1], u_phase, ab)) goto mma_done;
+        const uint32_t kv_next = kv_it + 2 * u.n_kv;  // the next unit's first K block in the ring
         uint32_t ks = stage_of(kv_it);
         if (!mbar_wait(&bars->kv_full[ks], phase_of(kv_it), ab)) goto mma_done;
-        tc_fence_after();
-        issue_s(0, ks);
-        mma_commit(&bars->s_full[0]);
-        issue_s(1, ks);
-        mma_commit(&bars->s_full[1]);
+        if (!s0_early) {
+          if (!mbar_wait(&bars->q_full[0], q_ph[0], ab)) goto mma_done;
+          tc_fence_after();
+          issue_s(0, ks);
+          mma_commit(&bars->s_full[0]);
+        }
+        q_ph[0] ^= 1;
+        s0_early = false;
+        if (u.nt == 2) {
+          if (!mbar_wait(&bars->q_full[1], q_ph[1], ab)) goto mma_done;
+          q_ph[1] ^= 1;
+          tc_fence_after();
+          issue_s(1, ks);
+          mma_commit(&bars->s_full[1]);
+        }
         mma_commit(&bars->kv_empty[ks]);
         if (u.n_kv == 1) mma_commit(&bars->q_empty);
         ++kv_it;
@@ -442,21 +487,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
             ++kv_it;
           }
-          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop one block early)
+          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop one block early;
+          // a single-tile unit visits every block with tile 0)
           if (j < u.n_kv0) {
-            if (j == 0 && !mbar_wait(&bars->o_empty[0], u_phase ^ 1, ab)) goto mma_done;
+            if (j == 0) {
+              if (!mbar_wait(&bars->o_empty[0], (o_cnt[0] & 1) ^ 1, ab)) goto mma_done;
+              ++o_cnt[0];
+            }
             if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
             p_phase[0] ^= 1;
             tc_fence_after();
             issue_pv(0, vs, j > 0);
-            if (j + 1 == u.n_kv0) mma_commit(&bars->o_full[0]);
-            if (j + 1 < u.n_kv0) {
+            if (j + 1 == u.n_kv0) {
+              mma_commit(&bars->o_full[0]);
+              if (u.nt == 1) mma_commit(&bars->kv_empty[vs]);
+              try_early_s0(it + 1, kv_next);
+            } else {
               issue_s(0, ks2);
               mma_commit(&bars->s_full[0]);
+              if (u.nt == 1) {
+                mma_commit(&bars->kv_empty[vs]);
+                mma_commit(&bars->kv_empty[ks2]);
+                if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+              }
             }
           }
+          if (u.nt == 1) continue;
           // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-          if (j == 0 && !mbar_wait(&bars->o_empty[1], u_phase ^ 1, ab)) goto mma_done;
+          if (j == 0) {
+            if (!mbar_wait(&bars->o_empty[1], (o_cnt[1] & 1) ^ 1, ab)) goto mma_done;
+            ++o_cnt[1];
+          }
+          if (!more) try_early_s0(it + 1, kv_next);  // a second chance before the last wait
           if (!mbar_wait(&bars->p_full[1], p_phase[1], ab)) goto mma_done;
           p_phase[1] ^= 1;
           tc_fence_after();
@@ -470,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
           }
         }
-        u_phase ^= 1;
       }
     mma_done:
       // wait until every issued MMA has landed before TMEM is released
@@ -500,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const Unit u = decode<CAUSAL>(p, cur);
         if (!mbar_wait(&bars->q_empty, u_phase ^ 1, ab)) break;
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < u.nt; ++t) {
           mbar_expect_tx(&bars->q_full[t], C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c)
