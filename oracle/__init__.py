@@ -64,9 +64,12 @@ def _load():
             i, d = ctypes.c_int, ctypes.c_double
             lib.oracle_attn_fwd.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, i, bp, dp, dp, i]
             lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, i, i, d, i, bp, dp, dp, dp, i]
+            lib.oracle_attn_fwd_window.argtypes = [dp, dp, dp, ip, i, i, i, i, i, d, i, i, bp, dp, dp, i]
+            lib.oracle_attn_bwd_window.argtypes = [dp, dp, dp, dp, ip, i, i, i, i, i, d, i, i, bp, dp, dp, dp, i]
             lib.oracle_block_fwd.argtypes = [dp, dp, dp, ip, i, i, i, d, i, bp, dp, i]
             lib.oracle_block_bwd.argtypes = [dp, dp, dp, dp, ip, i, i, i, d, i, bp, dp, dp, dp, i]
-            for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_block_fwd, lib.oracle_block_bwd):
+            for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_block_fwd, lib.oracle_block_bwd,
+                      lib.oracle_attn_fwd_window, lib.oracle_attn_bwd_window):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -92,12 +95,26 @@ def _sel(sel, batch, H):
     return s, s.ctypes.data_as(ctypes.c_void_p)
 
 
+def _window(causal, window):
+    """(left, right) of the visible window: key j is visible to query i iff
+    i - left <= j <= i + right (a side given as None or a negative number is
+    open); causal closes the right side at 0."""
+    left, right = window if window is not None else (None, None)
+    left = -1 if left is None or left < 0 else int(left)
+    right = -1 if right is None or right < 0 else int(right)
+    if causal:
+        right = 0 if right < 0 else min(right, 0)
+    return left, right
+
+
 def attn_fwd(q, k, v, offsets, *, scale: float, causal: bool = False, nq: int = 0,
-             sel=None, nthreads: int = 0, out=None):
+             sel=None, nthreads: int = 0, out=None, window=None):
     """Returns (o, lse, threads_used).
 
     Self mode (nq == 0): q [T,H,D], k/v [T,Hkv,D] -> o [T,H,D], lse [H,T].
     Broadcast (nq > 0): q [nq,H,D] -> o [B*nq,H,D], lse [H,B*nq].
+    ``window`` = (left, right) restricts query i to keys i-left .. i+right of
+    its sequence (self mode only).
     Units not selected by ``sel`` ([B,H] bool) are left as NaN.
     """
     lib = _load()
@@ -109,17 +126,19 @@ def attn_fwd(q, k, v, offsets, *, scale: float, causal: bool = False, nq: int = 
     o = np.full((rows, H, D), np.nan)
     lse = np.full((H, rows), np.nan)
     s_arr, s_ptr = _sel(sel, B, H)
-    used = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-                               B, nq, H, Hkv, D, float(scale), int(bool(causal)), s_ptr, _ptr(o), _ptr(lse),
-                               int(nthreads))
+    left, right = _window(causal, window)
+    used = lib.oracle_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v),
+                                      offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, nq, H, Hkv, D,
+                                      float(scale), left, right, s_ptr, _ptr(o), _ptr(lse), int(nthreads))
     if used < 0:
         raise ValueError(f"oracle_attn_fwd rejected its arguments ({used})")
     return o, lse, used
 
 
 def attn_bwd(q, k, v, dout, offsets, *, scale: float, causal: bool = False, nq: int = 0,
-             sel=None, nthreads: int = 0):
-    """Returns (dq, dk, dv, threads_used) for the loss sum(O * dout)."""
+             sel=None, nthreads: int = 0, window=None):
+    """Returns (dq, dk, dv, threads_used) for the loss sum(O * dout); ``window``
+    as in attn_fwd."""
     lib = _load()
     q, k, v, dout, offsets = _f64(q), _f64(k), _f64(v), _f64(dout), _offs(offsets)
     B = offsets.shape[0] - 1
@@ -129,9 +148,11 @@ def attn_bwd(q, k, v, dout, offsets, *, scale: float, causal: bool = False, nq: 
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     s_arr, s_ptr = _sel(sel, B, H)
-    used = lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
-                               offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, nq, H, Hkv, D,
-                               float(scale), int(bool(causal)), s_ptr, _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    left, right = _window(causal, window)
+    used = lib.oracle_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                      offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, nq, H, Hkv, D,
+                                      float(scale), left, right, s_ptr, _ptr(dq), _ptr(dk), _ptr(dv),
+                                      int(nthreads))
     if used < 0:
         raise ValueError(f"oracle_attn_bwd rejected its arguments ({used})")
     return dq, dk, dv, used

@@ -35,6 +35,12 @@
  *     contiguous-group map is this code's reading).
  *   - Causal: key j is visible to query i iff j <= i within the sequence (reading;
  *     the pages do not define causal masking for the jagged kernel).
+ *   - Sliding window: key j is visible to query i iff i - left <= j <= i + right
+ *     within the sequence, a negative bound leaving its side open; causal
+ *     attention is (left open, right 0).  The pages name windows among the
+ *     variants the kernels keep (commentary, "performance and feature scope";
+ *     aixai.ru summary, "MXFP8 and sparsity") without defining them; this
+ *     two-sided local window is the reading.
  *
  * All inputs and outputs are fp64 arrays, row-major [rows, heads, dim].  Work is
  * split over threads by (sequence, head) units; nothing is blocked or reordered
@@ -57,10 +63,14 @@ static double dot(const double* a, const double* b, int n) {
   return s;
 }
 
-/* Number of keys query row i may see. */
-static int visible_keys(int i, int nkeys, int causal) {
-  if (!causal) return nkeys;
-  return (i + 1 < nkeys) ? i + 1 : nkeys;
+/* Keys query row i may see: j in [*lo, *hi).  A negative left or right leaves
+   that side open; causal attention is left < 0, right = 0. */
+static void visible_range(int i, int nkeys, int left, int right, int* lo, int* hi) {
+  int a = 0, e = nkeys;
+  if (left >= 0 && i - left > a) a = i - left;
+  if (right >= 0 && i + right + 1 < e) e = i + right + 1;
+  *lo = a;
+  *hi = e > a ? e : a;
 }
 
 /*
@@ -69,31 +79,32 @@ static int visible_keys(int i, int nkeys, int causal) {
  * p is scratch of nkeys doubles.  lse may be NULL.
  */
 static void segment_fwd(const double* q, long qs, const double* k, const double* v, long ks,
-                        int nrows, int nkeys, int D, double scale, int causal,
+                        int nrows, int nkeys, int D, double scale, int left, int right,
                         double* o, long os, double* lse, long lse_stride, double* p) {
   for (int i = 0; i < nrows; ++i) {
-    const int n = visible_keys(i, nkeys, causal);
+    int j0, n;
+    visible_range(i, nkeys, left, right, &j0, &n);
     double* oi = o + (long)i * os;
-    if (n == 0) {
+    if (n == j0) {
       for (int d = 0; d < D; ++d) oi[d] = 0.0;
       if (lse) lse[(long)i * lse_stride] = -INFINITY;
       continue;
     }
     /* full score row, then its maximum */
     double m = -INFINITY;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       p[j] = scale * dot(q + (long)i * qs, k + (long)j * ks, D);
       if (p[j] > m) m = p[j];
     }
     /* softmax normaliser */
     double l = 0.0;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       p[j] = exp(p[j] - m);
       l += p[j];
     }
     /* O_i = sum_j P_ij V_j */
     for (int d = 0; d < D; ++d) oi[d] = 0.0;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       const double pij = p[j] / l;
       const double* vj = v + (long)j * ks;
       for (int d = 0; d < D; ++d) oi[d] += pij * vj[d];
@@ -108,35 +119,36 @@ static void segment_fwd(const double* q, long qs, const double* k, const double*
  */
 static void segment_bwd(const double* q, long qs, const double* k, const double* v, long ks,
                         const double* dout, long dos, int nrows, int nkeys, int D,
-                        double scale, int causal, double* dq, long dqs, double* dk,
+                        double scale, int left, int right, double* dq, long dqs, double* dk,
                         double* dv, long dks, double* p, double* dp) {
   for (int i = 0; i < nrows; ++i) {
-    const int n = visible_keys(i, nkeys, causal);
-    if (n == 0) continue;
+    int j0, n;
+    visible_range(i, nkeys, left, right, &j0, &n);
+    if (n == j0) continue;
     const double* qi = q + (long)i * qs;
     const double* doi = dout + (long)i * dos;
     /* recompute the softmax row P_i */
     double m = -INFINITY;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       p[j] = scale * dot(qi, k + (long)j * ks, D);
       if (p[j] > m) m = p[j];
     }
     double l = 0.0;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       p[j] = exp(p[j] - m);
       l += p[j];
     }
-    for (int j = 0; j < n; ++j) p[j] /= l;
+    for (int j = j0; j < n; ++j) p[j] /= l;
     /* dP_ij = dO_i . V_j and Di = sum_j P_ij dP_ij */
     double di = 0.0;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       dp[j] = dot(doi, v + (long)j * ks, D);
       di += p[j] * dp[j];
     }
     /* dS_ij = P_ij (dP_ij - Di); dQ_i += scale dS_ij K_j; dK_j += scale dS_ij Q_i;
        dV_j += P_ij dO_i */
     double* dqi = dq + (long)i * dqs;
-    for (int j = 0; j < n; ++j) {
+    for (int j = j0; j < n; ++j) {
       const double ds = p[j] * (dp[j] - di);
       const double* kj = k + (long)j * ks;
       double* dkj = dk + (long)j * dks;
@@ -158,7 +170,7 @@ typedef struct {
   /* problem */
   const double *q, *k, *v, *dout;
   const int32_t* offsets;
-  int batch, nq, H, Hkv, D, causal, block;
+  int batch, nq, H, Hkv, D, left, right, block; /* left, right: visible window (see visible_range) */
   double scale;
   const uint8_t* sel; /* [batch*H] or NULL: which (b, h) units to evaluate */
   double *o, *lse, *dq, *dk, *dv;
@@ -191,17 +203,17 @@ static void run_unit(job_t* J, long u, double* p, double* dp) {
       for (int s = 0; s < L; s += J->block) {
         const int n = (L - s < J->block) ? L - s : J->block;
         segment_fwd(J->q + (t0 + s) * qs + (long)h * D, qs, kb + (long)s * ks, vb + (long)s * ks, ks,
-                    n, n, D, J->scale, 0, J->o + (t0 + s) * qs + (long)h * D, qs, NULL, 0, p);
+                    n, n, D, J->scale, -1, -1, J->o + (t0 + s) * qs + (long)h * D, qs, NULL, 0, p);
       }
     } else if (J->nq > 0) {
       /* broadcast-Q: shared Q rows, output rows b*nq .. */
       const long r0 = (long)b * J->nq;
       const long total_rows = (long)J->batch * J->nq;
-      segment_fwd(J->q + (long)h * D, qs, kb, vb, ks, J->nq, L, D, J->scale, 0,
+      segment_fwd(J->q + (long)h * D, qs, kb, vb, ks, J->nq, L, D, J->scale, -1, -1,
                   J->o + r0 * qs + (long)h * D, qs, J->lse ? J->lse + (long)h * total_rows + r0 : NULL, 1, p);
     } else {
       const long total_rows = J->offsets[J->batch];
-      segment_fwd(J->q + t0 * qs + (long)h * D, qs, kb, vb, ks, L, L, D, J->scale, J->causal,
+      segment_fwd(J->q + t0 * qs + (long)h * D, qs, kb, vb, ks, L, L, D, J->scale, J->left, J->right,
                   J->o + t0 * qs + (long)h * D, qs, J->lse ? J->lse + (long)h * total_rows + t0 : NULL, 1, p);
     }
     return;
@@ -218,7 +230,8 @@ static void run_unit(job_t* J, long u, double* p, double* dp) {
         const int n = (L - s < step) ? L - s : step;
         const long r = t0 + s;
         segment_bwd(J->q + r * qs + (long)h * D, qs, J->k + r * ks + (long)g * D, J->v + r * ks + (long)g * D, ks,
-                    J->dout + r * qs + (long)h * D, qs, n, n, D, J->scale, J->kind == 1 ? J->causal : 0,
+                    J->dout + r * qs + (long)h * D, qs, n, n, D, J->scale, J->kind == 1 ? J->left : -1,
+                    J->kind == 1 ? J->right : -1,
                     J->dq + r * qs + (long)h * D, qs, J->dk + r * ks + (long)g * D, J->dv + r * ks + (long)g * D,
                     ks, p, dp);
       }
@@ -239,7 +252,7 @@ static void run_unit(job_t* J, long u, double* p, double* dp) {
         const int L = seq_len(J, b);
         const long t0 = J->offsets[b];
         segment_bwd(J->q + (long)h * D, qs, J->k + t0 * ks + (long)g * D, J->v + t0 * ks + (long)g * D, ks,
-                    J->dout + (long)b * nq * qs + (long)h * D, qs, (int)nq, L, D, J->scale, 0,
+                    J->dout + (long)b * nq * qs + (long)h * D, qs, (int)nq, L, D, J->scale, -1, -1,
                     part, D, J->dk + t0 * ks + (long)g * D, J->dv + t0 * ks + (long)g * D, ks, p, dp);
       }
     }
@@ -299,17 +312,25 @@ static int check_common(const int32_t* offsets, int batch, int H, int Hkv, int D
  * sel: optional [batch*H] bytes choosing which (b,h) units to evaluate.
  * Returns the number of threads used, or a negative error.
  */
-int oracle_attn_fwd(const double* q, const double* k, const double* v, const int32_t* offsets,
-                    int batch, int nq, int H, int Hkv, int D, double scale, int causal,
-                    const uint8_t* sel, double* o, double* lse, int nthreads) {
+int oracle_attn_fwd_window(const double* q, const double* k, const double* v, const int32_t* offsets,
+                           int batch, int nq, int H, int Hkv, int D, double scale, int left, int right,
+                           const uint8_t* sel, double* o, double* lse, int nthreads) {
   job_t J;
   memset(&J, 0, sizeof J);
   if (check_common(offsets, batch, H, Hkv, D, &J.max_len)) return -1;
-  if (nq > 0 && causal) return -1;
+  if (nq > 0 && (left >= 0 || right >= 0)) return -1;
   J.q = q; J.k = k; J.v = v; J.offsets = offsets; J.batch = batch; J.nq = nq;
-  J.H = H; J.Hkv = Hkv; J.D = D; J.scale = scale; J.causal = causal; J.sel = sel;
+  J.H = H; J.Hkv = Hkv; J.D = D; J.scale = scale; J.left = left; J.right = right; J.sel = sel;
   J.o = o; J.lse = lse; J.kind = 0; J.n_units = (long)batch * H; J.block = 1;
   return run_job(&J, nthreads);
+}
+
+/* The same without a window, or causal (left open, right 0). */
+int oracle_attn_fwd(const double* q, const double* k, const double* v, const int32_t* offsets,
+                    int batch, int nq, int H, int Hkv, int D, double scale, int causal,
+                    const uint8_t* sel, double* o, double* lse, int nthreads) {
+  return oracle_attn_fwd_window(q, k, v, offsets, batch, nq, H, Hkv, D, scale, -1, causal ? 0 : -1, sel, o, lse,
+                                nthreads);
 }
 
 /*
@@ -317,16 +338,17 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v, const int
  * (shaped like q), dk and dv (shaped like k); all three are overwritten.
  * Broadcast mode sums the shared-Q gradient over all sequences.
  */
-int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
-                    const int32_t* offsets, int batch, int nq, int H, int Hkv, int D, double scale,
-                    int causal, const uint8_t* sel, double* dq, double* dk, double* dv, int nthreads) {
+int oracle_attn_bwd_window(const double* q, const double* k, const double* v, const double* dout,
+                           const int32_t* offsets, int batch, int nq, int H, int Hkv, int D, double scale,
+                           int left, int right, const uint8_t* sel, double* dq, double* dk, double* dv,
+                           int nthreads) {
   job_t J;
   memset(&J, 0, sizeof J);
   if (check_common(offsets, batch, H, Hkv, D, &J.max_len)) return -1;
-  if (nq > 0 && causal) return -1;
+  if (nq > 0 && (left >= 0 || right >= 0)) return -1;
   const long T = offsets[batch];
   J.q = q; J.k = k; J.v = v; J.dout = dout; J.offsets = offsets; J.batch = batch; J.nq = nq;
-  J.H = H; J.Hkv = Hkv; J.D = D; J.scale = scale; J.causal = causal; J.sel = sel;
+  J.H = H; J.Hkv = Hkv; J.D = D; J.scale = scale; J.left = left; J.right = right; J.sel = sel;
   J.dq = dq; J.dk = dk; J.dv = dv; J.block = 1;
   memset(dk, 0, sizeof(double) * (size_t)(T * Hkv * D));
   memset(dv, 0, sizeof(double) * (size_t)(T * Hkv * D));
@@ -353,6 +375,14 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
       }
   free(J.dq_part);
   return used;
+}
+
+/* The same without a window, or causal (left open, right 0). */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    const int32_t* offsets, int batch, int nq, int H, int Hkv, int D, double scale,
+                    int causal, const uint8_t* sel, double* dq, double* dk, double* dv, int nthreads) {
+  return oracle_attn_bwd_window(q, k, v, dout, offsets, batch, nq, H, Hkv, D, scale, -1, causal ? 0 : -1, sel,
+                                dq, dk, dv, nthreads);
 }
 
 /* Block-diagonal forward: blocks of `block` tokens inside each sequence; no LSE. */

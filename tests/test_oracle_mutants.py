@@ -26,16 +26,22 @@ MUTANTS = {
         "p[j] = scale * dot(q + (long)i * qs, k + (long)j * ks, D);",
         "p[j] = dot(q + (long)i * qs, k + (long)j * ks, D);", None),
     "causal mask one key short": (
-        "return (i + 1 < nkeys) ? i + 1 : nkeys;", "return (i < nkeys) ? i : nkeys;", None),
+        "if (right >= 0 && i + right + 1 < e) e = i + right + 1;", "if (right >= 0 && i + right < e) e = i + right;",
+        None),
     "causal mask one key long": (
-        "return (i + 1 < nkeys) ? i + 1 : nkeys;", "return (i + 2 < nkeys) ? i + 2 : nkeys;", None),
+        "if (right >= 0 && i + right + 1 < e) e = i + right + 1;",
+        "if (right >= 0 && i + right + 2 < e) e = i + right + 2;", None),
+    "window start one key early": (
+        "if (left >= 0 && i - left > a) a = i - left;", "if (left >= 0 && i - left - 1 > a) a = i - left - 1;", None),
+    "window start one key late": (
+        "if (left >= 0 && i - left > a) a = i - left;", "if (left >= 0 && i - left + 1 > a) a = i - left + 1;", None),
     "row maximum not subtracted (LSE loses m)": ("p[j] = exp(p[j] - m);", "p[j] = exp(p[j]);", 0),
     "LSE without the maximum": ("lse[(long)i * lse_stride] = m + log(l);", "lse[(long)i * lse_stride] = log(l);",
                                 None),
     "LSE in base 2": ("lse[(long)i * lse_stride] = m + log(l);", "lse[(long)i * lse_stride] = m + log2(l);",
                       None),
     "output not normalised": ("const double pij = p[j] / l;", "const double pij = p[j];", None),
-    "backward P not normalised": ("for (int j = 0; j < n; ++j) p[j] /= l;", "", None),
+    "backward P not normalised": ("for (int j = j0; j < n; ++j) p[j] /= l;", "", None),
     "Di dropped from dS": ("const double ds = p[j] * (dp[j] - di);", "const double ds = p[j] * dp[j];", None),
     "Di with the wrong sign": ("const double ds = p[j] * (dp[j] - di);", "const double ds = p[j] * (dp[j] + di);",
                                None),
@@ -53,7 +59,8 @@ MUTANTS = {
         "for (int h = g * G; h < (g + 1) * G; ++h) {\n      if (!unit_selected(J, b, h)) continue;\n      const int step",
         "for (int h = g * G; h < g * G + 1; ++h) {\n      if (!unit_selected(J, b, h)) continue;\n      const int step",
         None),
-    "backward ignores the causal mask": ("J->kind == 1 ? J->causal : 0", "0", None),
+    "backward ignores the causal mask": ("J->kind == 1 ? J->right : -1", "-1", None),
+    "backward ignores the window start": ("J->kind == 1 ? J->left : -1", "-1", None),
     "broadcast: every sequence writes the first output rows": ("const long r0 = (long)b * J->nq;",
                                                                "const long r0 = 0;", None),
     "broadcast backward: dO of the first sequence for all": ("J->dout + (long)b * nq * qs", "J->dout", None),
@@ -61,7 +68,8 @@ MUTANTS = {
         "s += J.dq_part[((size_t)c * H + h) * part + (size_t)i * D + d];",
         "s = J.dq_part[((size_t)c * H + h) * part + (size_t)i * D + d];", None),
     "block forward: keys of the rest of the sequence visible": (
-        "n, n, D, J->scale, 0, J->o + (t0 + s) * qs", "n, L - s, D, J->scale, 0, J->o + (t0 + s) * qs", None),
+        "n, n, D, J->scale, -1, -1, J->o + (t0 + s) * qs", "n, L - s, D, J->scale, -1, -1, J->o + (t0 + s) * qs",
+        None),
     "block backward: whole sequence as one block": (
         "const int step = (J->kind == 4) ? J->block : (L > 0 ? L : 1);", "const int step = (L > 0 ? L : 1);", None),
 }

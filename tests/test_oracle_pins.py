@@ -270,6 +270,67 @@ def test_block_mode_equals_jagged_over_blocks(lengths):
     np.testing.assert_allclose(o_b, o_ref, rtol=0, atol=1e-12)
 
 
+# --------------------------------------------------------------------------- sliding window
+WINDOWS = [(0, 0), (2, 0), (1, 3), (5, None), (None, 2), (3, 1)]
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+@pytest.mark.parametrize("H,Hkv", [(2, 2), (4, 2)])
+def test_window_forward_matches_textbook_dense(window, H, Hkv):
+    # query i sees keys i-left .. i+right of its own sequence: the textbook form
+    # with that mask, on sequences shorter and longer than the window
+    rng = np.random.default_rng(50 + H + Hkv)
+    lengths = [3, 1, 9, 0, 7]
+    offs, q, k, v, _ = _problem(rng, lengths, H, Hkv, 8)
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.45, window=window)
+    o_ref, lse_ref = packed_dense(q, k, v, offs, 0.45, window=window)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_window_of_one_key_is_the_identity():
+    # left = right = 0: every query sees only its own key, so P = 1, O = V,
+    # LSE = scale q.k, dS = 0 (dQ = dK = 0) and dV = dO summed over the group
+    rng = np.random.default_rng(51)
+    offs, q, k, v, do = _problem(rng, [4, 1, 6], 4, 2, 8)
+    o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.8, window=(0, 0))
+    g = np.arange(4) // 2
+    np.testing.assert_array_equal(o, v[:, g])
+    np.testing.assert_allclose(lse, 0.8 * np.einsum("thd,thd->ht", q, k[:, g]), atol=1e-14)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.8, window=(0, 0))
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_allclose(dv, do.reshape(-1, 2, 2, 8).sum(axis=2), atol=1e-14)
+
+
+def test_wide_window_is_full_and_causal_window_is_causal():
+    rng = np.random.default_rng(52)
+    offs, q, k, v, do = _problem(rng, [5, 9, 2], 2, 1, 4)
+    for causal, window in ((False, (9, 9)), (True, (9, None)), (False, (9, 0))):
+        want_causal = causal or window[1] == 0
+        o, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.5, causal=causal, window=window)
+        o0, lse0, _ = oracle.attn_fwd(q, k, v, offs, scale=0.5, causal=want_causal)
+        np.testing.assert_array_equal(o, o0)
+        np.testing.assert_array_equal(lse, lse0)
+        g = oracle.attn_bwd(q, k, v, do, offs, scale=0.5, causal=causal, window=window)
+        g0 = oracle.attn_bwd(q, k, v, do, offs, scale=0.5, causal=want_causal)
+        for a, b in zip(g[:3], g0[:3]):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_window_edge_rows():
+    # With a window of `left` keys to the left and none to the right, the key
+    # gradient of key j collects queries j .. j+left only, so for a sequence
+    # longer than the window the first key's dV is the sum over queries
+    # 0 .. left of P_i0 dO_i, with P from the forward's log-sum-exp.
+    rng = np.random.default_rng(53)
+    left = 2
+    offs, q, k, v, do = _problem(rng, [8], 1, 1, 4)
+    _, lse, _ = oracle.attn_fwd(q, k, v, offs, scale=0.7, window=(left, 0))
+    _, _, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.7, window=(left, 0))
+    want = sum(math.exp(0.7 * q[i, 0] @ k[0, 0] - lse[0, i]) * do[i, 0] for i in range(left + 1))
+    np.testing.assert_allclose(dv[0, 0], want, atol=1e-13)
+
+
 # --------------------------------------------------------------------------- finite differences
 def _loss(fwd, x_name, x, base, h_idx, eps, dout):
     args = dict(base)
@@ -303,6 +364,18 @@ def test_gradients_finite_differences(causal, H, Hkv):
         return oracle.attn_fwd(q, k, v, offs, scale=scale, causal=causal)[0]
 
     dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=scale, causal=causal)
+    _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng)
+
+
+@pytest.mark.parametrize("window,H,Hkv", [((1, 0), 2, 2), ((2, 1), 4, 2), ((None, 1), 2, 1), ((3, None), 2, 2)])
+def test_window_gradients_finite_differences(window, H, Hkv):
+    rng = np.random.default_rng(60 + H + Hkv)
+    offs, q, k, v, do = _problem(rng, [5, 7, 1], H, Hkv, 4)
+
+    def fwd(q, k, v):
+        return oracle.attn_fwd(q, k, v, offs, scale=0.6, window=window)[0]
+
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, offs, scale=0.6, window=window)
     _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng)
 
 
