@@ -122,3 +122,51 @@ def test_pins_catch_planted_mistake(outcomes, name):
         assert rc == 0, last  # the unmodified oracle passes its pins
     else:
         assert rc == 1, f"{name}: pins exit {rc} ({last})"  # 1: a pin failed (not a crash, not a usage error)
+
+
+# Planted mistakes in the rotary embedding (Python, fp64): each variant of the
+# rotation must fail the rotary pins.
+def _rope_variant(kind):
+    import numpy as np
+    import oracle
+
+    def rope(x, offsets, base, *, transpose=False):
+        x = np.asarray(x, dtype=np.float64)
+        D = x.shape[2]
+        half = D // 2
+        pos = np.zeros(x.shape[0])
+        for b in range(len(offsets) - 1):
+            a, e = int(offsets[b]), int(offsets[b + 1])
+            pos[a:e] = np.arange(e - a) if kind != "global positions" else np.arange(a, e)
+        expo = -1.0 if kind == "angle exponent halved" else -2.0
+        theta = base ** (expo * np.arange(half) / D)
+        ang = pos[:, None] * theta[None, :]
+        c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+        if transpose and kind != "transpose not inverted":
+            s = -s
+        if kind == "sine with the wrong sign":
+            s = -s
+        if kind == "adjacent pairs instead of halves":
+            x1, x2 = x[..., 0::2], x[..., 1::2]
+            y = np.empty_like(x)
+            y[..., 0::2], y[..., 1::2] = x1 * c - x2 * s, x2 * c + x1 * s
+            return y
+        x1, x2 = x[..., :half], x[..., half:]
+        return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+    return rope
+
+
+ROPE_MUTANTS = ["sine with the wrong sign", "angle exponent halved", "global positions", "transpose not inverted",
+                "adjacent pairs instead of halves"]
+
+
+@pytest.mark.parametrize("kind", ROPE_MUTANTS)
+def test_rope_pins_catch_planted_mistake(kind):
+    from tests.test_oracle_pins import _rope_pins
+    with pytest.raises(AssertionError):
+        _rope_pins(_rope_variant(kind))
+
+
+def test_rope_variant_control_passes():
+    from tests.test_oracle_pins import _rope_pins
+    _rope_pins(_rope_variant("control"))

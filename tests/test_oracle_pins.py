@@ -419,3 +419,69 @@ def test_unit_selection_and_threads():
                 np.testing.assert_array_equal(o_sel[a:e, h], o_all[a:e, h])
             else:
                 assert np.all(np.isnan(o_sel[a:e, h]))
+
+
+# --------------------------------------------------------------------------- rotary embedding (block attention)
+def _rope_pins(rope_fn):
+    """The rotary pins, parameterised by the rotation so that planted mistakes
+    in it can be shown to fail them (tests/test_oracle_mutants.py)."""
+    rng = np.random.default_rng(70)
+    # closed form, D = 4: the pair (x0, x2) turns by pos, (x1, x3) by pos * base^(-1/2)
+    base = 100.0
+    offs = offsets_from_lengths([3, 5])
+    x = rng.standard_normal((8, 1, 4))
+    y = rope_fn(x, offs, base)
+    for r in range(8):
+        pos = r if r < 3 else r - 3
+        for i, ang in ((0, pos * 1.0), (1, pos * base ** -0.5)):
+            c, s = math.cos(ang), math.sin(ang)
+            a, b = x[r, 0, i], x[r, 0, i + 2]
+            assert abs(y[r, 0, i] - (a * c - b * s)) < 1e-14
+            assert abs(y[r, 0, i + 2] - (b * c + a * s)) < 1e-14
+    # the transposed rotation undoes it; every pair keeps its length
+    x = rng.standard_normal((20, 3, 8))
+    offs = offsets_from_lengths([7, 13])
+    y = rope_fn(x, offs, 10000.0)
+    np.testing.assert_allclose(rope_fn(y, offs, 10000.0, transpose=True), x, atol=1e-13)
+    np.testing.assert_allclose(y[..., :4] ** 2 + y[..., 4:] ** 2, x[..., :4] ** 2 + x[..., 4:] ** 2, atol=1e-13)
+    # scores of rotated rows depend on the positions only through their
+    # difference: equal raw rows give a Toeplitz score matrix in every sequence
+    L, D = 9, 8
+    offs = offsets_from_lengths([L, L])
+    a, b = rng.standard_normal(D), rng.standard_normal(D)
+    q = np.broadcast_to(a, (2 * L, 1, D)).copy()
+    k = np.broadcast_to(b, (2 * L, 1, D)).copy()
+    sc = rope_fn(q, offs, 50.0)[:, 0] @ rope_fn(k, offs, 50.0)[:, 0].T
+    for m in range(1, L):
+        for n in range(1, L):
+            assert abs(sc[m, n] - sc[m - 1, n - 1]) < 1e-12
+    # positions restart in every sequence
+    np.testing.assert_allclose(sc[:L, :L], sc[L:, L:], atol=1e-13)
+    np.testing.assert_allclose(sc[0, 0], a @ b, atol=1e-13)
+
+
+def test_rope_pins():
+    _rope_pins(oracle.rope)
+
+
+def test_rope_block_attention_finite_differences():
+    # gradients of rotary block attention with respect to the unrotated Q, K
+    # (the rotation's transpose carries them back) and V
+    rng = np.random.default_rng(71)
+    offs, q, k, v, do = _problem(rng, [70, 5], 1, 1, 4)
+
+    def fwd(q, k, v):
+        return oracle.block_fwd(q, k, v, offs, scale=0.5, rope_base=30.0)[0]
+
+    dq, dk, dv, _ = oracle.block_bwd(q, k, v, do, offs, scale=0.5, rope_base=30.0)
+    _check_fd(fwd, (dq, dk, dv), dict(q=q, k=k, v=v), do, rng, n_probe=20)
+
+
+def test_rope_block_attention_is_attention_of_rotated_rows():
+    # sequences of at most one 64-token block: rotary block attention is the
+    # textbook attention of the rotated Q and K rows of each sequence
+    rng = np.random.default_rng(72)
+    offs, q, k, v, _ = _problem(rng, [64, 30], 2, 2, 8)
+    o, _ = oracle.block_fwd(q, k, v, offs, scale=0.4, rope_base=1e4)
+    o_ref, _ = packed_dense(oracle.rope(q, offs, 1e4), oracle.rope(k, offs, 1e4), v, offs, 0.4)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
