@@ -20,6 +20,9 @@ block_fwd  / block_bwd: the same inside fixed blocks of ``block`` tokens;
            with ``rope_base`` the rotary embedding is applied to Q and K first
            (and the gradients are taken with respect to the unrotated Q, K).
 rope       the rotary embedding itself (and its transpose).
+topk_scores / topk_select / attn_fwd_topk: the two-stage block-sparse
+           forward (block means, top-k key blocks per query block, attention
+           over the selected blocks only).
 """
 from __future__ import annotations
 
@@ -228,3 +231,88 @@ def block_bwd(q, k, v, dout, offsets, *, scale: float, block: int = 64, sel=None
     if used < 0:
         raise ValueError(f"oracle_block_bwd rejected its arguments ({used})")
     return dq, dk, dv, used
+
+
+# --------------------------------------------------------------------------- block-sparse top-k forward
+# The aixai.ru summary ("MXFP8 and sparsity") describes a two-stage variant for
+# long histories: a cheap first stage averages blocks of Q and of K and picks
+# the top-k most relevant key blocks, and the attention kernel then attends
+# over those blocks only.  The block sizes, the score and the tie rule are not
+# given; the readings here: query blocks of 256 rows (the forward kernel's
+# unit) and key blocks of 128 keys, each block's mean over the rows it really
+# has; score = mean query . mean key (key/value head h // (H/Hkv)); the k
+# highest scores, ties to the lower block index; attention is exact softmax
+# attention over every key of the chosen blocks.
+TOPK_Q_BLOCK = 256
+TOPK_K_BLOCK = 128
+
+
+def _topk_units(offsets, H, nq):
+    """(b, h, m, query row range, key range) of every query block, in the
+    order b, h, m (a sequence without keys has none)."""
+    offsets = _offs(offsets)
+    out = []
+    for b in range(len(offsets) - 1):
+        a, e = int(offsets[b]), int(offsets[b + 1])
+        if e == a:
+            continue
+        rows = nq if nq > 0 else e - a
+        for h in range(H):
+            for m in range(-(-rows // TOPK_Q_BLOCK)):
+                r0 = m * TOPK_Q_BLOCK
+                r1 = min(rows, r0 + TOPK_Q_BLOCK)
+                out.append((b, h, m, (r0, r1), (a, e)))
+    return out
+
+
+def topk_scores(q, k, offsets, *, nq: int = 0):
+    """Stage one, fp64: for every query block (order b, h, m) the scores of the
+    key blocks of its sequence, mean query row . mean key row."""
+    q, k = _f64(q), _f64(k)
+    H, Hkv = q.shape[1], k.shape[1]
+    G = H // Hkv
+    scores = []
+    for b, h, m, (r0, r1), (a, e) in _topk_units(offsets, H, nq):
+        qb = q[r0:r1, h] if nq > 0 else q[a + r0:a + r1, h]
+        qm = qb.mean(axis=0)
+        ks = k[a:e, h // G]
+        sc = [qm @ ks[j:j + TOPK_K_BLOCK].mean(axis=0) for j in range(0, e - a, TOPK_K_BLOCK)]
+        scores.append(np.array(sc))
+    return scores
+
+
+def topk_select(scores, topk: int):
+    """The chosen key blocks of every query block: the topk highest scores
+    (all blocks if there are fewer), ties to the lower index, ascending."""
+    sel = []
+    for sc in scores:
+        order = sorted(range(len(sc)), key=lambda j: (-sc[j], j))
+        sel.append(sorted(order[:topk]))
+    return sel
+
+
+def attn_fwd_topk(q, k, v, offsets, selection, *, scale: float, nq: int = 0):
+    """Stage two, fp64: every query row attends over the keys of its query
+    block's chosen key blocks (``selection`` as topk_select returns it, in the
+    order b, h, m).  Returns (o, lse) shaped like attn_fwd's."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    offsets = _offs(offsets)
+    H, Hkv, D = q.shape[1], k.shape[1], q.shape[2]
+    G = H // Hkv
+    B = len(offsets) - 1
+    rows_out = B * nq if nq > 0 else int(offsets[-1])
+    o = np.zeros((rows_out, H, D))
+    lse = np.full((H, rows_out), -np.inf)
+    units = _topk_units(offsets, H, nq)
+    assert len(units) == len(selection)
+    for (b, h, m, (r0, r1), (a, e)), blocks in zip(units, selection):
+        keys = np.concatenate([np.arange(a + j * TOPK_K_BLOCK, min(e, a + (j + 1) * TOPK_K_BLOCK)) for j in blocks])
+        qb = q[r0:r1, h] if nq > 0 else q[a + r0:a + r1, h]
+        s = scale * (qb @ k[keys, h // G].T)
+        mx = s.max(axis=1, keepdims=True)
+        p = np.exp(s - mx)
+        l = p.sum(axis=1, keepdims=True)
+        out_rows = slice(b * nq + r0, b * nq + r1) if nq > 0 else slice(a + r0, a + r1)
+        o[out_rows, h] = (p / l) @ v[keys, h // G]
+        lse[h, out_rows] = (mx + np.log(l))[:, 0]
+    return o, lse

@@ -170,3 +170,65 @@ def test_rope_pins_catch_planted_mistake(kind):
 def test_rope_variant_control_passes():
     from tests.test_oracle_pins import _rope_pins
     _rope_pins(_rope_variant("control"))
+
+
+# Planted mistakes in the two-stage block-sparse forward (Python, fp64): each
+# must fail the top-k pins.
+def _topk_variant(kind):
+    import types
+
+    import numpy as np
+    import oracle
+
+    ns = types.SimpleNamespace(topk_scores=oracle.topk_scores, topk_select=oracle.topk_select,
+                               attn_fwd_topk=oracle.attn_fwd_topk)
+    if kind == "lowest scores chosen":
+        ns.topk_select = lambda scores, topk: [sorted(sorted(range(len(sc)), key=lambda j: (sc[j], j))[:topk])
+                                               for sc in scores]
+    elif kind == "ties to the higher index":
+        ns.topk_select = lambda scores, topk: [sorted(sorted(range(len(sc)), key=lambda j: (-sc[j], -j))[:topk])
+                                               for sc in scores]
+    elif kind == "tail block mean over the full block size":
+        def scores_fn(q, k, offsets, nq=0):
+            q, k = np.asarray(q, float), np.asarray(k, float)
+            H, Hkv = q.shape[1], k.shape[1]
+            out = []
+            for b, h, m, (r0, r1), (a, e) in oracle._topk_units(offsets, H, nq):
+                qm = (q[r0:r1, h] if nq > 0 else q[a + r0:a + r1, h]).mean(axis=0)
+                ks = k[a:e, h // (H // Hkv)]
+                out.append(np.array([qm @ (ks[j:j + 128].sum(axis=0) / 128) for j in range(0, e - a, 128)]))
+            return out
+        ns.topk_scores = scores_fn
+    elif kind == "unchosen keys attended":
+        def attn_all(q, k, v, offsets, selection, *, scale, nq=0):
+            full = [list(range(-(-(int(e) - int(a)) // 128))) for (_, _, _, _, (a, e)) in
+                    oracle._topk_units(offsets, q.shape[1], nq)]
+            return oracle.attn_fwd_topk(q, k, v, offsets, full, scale=scale, nq=nq)
+        ns.attn_fwd_topk = attn_all
+    elif kind == "query blocks of 128 rows":
+        saved = oracle.TOPK_Q_BLOCK
+
+        def scores_fn(*args, **kw):
+            oracle.TOPK_Q_BLOCK = 128
+            try:
+                return oracle.topk_scores(*args, **kw)
+            finally:
+                oracle.TOPK_Q_BLOCK = saved
+        ns.topk_scores = scores_fn
+    return ns
+
+
+TOPK_MUTANTS = ["lowest scores chosen", "ties to the higher index", "tail block mean over the full block size",
+                "unchosen keys attended", "query blocks of 128 rows"]
+
+
+@pytest.mark.parametrize("kind", TOPK_MUTANTS)
+def test_topk_pins_catch_planted_mistake(kind):
+    from tests.test_oracle_pins import _topk_pins
+    with pytest.raises((AssertionError, ValueError)):
+        _topk_pins(_topk_variant(kind))
+
+
+def test_topk_variant_control_passes():
+    from tests.test_oracle_pins import _topk_pins
+    _topk_pins(_topk_variant("control"))

@@ -485,3 +485,77 @@ def test_rope_block_attention_is_attention_of_rotated_rows():
     o, _ = oracle.block_fwd(q, k, v, offs, scale=0.4, rope_base=1e4)
     o_ref, _ = packed_dense(oracle.rope(q, offs, 1e4), oracle.rope(k, offs, 1e4), v, offs, 0.4)
     np.testing.assert_allclose(o, o_ref, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- two-stage block-sparse forward
+def _topk_pins(ns):
+    """The top-k pins, parameterised by the three stage functions (``ns`` has
+    topk_scores, topk_select, attn_fwd_topk) so that planted mistakes in them
+    can be shown to fail them (tests/test_oracle_mutants.py)."""
+    rng = np.random.default_rng(80)
+    # closed form of the scores: every row of query block m equal to a_m, every
+    # key of key block n (the short tail block too) equal to c_n; grouped heads
+    L, H, Hkv, D = 300, 4, 2, 8
+    offs = offsets_from_lengths([L, 129])
+    a = rng.standard_normal((2, H, D))
+    c = rng.standard_normal((3, Hkv, D))
+    q = np.zeros((L + 129, H, D))
+    k = np.zeros((L + 129, Hkv, D))
+    for r in range(L):
+        q[r] = a[r // 256]
+        k[r] = c[r // 128]
+    q[L:] = rng.standard_normal((129, H, D))
+    k[L:] = rng.standard_normal((129, Hkv, D))
+    sc = ns.topk_scores(q, k, offs)
+    # order b, h, m: sequence 0 has 2 query blocks per head, sequence 1 has 1
+    assert len(sc) == H * 2 + H * 1
+    for h in range(H):
+        for m in range(2):
+            want = [a[m, h] @ c[n, h // 2] for n in range(3)]
+            np.testing.assert_allclose(sc[h * 2 + m], want, atol=1e-12)
+    # selection: the k highest, ties to the lower index, ascending
+    sel = ns.topk_select([np.array([0.1, 0.9, -0.5, 0.9, 0.3])], 2)
+    assert sel == [[1, 3]]
+    assert ns.topk_select([np.array([0.5, 0.2, 0.5, 0.5])], 2) == [[0, 2]]
+    assert ns.topk_select([np.array([3.0, 1.0])], 5) == [[0, 1]]
+    # every block chosen: exact attention
+    offs = offsets_from_lengths([300, 40, 513])
+    q = rng.standard_normal((853, 2, 8))
+    k = rng.standard_normal((853, 2, 8))
+    v = rng.standard_normal((853, 2, 8))
+    sel = ns.topk_select(ns.topk_scores(q, k, offs), 99)
+    o, lse = ns.attn_fwd_topk(q, k, v, offs, sel, scale=0.4)
+    o_ref, lse_ref, _ = oracle.attn_fwd(q, k, v, offs, scale=0.4)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-12)
+    # one chosen block: textbook attention over that block's keys, per query
+    # block of 256 rows (rows 0..255 and 256..299 of sequence 0 choose
+    # different blocks here)
+    # units of sequence 0: (h0, m0), (h0, m1), (h1, m0), (h1, m1); then sequence 1
+    # (one query block per head) and sequence 2 (three per head)
+    sel1 = [[2], [0], [2], [0]] + [[0]] * 2 + [[1], [3], [4], [1], [3], [4]]
+    assert len(sel1) == len(sel)
+    o1, _ = ns.attn_fwd_topk(q, k, v, offs, sel1, scale=0.4)
+    for h in range(2):
+        s = 0.4 * q[0:256, h] @ k[256:300, h].T
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        np.testing.assert_allclose(o1[0:256, h], (p / p.sum(axis=1, keepdims=True)) @ v[256:300, h], atol=1e-12)
+        s = 0.4 * q[256:300, h] @ k[0:128, h].T
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        np.testing.assert_allclose(o1[256:300, h], (p / p.sum(axis=1, keepdims=True)) @ v[0:128, h], atol=1e-12)
+    # broadcast-Q: query blocks of the shared Q against each sequence, an empty
+    # sequence has none; every block chosen is exact broadcast attention
+    offs = offsets_from_lengths([200, 0, 390])
+    qs = rng.standard_normal((300, 2, 8))
+    k = rng.standard_normal((590, 2, 8))
+    v = rng.standard_normal((590, 2, 8))
+    sel = ns.topk_select(ns.topk_scores(qs, k, offs, nq=300), 99)
+    assert len(sel) == 2 * 2 * 2  # 2 sequences with keys x 2 heads x 2 query blocks
+    o, lse = ns.attn_fwd_topk(qs, k, v, offs, sel, scale=0.3, nq=300)
+    o_ref, lse_ref, _ = oracle.attn_fwd(qs, k, v, offs, scale=0.3, nq=300)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    assert np.array_equal(np.isinf(lse), np.isinf(lse_ref))
+
+
+def test_topk_pins():
+    _topk_pins(oracle)
