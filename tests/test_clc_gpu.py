@@ -72,3 +72,37 @@ def test_bwd_clc_full_size_matches_static(bwd_clc_mode):
     assert torch.equal(g_clc[1], g_st[1]) and torch.equal(g_clc[2], g_st[2])
     assert (g_clc[0].float() - g_st[0].float()).abs().max().item() < 1e-2
     assert_bwd_ok(check_bwd(w, sel=sample_units(w.batch, w.num_heads, 8, seed=6)))
+
+
+@pytest.fixture
+def block_clc_mode():
+    old = V.jfa_get_block_schedule()
+    V.jfa_set_block_schedule("clc")
+    yield
+    V.jfa_set_block_schedule(old)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lengths", [[64, 128, 192], [130, 64, 7, 1, 0, 63, 65, 200], [4032] * 3, [0, 150, 0]])
+def test_block_clc_parity(block_clc_mode, D, lengths):
+    # chunks of 16 tiles taken under Cluster Launch Control: parity with the
+    # oracle, including tail blocks, empty sequences and an odd block count
+    from tests.test_block_gpu import _assert, _compare, _run
+    w = W.custom(lengths, 3, D, mode="block", seed_base=970 + D + len(lengths))
+    q, k, v, do = [t.cuda() for t in w.tensors("cpu")]
+    o, dq, dk, dv = _run(w, q, k, v, do)
+    _assert(_compare(w, [b for b in range(w.batch) if w.lengths[b] > 0], q, k, v, do, o, dq, dk, dv))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_block_clc_matches_static(block_clc_mode, D):
+    # every tile owns its outputs, so the two schedules give identical bits
+    from tests.test_block_gpu import _run
+    w = W.block(D, batch=96)
+    q, k, v, do = w.tensors("cuda")
+    r_clc = _run(w, q, k, v, do)
+    V.jfa_set_block_schedule("static")
+    r_st = _run(w, q, k, v, do)
+    V.jfa_set_block_schedule("clc")
+    for a, b in zip(r_clc, r_st):
+        assert torch.equal(a, b)

@@ -9,15 +9,26 @@
 // recomputes P from Q and K, forms Di = rowsum(P o dP) inline, and every block
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
+// Rotary embedding (the "with rotary fused" variant of "TLX Block Attention",
+// introduction): when the caller passes cos/sin tables, Q and K are rotated in
+// shared memory right after they land -- the rotate-half form, row position =
+// index inside its sequence -- and the backward carries dQ and dK back through
+// the transposed rotation before storing them, so no separate pass over Q, K,
+// dQ or dK is needed.
+//
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
 // rows 64-127 block 2p+1, and the off-diagonal quadrants of the 128 x 128 score
 // tile are masked.  That doubles the tensor work, which is free here: the kernel
 // moves ~33 FLOP per byte, far below the ridge, so it is bound by HBM
 // ("TLX Block Attention", section 3.3).  Persistent programs take balanced
-// contiguous ranges of (pair, head) tiles from the host plan, and find the
-// sequence of a global block by a branchless binary search over the per-batch
-// block prefix sums (section 5).
+// contiguous ranges of (pair, head) tiles from the host plan, or, under
+// Cluster Launch Control, chunks of consecutive tiles: one CTA per chunk is
+// launched and a CTA that finishes a chunk cancels the launch of a CTA not yet
+// running and takes its chunk, so imbalance that shows only at run time is
+// absorbed ("TLX Block Attention", section 5; aixai.ru summary, "Tile balancing
+// and Cluster Launch Control").  The sequence of a global block is found by a
+// branchless binary search over the per-batch block prefix sums (section 5).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,20 +47,80 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct Params {
   const int32_t* offsets;
   const int32_t* bpb;         // [batch+1] prefix sums of blocks per sequence
-  const int32_t* prog_start;  // [P+1]
+  const int32_t* prog_start;  // [P+1] (static ranges)
   int* err;
   __nv_bfloat16 *o, *dq, *dk, *dv;
   int batch, H, n_blocks;
   float scale, scale_log2;
+  int use_clc;                // 1: one CTA per chunk of `chunk` tiles, Cluster Launch Control
+  int chunk, n_tiles, n_chunks;
+  const float* rope_cos;      // rotary tables [positions, D/2] (rotary variant only)
+  const float* rope_sin;
 };
+
+// Tiles [*tb, *te) of schedule entry `ch`: chunk ch under Cluster Launch
+// Control, else the CTA's own static range.
+__device__ __forceinline__ void chunk_range(const Params& p, int ch, int* tb, int* te) {
+  if (p.use_clc) {
+    *tb = ch * p.chunk;
+    *te = min(*tb + p.chunk, p.n_tiles);
+  } else {
+    *tb = p.prog_start[blockIdx.x];
+    *te = p.prog_start[blockIdx.x + 1];
+  }
+}
+
+// The tiles a CTA works on, in order, as every role sees them: the loader
+// publishes schedule entries (chunks) through the 4-slot ring; each consumer
+// walks the tiles of the entries it pops.
+struct TileCursor {
+  int t = 0, te = 0;
+  uint32_t sit = 0;
+};
+// Next tile id; -1 at the end, -2 if the CTA aborts.
+template <class Bars>
+__device__ __forceinline__ int next_tile(TileCursor& c, Bars* bars, const Params& p, const Abort& ab, bool per_warp) {
+  while (c.t >= c.te) {
+    const int ch = sched_pop(bars, c.sit++, ab, per_warp);
+    if (ch < 0) return ch;
+    chunk_range(p, ch, &c.t, &c.te);
+  }
+  return c.t++;
+}
+
+// The loader's side of the schedule: publishes entry `cur` in ring slot `sit`,
+// and under Cluster Launch Control asks for a CTA not yet launched.  Returns
+// false if the CTA aborts.
+template <class Bars>
+__device__ __forceinline__ bool publish(Bars* bars, uint32_t sit, int cur, const Params& p, const Abort& ab) {
+  const int slot = sit & 3;
+  if (!mbar_wait(&bars->sched_empty[slot], ((sit >> 2) & 1) ^ 1, ab)) return false;
+  bars->sched_unit[slot] = cur;
+  mbar_arrive(&bars->sched_full[slot]);
+  if (cur >= 0 && p.use_clc) {
+    mbar_expect_tx(&bars->clc_bar, 16);
+    clc_try_cancel(&bars->clc_resp, &bars->clc_bar);
+  }
+  return true;
+}
+// The entry after `sit`'s: the cancelled CTA's chunk, or -1 (also -1 under the
+// static ranges, which have one entry); -2 if the CTA aborts.
+template <class Bars>
+__device__ __forceinline__ int next_entry(Bars* bars, uint32_t sit, const Params& p, const Abort& ab) {
+  if (!p.use_clc) return -1;
+  if (!mbar_wait(&bars->clc_bar, sit & 1, ab)) return -2;
+  const int nxt = clc_cancelled_x(&bars->clc_resp);
+  return nxt >= p.n_chunks ? -1 : nxt;
+}
 
 // One 64-token block: first token row and length (0 if the block does not exist).
 struct Blk {
   int row0, len;
+  int pos0;  // position of the block's first row inside its sequence
 };
 
 __device__ __forceinline__ Blk locate(const Params& p, int g) {
-  Blk r{0, 0};
+  Blk r{0, 0, 0};
   if (g >= p.n_blocks) return r;
   // largest b in [0, batch) with bpb[b] <= g (branchless halving search)
   int lo = 0, n = p.batch;
@@ -63,7 +134,63 @@ __device__ __forceinline__ Blk locate(const Params& p, int g) {
   const int L = __ldg(p.offsets + lo + 1) - s;
   r.row0 = s + kBlk * j;
   r.len = min(kBlk, L - kBlk * j);
+  r.pos0 = kBlk * j;
   return r;
+}
+
+// Rotates row r of a 128-row bf16 tile stored as D/64 128-byte-swizzled
+// 64-column boxes, in place: for i < D/2 the pair (x_i, x_{i+D/2}) becomes
+// (x_i c_i - x_{i+D/2} s_i, x_{i+D/2} c_i + x_i s_i), c and s being the row's
+// cosine and sine table rows.
+template <int D>
+__device__ __forceinline__ void rope_smem_row(uint8_t* tile, int r, const float* __restrict__ cs,
+                                              const float* __restrict__ sn) {
+  constexpr int HC = D / 16;  // 16-byte pieces (8 columns) in half a row
+#pragma unroll
+  for (int j = 0; j < HC; ++j) {
+    const int j2 = j + HC;
+    const uint32_t a1 = smem_u32(tile + (j / 8) * 16384 + r * 128 + (((j % 8) ^ (r & 7)) << 4));
+    const uint32_t a2 = smem_u32(tile + (j2 / 8) * 16384 + r * 128 + (((j2 % 8) ^ (r & 7)) << 4));
+    uint32_t x[4], y[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2));
+    const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + 8 * j));
+    const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + 8 * j + 4));
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(sn + 8 * j));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(sn + 8 * j + 4));
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
+      const float2 w = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y[e]));
+      x[e] = pack_bf16(u.x * c[2 * e] - w.x * sv[2 * e], u.y * c[2 * e + 1] - w.y * sv[2 * e + 1]);
+      y[e] = pack_bf16(w.x * c[2 * e] + u.x * sv[2 * e], w.y * c[2 * e + 1] + u.y * sv[2 * e + 1]);
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a2), "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
+                 : "memory");
+  }
+}
+
+// The rotation of one Q/K tile pair by a warpgroup (thread r takes row r of
+// both): rows past their block's end are left alone (their scores are masked).
+template <int D>
+__device__ __forceinline__ void rope_tile(const Params& p, uint8_t* q_tile, uint8_t* k_tile, int r, const Blk& blk) {
+  const int rr = r & 63;
+  if (rr >= blk.len) return;
+  const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
+  rope_smem_row<D>(q_tile, r, p.rope_cos + at, p.rope_sin + at);
+  rope_smem_row<D>(k_tile, r, p.rope_cos + at, p.rope_sin + at);
+}
+
+// (g1, g2) <- (g1 c + g2 s, g2 c - g1 s): the transposed rotation of one column
+// pair of a gradient row, in fp32 before it is rounded.
+__device__ __forceinline__ void rope_back(float& g1, float& g2, float c, float s) {
+  const float a = g1 * c + g2 * s, b = g2 * c - g1 * s;
+  g1 = a;
+  g2 = b;
 }
 
 // Operands come in two rings: Q and K of a tile together (released as soon as
@@ -78,17 +205,22 @@ struct FwdCfg {
                                                    // faster than filling the 227 KB)
   static constexpr int OFF_V = NQK * 2 * TILE;
   static constexpr int OFF_BAR = OFF_V + NV * TILE;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct FwdBars {
+  int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[2], qk_empty[2], v_full[6], v_empty[6];
+  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
   uint64_t drain;
+  uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
+  int sched_unit[4];
   uint32_t tmem_base;
   int abort_flag;
 };
+constexpr int kFwdSchedConsumers = 9;  // the MMA thread and the 8 softmax warps
 
 // Loads rows [row0, row0+64) of every 64-column chunk of head h into rows
 // [64*half, 64*half+64) of a 128-row swizzled tile.
@@ -98,7 +230,7 @@ __device__ __forceinline__ void load_half(const CUtensorMap* tm, uint64_t* bar, 
   for (int c = 0; c < D / 64; ++c) tma_load_2d(tm, bar, tile + c * 16384 + half * 8192, h * D + c * 64, row0);
 }
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(384, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -106,14 +238,19 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::OFF_BAR);
-  static_assert(sizeof(FwdBars) <= 256, "barrier block");
+  static_assert(sizeof(FwdBars) <= 512, "barrier block");
   const int warp = warp_id(), lane = lane_id();
-  const int t0 = p.prog_start[blockIdx.x], t1 = p.prog_start[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->sched_full[s], 1);
+      mbar_init(&bars->sched_empty[s], kFwdSchedConsumers);
+    }
+    mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
+      mbar_init(&bars->qk_rot[s], 4);
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -140,15 +277,14 @@ __global__ void __launch_bounds__(384, 1)
   const Abort ab{&bars->abort_flag, p.err};
 
   if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- loader
-    // In the order the tensor core consumes them: QK(0), then QK(i+1), V(i).
-    // Consecutive tiles share their pair of blocks across the heads, so the
-    // block search runs once per pair, not per load.
-    const int n = t1 - t0;
+    // ---------------------------------------------------------------- loader and scheduler
+    // In the order the tensor core consumes them: QK(0), then QK(i+1), V(i),
+    // across chunk boundaries.  Consecutive tiles share their pair of blocks
+    // across the heads, so the block search runs once per pair, not per load.
     int cached_pair = -1;
     Blk ca{0, 0}, cb{0, 0};
-    auto rows = [&](int i, Blk& a, Blk& b, int& h) {
-      const int t = t0 + i, pair = t / p.H;
+    auto rows = [&](int t, Blk& a, Blk& b, int& h) {
+      const int pair = t / p.H;
       h = t % p.H;
       if (pair != cached_pair) {
         cached_pair = pair;
@@ -159,12 +295,12 @@ __global__ void __launch_bounds__(384, 1)
       a = ca;
       b = cb;
     };
-    auto load_qk = [&](int i) -> bool {
+    auto load_qk = [&](int i, int t) -> bool {
       const int st = i % C::NQK;
       if (!mbar_wait(&bars->qk_empty[st], ((i / C::NQK) & 1) ^ 1, ab)) return false;
       Blk a, b;
       int h;
-      rows(i, a, b, h);
+      rows(t, a, b, h);
       uint8_t* base = smem + st * 2 * C::TILE;
       mbar_expect_tx(&bars->qk_full[st], 2 * C::TILE);
       load_half<D>(&tm_q, &bars->qk_full[st], base, 0, h, a.row0);
@@ -173,23 +309,33 @@ __global__ void __launch_bounds__(384, 1)
       load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 1, h, b.row0);
       return true;
     };
-    auto load_v = [&](int i) -> bool {
+    auto load_v = [&](int i, int t) -> bool {
       const int st = i % C::NV;
       if (!mbar_wait(&bars->v_empty[st], ((i / C::NV) & 1) ^ 1, ab)) return false;
       Blk a, b;
       int h;
-      rows(i, a, b, h);
+      rows(t, a, b, h);
       uint8_t* base = smem + C::OFF_V + st * C::TILE;
       mbar_expect_tx(&bars->v_full[st], C::TILE);
       load_half<D>(&tm_v, &bars->v_full[st], base, 0, h, a.row0);
       load_half<D>(&tm_v, &bars->v_full[st], base, 1, h, b.row0);
       return true;
     };
-    if (n > 0 && load_qk(0)) {
-      for (int i = 0; i < n; ++i) {
-        if (i + 1 < n && !load_qk(i + 1)) break;
-        if (!load_v(i)) break;
+    int cur = p.use_clc ? static_cast<int>(blockIdx.x) : 0;
+    int i = 0, prev_t = -1;  // tiles loaded so far; the tile whose V is still to load
+    for (uint32_t sit = 0;; ++sit) {
+      if (!publish(bars, sit, cur, p, ab) || cur < 0) break;
+      int tb, te;
+      chunk_range(p, cur, &tb, &te);
+      bool ok = true;
+      for (int t = tb; t < te && ok; ++t, ++i) {
+        ok = load_qk(i, t) && (prev_t < 0 || load_v(i - 1, prev_t));
+        prev_t = t;
       }
+      if (!ok) break;
+      cur = next_entry(bars, sit, p, ab);
+      if (cur == -2) break;
+      if (cur < 0 && prev_t >= 0) load_v(i - 1, prev_t);  // the last tile's V
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -216,10 +362,12 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(&bars->o_full[b]);
       mma_commit(&bars->v_empty[st]);
     };
-    const int n = t1 - t0;
-    for (int i = 0; i <= n; ++i) {
-      if (i < n) {  // S of tile i, once its operands landed and its TMEM buffer is free
-        if (!mbar_wait(&bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
+    TileCursor cur;
+    for (int i = 0;; ++i) {
+      const int t = next_tile(cur, bars, p, ab, false);
+      if (t == -2) break;
+      if (t >= 0) {  // S of tile i, once its operands landed (and are rotated) and its TMEM buffer is free
+        if (!mbar_wait(ROPE ? &bars->qk_rot[i % C::NQK] : &bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
         if (!mbar_wait(&bars->t_free[i & 1], ((i >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after();
         issue_s(i);
@@ -231,6 +379,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         issue_pv(j);
       }
+      if (t < 0) break;
     }
     mma_commit(&bars->drain);
     const uint64_t tw = global_timer_ns();
@@ -245,11 +394,23 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_addr + 256 * b;
     const uint32_t tO = tS + 128;
     const float sl2 = p.scale_log2;
-    for (int i = b; i < t1 - t0; i += 2) {
-      const int t = t0 + i;
+    TileCursor cur;
+    for (int i = 0;; ++i) {
+      const int t = next_tile(cur, bars, p, ab, true);
+      if (t == -2) goto done;
+      if (t < 0) break;
+      if ((i & 1) != b) continue;  // the other warpgroup's tile
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
       const int rr = r & 63;
+      if constexpr (ROPE) {  // this warpgroup rotates its own tile's Q and K (slot i % 2 == b)
+        const int st = i % C::NQK;
+        if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) goto done;
+        rope_tile<D>(p, smem + st * 2 * C::TILE, smem + st * 2 * C::TILE + C::TILE, r, blk);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
+      }
       if (!mbar_wait(&bars->s_full[b], (i >> 1) & 1, ab)) goto done;
       tc_fence_after();
       uint32_t sr[64];
@@ -329,17 +490,22 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_V + TILE;
   static constexpr int OFF_PDS = OFF_DO + TILE;     // P, then dS: [128 q][128 keys] bf16
   static constexpr int OFF_BAR = OFF_PDS + 32768;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
 };
 
 struct BwdBars {
+  int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[2], qk_empty[2], vdo_full, vdo_empty;
+  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
   uint64_t drain;
+  uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
+  int sched_unit[4];
   uint32_t tmem_base;
   int abort_flag;
 };
+constexpr int kBwdSchedConsumers = 5;  // the MMA thread and the 4 softmax / dS / epilogue warps
 
 // Row q of a [128][128] bf16 tile stored as two swizzled 64-column boxes:
 // 16-byte piece j (columns 8j..8j+7) of box c.
@@ -349,7 +515,7 @@ __device__ __forceinline__ void st_row_piece(uint8_t* tile, int q, int c, int j,
                : "memory");
 }
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(256, 1)
     block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -359,15 +525,21 @@ __global__ void __launch_bounds__(256, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
+  static_assert(sizeof(BwdBars) <= 512, "barrier block");
   const int warp = warp_id(), lane = lane_id();
-  const int t0 = p.prog_start[blockIdx.x], t1 = p.prog_start[blockIdx.x + 1];
   // TMEM columns: S (then dQ) [0,128), dP (then dK) [128,256), dV [256, 256+D)
   constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->sched_full[s], 1);
+      mbar_init(&bars->sched_empty[s], kBwdSchedConsumers);
+    }
+    mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
+      mbar_init(&bars->qk_rot[s], 4);
     }
     mbar_init(&bars->vdo_full, 1);
     mbar_init(&bars->vdo_empty, 1);
@@ -395,15 +567,14 @@ __global__ void __launch_bounds__(256, 1)
   const Abort ab{&bars->abort_flag, p.err};
 
   if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- loader
-    // Order: QK(0), VdO(0), then QK(i+1) (its slot was freed by tile i-1) and
-    // VdO(i+1) (free once tile i's dV has run).  The block search runs once per
-    // pair of blocks, shared by the pair's heads.
-    const int n = t1 - t0;
+    // ---------------------------------------------------------------- loader and scheduler
+    // Per tile, in order: QK(i) (its slot was freed by tile i-2) and VdO(i)
+    // (free once tile i-1's dV has run), across chunk boundaries.  The block
+    // search runs once per pair of blocks, shared by the pair's heads.
     int cached_pair = -1;
     Blk ca{0, 0}, cb{0, 0};
-    auto rows = [&](int i, Blk& a, Blk& b, int& h) {
-      const int t = t0 + i, pair = t / p.H;
+    auto rows = [&](int t, Blk& a, Blk& b, int& h) {
+      const int pair = t / p.H;
       h = t % p.H;
       if (pair != cached_pair) {
         cached_pair = pair;
@@ -414,12 +585,12 @@ __global__ void __launch_bounds__(256, 1)
       a = ca;
       b = cb;
     };
-    auto load_qk = [&](int i) -> bool {
+    auto load_qk = [&](int i, int t) -> bool {
       const int st = i % C::NQK;
       if (!mbar_wait(&bars->qk_empty[st], ((i / C::NQK) & 1) ^ 1, ab)) return false;
       Blk a, b;
       int h;
-      rows(i, a, b, h);
+      rows(t, a, b, h);
       uint8_t* base = smem + st * 2 * C::TILE;
       mbar_expect_tx(&bars->qk_full[st], 2 * C::TILE);
       load_half<D>(&tm_q, &bars->qk_full[st], base, 0, h, a.row0);
@@ -428,11 +599,11 @@ __global__ void __launch_bounds__(256, 1)
       load_half<D>(&tm_k, &bars->qk_full[st], base + C::TILE, 1, h, b.row0);
       return true;
     };
-    auto load_vdo = [&](int i) -> bool {
+    auto load_vdo = [&](int i, int t) -> bool {
       if (!mbar_wait(&bars->vdo_empty, (i & 1) ^ 1, ab)) return false;
       Blk a, b;
       int h;
-      rows(i, a, b, h);
+      rows(t, a, b, h);
       mbar_expect_tx(&bars->vdo_full, 2 * C::TILE);
       load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 0, h, a.row0);
       load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 1, h, b.row0);
@@ -440,9 +611,17 @@ __global__ void __launch_bounds__(256, 1)
       load_half<D>(&tm_do, &bars->vdo_full, smem + C::OFF_DO, 1, h, b.row0);
       return true;
     };
-    if (n > 0 && load_qk(0) && load_vdo(0)) {
-      for (int i = 0; i + 1 < n; ++i)
-        if (!load_qk(i + 1) || !load_vdo(i + 1)) break;
+    int cur = p.use_clc ? static_cast<int>(blockIdx.x) : 0;
+    int i = 0;
+    for (uint32_t sit = 0;; ++sit) {
+      if (!publish(bars, sit, cur, p, ab) || cur < 0) break;
+      int tb, te;
+      chunk_range(p, cur, &tb, &te);
+      bool ok = true;
+      for (int t = tb; t < te && ok; ++t, ++i) ok = load_qk(i, t) && load_vdo(i, t);
+      if (!ok) break;
+      cur = next_entry(bars, sit, p, ab);
+      if (cur == -2) break;
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -451,10 +630,12 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t id_q = idesc_bf16(128, D, 0, 1);     // dQ = dS K
     const uint32_t sP = smem_u32(smem + C::OFF_PDS), sDS = sP;
     const uint32_t v = smem_u32(smem + C::OFF_V), dO = smem_u32(smem + C::OFF_DO);
-    for (int i = 0; i < t1 - t0; ++i) {
+    TileCursor cur;
+    for (int i = 0;; ++i) {
+      if (next_tile(cur, bars, p, ab, false) < 0) break;
       const int st = i % C::NQK;
       const uint32_t q = smem_u32(smem + st * 2 * C::TILE), k = q + C::TILE;
-      if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
+      if (!mbar_wait(ROPE ? &bars->qk_rot[st] : &bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
       if (!mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
       tc_fence_after();
 #pragma unroll
@@ -510,10 +691,28 @@ __global__ void __launch_bounds__(256, 1)
     const float sl2 = p.scale_log2;
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
     uint32_t stg_full_ph = 0, stg_free_ph = 0;
-    for (int i = 0; i < t1 - t0; ++i) {
-      const int t = t0 + i;
+    TileCursor cur;
+    int rot_ahead = -1;  // rotary: the tile whose Q and K were rotated while the previous one finished
+    // rotary: rotate the Q and K rows of tile counter j (tile id tj) in their slot
+    auto rotate = [&](int j, int tj) -> bool {
+      const int st = j % C::NQK;
+      if (!mbar_wait(&bars->qk_full[st], (j / C::NQK) & 1, ab)) return false;
+      rope_tile<D>(p, smem + st * 2 * C::TILE, smem + st * 2 * C::TILE + C::TILE, r,
+                   locate(p, 2 * (tj / p.H) + half));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
+      return true;
+    };
+    for (int i = 0;; ++i) {
+      const int t = next_tile(cur, bars, p, ab, true);
+      if (t == -2) goto done;
+      if (t < 0) break;
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
+      if constexpr (ROPE) {
+        if (rot_ahead != i && !rotate(i, t)) goto done;
+      }
       if (!mbar_wait(&bars->s_full, i & 1, ab)) goto done;
       tc_fence_after();
       float pr[64];
@@ -579,6 +778,14 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full);
+      if constexpr (ROPE) {
+        // while the tensor core computes this tile's dK and dQ, rotate the next
+        // tile's Q and K if it is already known (not at the end of a chunk)
+        if (cur.t < cur.te) {
+          if (!rotate(i + 1, cur.t)) goto done;
+          rot_ahead = i + 1;
+        }
+      }
       if constexpr (D == 128) {
         // epilogue: row r is query r for dQ and key r for dK, dV (same block, same token).
         // Each result is staged as bf16 rows in the P/dS buffer (free once dK and dQ
@@ -607,22 +814,61 @@ __global__ void __launch_bounds__(256, 1)
               if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
               stg_free_ph ^= 1;
             }
-  #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_addr + col + c, v);
-              tmem_wait_ld();
-              reg_fence<32>(v);
+            // columns c..c+31 of the result row, as fp32: staged (pieces (c%64)/8 ..
+            // (c%64)/8+3 of the 64-column box c/64) and, for a short block, stored
+            auto put = [&](int c, const float* f) {
               uint32_t w[16];
   #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-              // columns c..c+31: pieces (c%64)/8 .. (c%64)/8+3 of the 64-column box c/64
+              for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
   #pragma unroll
               for (int e = 0; e < 4; ++e) st_row_piece(sP, r, c / 64, (c % 64) / 8 + e, w + 4 * e);
               if (valid && !full_half) {
   #pragma unroll
                 for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              }
+            };
+            if (ROPE && which < 2) {
+              // dQ and dK of the rotated rows go back through the transposed rotation
+  #pragma unroll 1
+              for (int c = 0; c < D / 2; c += 32) {
+                uint32_t v1[32], v2[32];
+                tmem_ld32(tmem + lane_addr + col + c, v1);
+                tmem_ld32(tmem + lane_addr + col + c + D / 2, v2);
+                tmem_wait_ld();
+                reg_fence<32>(v1);
+                reg_fence<32>(v2);
+                float f1[32], f2[32];
+  #pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  f1[e] = __uint_as_float(v1[e]) * mul;
+                  f2[e] = __uint_as_float(v2[e]) * mul;
+                }
+                if (valid) {
+                  const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2) + c;
+  #pragma unroll
+                  for (int e = 0; e < 32; e += 4) {
+                    const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
+                    const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
+                    rope_back(f1[e], f2[e], cs.x, sn.x);
+                    rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
+                    rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
+                    rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
+                  }
+                }
+                put(c, f1);
+                put(c + D / 2, f2);
+              }
+            } else {
+  #pragma unroll 1
+              for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + col + c, v);
+                tmem_wait_ld();
+                reg_fence<32>(v);
+                float f[32];
+  #pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+                put(c, f);
               }
             }
             if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
@@ -667,20 +913,56 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
             const float mul = which == 2 ? 1.0f : p.scale;
             __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
-  #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_addr + col + c, v);
-              tmem_wait_ld();
-              reg_fence<32>(v);
+            // columns c..c+31 of the result row, as fp32, stored
+            auto put = [&](int c, const float* f) {
+              if (!valid) return;
               uint32_t w[16];
   #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-              if (valid) {
+              for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
   #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              for (int e = 0; e < 4; ++e)
+                st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            };
+            if (ROPE && which < 2) {
+              // dQ and dK of the rotated rows go back through the transposed
+              // rotation: columns c and c + 32 form the pairs
+              uint32_t v1[32], v2[32];
+              tmem_ld32(tmem + lane_addr + col, v1);
+              tmem_ld32(tmem + lane_addr + col + 32, v2);
+              tmem_wait_ld();
+              reg_fence<32>(v1);
+              reg_fence<32>(v2);
+              float f1[32], f2[32];
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                f1[e] = __uint_as_float(v1[e]) * mul;
+                f2[e] = __uint_as_float(v2[e]) * mul;
+              }
+              if (valid) {
+                const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
+  #pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                  const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
+                  const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
+                  rope_back(f1[e], f2[e], cs.x, sn.x);
+                  rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
+                  rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
+                  rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
+                }
+              }
+              put(0, f1);
+              put(32, f2);
+            } else {
+  #pragma unroll 1
+              for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + col + c, v);
+                tmem_wait_ld();
+                reg_fence<32>(v);
+                float f[32];
+  #pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+                put(c, f);
               }
             }
           }
@@ -701,7 +983,7 @@ done:
   }
 }
 
-template <int D>
+template <int D, bool ROPE>
 int launch_fwd_impl(const BlockArgs& a) {
   using C = FwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -713,7 +995,7 @@ int launch_fwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_fwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -730,12 +1012,18 @@ int launch_fwd_impl(const BlockArgs& a) {
   p.n_blocks = a.n_blocks;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.use_clc = a.use_clc;
+  p.chunk = a.chunk;
+  p.n_tiles = a.n_tiles;
+  p.n_chunks = a.n_chunks;
+  p.rope_cos = a.rope_cos;
+  p.rope_sin = a.rope_sin;
   ProfileScope prof(kKindBlockFwd, a.stream);
-  block_fwd_kernel<D><<<a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
+  block_fwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool ROPE>
 int launch_bwd_impl(const BlockArgs& a) {
   using C = BwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -751,7 +1039,7 @@ int launch_bwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_bwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -770,18 +1058,29 @@ int launch_bwd_impl(const BlockArgs& a) {
   p.n_blocks = a.n_blocks;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.use_clc = a.use_clc;
+  p.chunk = a.chunk;
+  p.n_tiles = a.n_tiles;
+  p.n_chunks = a.n_chunks;
+  p.rope_cos = a.rope_cos;
+  p.rope_sin = a.rope_sin;
   ProfileScope prof(kKindBlockBwd, a.stream);
-  block_bwd_kernel<D><<<a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+  block_bwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq,
+                                                                                             tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
 }  // namespace blk
 
 int launch_block_fwd(const BlockArgs& a) {
-  return a.D == 128 ? blk::launch_fwd_impl<128>(a) : blk::launch_fwd_impl<64>(a);
+  if (a.rope_cos != nullptr)
+    return a.D == 128 ? blk::launch_fwd_impl<128, true>(a) : blk::launch_fwd_impl<64, true>(a);
+  return a.D == 128 ? blk::launch_fwd_impl<128, false>(a) : blk::launch_fwd_impl<64, false>(a);
 }
 int launch_block_bwd(const BlockArgs& a) {
-  return a.D == 128 ? blk::launch_bwd_impl<128>(a) : blk::launch_bwd_impl<64>(a);
+  if (a.rope_cos != nullptr)
+    return a.D == 128 ? blk::launch_bwd_impl<128, true>(a) : blk::launch_bwd_impl<64, true>(a);
+  return a.D == 128 ? blk::launch_bwd_impl<128, false>(a) : blk::launch_bwd_impl<64, false>(a);
 }
 
 }  // namespace jfa
