@@ -84,7 +84,14 @@ typedef enum {
   JFA_ERR_TOO_LARGE = 8             /* jfa_fwd_noalloc: the plan exceeds its static scratch */
 } jfa_status;
 
-typedef enum { JFA_OP_FWD = 0, JFA_OP_BWD = 1, JFA_OP_BLOCK_FWD = 2, JFA_OP_BLOCK_BWD = 3 } jfa_op;
+typedef enum {
+  JFA_OP_FWD = 0,
+  JFA_OP_BWD = 1,
+  JFA_OP_BLOCK_FWD = 2,
+  JFA_OP_BLOCK_BWD = 3,
+  JFA_OP_TOPK_SELECT = 4,  /* jfa_topk_select (an upper bound with grouped K/V heads) */
+  JFA_OP_FWD_TOPK = 5      /* jfa_fwd_topk */
+} jfa_op;
 
 /*
  * jfa_fwd -- jagged flash-attention forward [C "architecture"; R "Framework";
@@ -122,6 +129,66 @@ int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const vo
             int broadcast_q, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * jfa_fwd_window, jfa_bwd_window -- jfa_fwd / jfa_bwd for self-attention under
+ * a sliding window [C "performance and feature scope" and R "MXFP8 and
+ * sparsity" name windows among the variants the kernels keep; the pages do not
+ * define them, and this two-sided local window is this library's reading]:
+ * query i of a sequence sees the keys j of its sequence with
+ *   i - window_left <= j <= i + window_right,
+ * where -1 leaves a side open.  (-1, -1) is jfa_fwd without causal masking,
+ * (-1, 0) causal attention, (W-1, 0) causal attention over the last W keys.
+ * Every query sees at least itself, so no output row is empty.  Each query
+ * tile visits only the K/V blocks its rows can see (forward), and each key
+ * block only the query tiles that see it (backward); blocks that straddle a
+ * window edge are masked element-wise.  Bounds below -1 return
+ * JFA_ERR_INVALID_ARG.  Other arguments, the workspace (jfa_workspace_size with
+ * causal = 0) and lse as in jfa_fwd / jfa_bwd; the backward takes the lse of
+ * the forward with the same window.
+ */
+int jfa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+                   const int32_t* offsets_host, int batch, int max_len, int num_heads, int num_kv_heads, int head_dim,
+                   float scale, int window_left, int window_right, void* workspace, size_t workspace_bytes,
+                   void* stream);
+int jfa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                   int max_len, int num_heads, int num_kv_heads, int head_dim, float scale, int window_left,
+                   int window_right, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Two-stage block-sparse forward [R "MXFP8 and sparsity": a cheap kernel
+ * averages blocks of Q and K and picks the top-k most relevant key blocks,
+ * then the attention kernel attends over those blocks only].  The pages give
+ * neither block sizes, score nor tie rule; this library's reading: query
+ * blocks of 256 rows (the forward's unit), key blocks of 128 keys, each
+ * block's mean over the rows it really has, score = mean query . mean key
+ * (key/value head h / (num_heads / num_kv_heads)), the topk highest scores,
+ * ties to the lower block index, and exact softmax attention over every key of
+ * the chosen blocks.  Self-attention or broadcast-Q, no causal mask.
+ *
+ * jfa_topk_rows: the number of query blocks (rows of the selection): for
+ *   each sequence with keys, num_heads * ceil(rows / 256), rows = its length or
+ *   nq_broadcast.  Returns the count or -jfa_status.
+ * jfa_topk_select: first stage.  selection is device int32 [rows, topk], rows
+ *   ordered by sequence, query head, query block; each row holds its chosen key
+ *   block indices (0-based, within the sequence) in ascending order, then -1
+ *   where the sequence has fewer than topk blocks.  Workspace:
+ *   jfa_workspace_size(JFA_OP_TOPK_SELECT, ...).  Sequences of more than
+ *   393,216 keys return JFA_ERR_UNSUPPORTED.
+ * jfa_fwd_topk: second stage, o and lse as jfa_fwd, with the selection of
+ *   jfa_topk_select (or any selection of ascending, in-range block indices,
+ *   min(topk, blocks) of them per row).  Workspace:
+ *   jfa_workspace_size(JFA_OP_FWD_TOPK, ...).
+ */
+int jfa_topk_rows(const int32_t* offsets_host, int batch, int nq_broadcast, int num_heads, int broadcast_q);
+int jfa_topk_select(const void* q, const void* k, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                    int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, int topk,
+                    int broadcast_q, int32_t* selection, void* workspace, size_t workspace_bytes, void* stream);
+int jfa_fwd_topk(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* selection,
+                 int topk, const int32_t* offsets_dev, const int32_t* offsets_host, int batch, int max_len,
+                 int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale, int broadcast_q,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * block_attn_fwd -- fixed 64-token block-diagonal self-attention [B 1, 2.1, 3].
  * Each sequence is cut into blocks of 64 tokens (the last one may be shorter)
  * and every block attends only within itself: one score GEMM and one PV GEMM per
@@ -143,6 +210,33 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
                    void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
                    int max_len, int num_heads, int head_dim, float scale, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/*
+ * block_attn_fwd_rope, block_attn_bwd_rope -- block_attn_fwd / block_attn_bwd
+ * with a rotary position embedding of q and k fused into the kernels [B
+ * introduction: "with rotary fused"].  The pages do not state the rotary
+ * convention; this library's reading is the rotate-half form: the position of
+ * a row is its index inside its sequence, and for i < head_dim/2 the pair
+ * (x_i, x_{i+head_dim/2}) of a q or k row at position p turns by the angle
+ * a(p, i):
+ *   (x_i, x_{i+D/2}) -> (x_i cos a - x_{i+D/2} sin a, x_{i+D/2} cos a + x_i sin a).
+ * rope_cos and rope_sin are fp32 device tables [rope_rows, head_dim/2] (row p,
+ * column i = cos / sin of a(p, i); any angles, e.g. p * base^(-2i/D)), 16-byte
+ * aligned, rope_rows >= max_len.  The forward attends with the rotated q and k;
+ * the backward recomputes them and returns dq and dk with respect to the
+ * unrotated q and k (the transposed rotation is applied before they are
+ * stored).  q, k, dq, dk stay unrotated in memory.  Errors as block_attn_*,
+ * plus JFA_ERR_INVALID_ARG for missing, misaligned or too short tables.
+ */
+int block_attn_fwd_rope(const void* q, const void* k, const void* v, void* o, const float* rope_cos,
+                        const float* rope_sin, int rope_rows, const int32_t* offsets_dev,
+                        const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim,
+                        float scale, void* workspace, size_t workspace_bytes, void* stream);
+int block_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,
+                        void* dk, void* dv, const float* rope_cos, const float* rope_sin, int rope_rows,
+                        const int32_t* offsets_dev, const int32_t* offsets_host, int batch, int max_len,
+                        int num_heads, int head_dim, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /*
  * jfa_fwd_noalloc -- jfa_fwd for callers that cannot allocate device memory.
@@ -222,6 +316,14 @@ int jfa_plan_fwd(const int32_t* offsets_host, int batch, int num_heads, int nq_b
 int jfa_plan_bwd(const int32_t* offsets_host, int batch, int num_heads, int nq_broadcast, int causal, int n_cta,
                  int32_t* units, int32_t* cta_start);
 /*
+ *   jfa_plan_window: the same planners for self-attention under a window (see
+ *     jfa_fwd_window): which = 0 forward (as jfa_plan_fwd), 1 backward (as
+ *     jfa_plan_bwd).  A unit's cost counts the blocks or tiles it visits
+ *     inside the window.
+ */
+int jfa_plan_window(int which, const int32_t* offsets_host, int batch, int num_heads, int window_left,
+                    int window_right, int n_cta, int32_t* units, int32_t* cta_start);
+/*
  *   block_plan: block_per_batch [batch+1] = exclusive prefix sum of ceil(L/64);
  *     tiles are pairs of consecutive global blocks per head (id = pair*H + h);
  *     prog_start [P+1] with P = min(n_sm, tiles) from closed-form divmod.
@@ -258,18 +360,31 @@ int jfa_set_bwd_schedule(int mode);
 int jfa_get_bwd_schedule(void);
 
 /*
+ * The same two modes for the block-diagonal kernels [B 5; R "Tile balancing and
+ * Cluster Launch Control"]: 0 closed-form static ranges (programs get balanced
+ * contiguous ranges of (block pair, head) tiles, one CTA per SM); 1 Cluster
+ * Launch Control (one CTA per chunk of 16 consecutive tiles; a CTA that
+ * finishes a chunk takes over the chunk of a CTA not yet launched).  Both
+ * modes give bit-identical results (every tile owns its outputs).  Initially
+ * JFA_SCHED_BLOCK ("static" or "clc") if set, else Cluster Launch Control;
+ * jfa_set_block_schedule() changes it for subsequent calls (process-wide).
+ */
+int jfa_set_block_schedule(int mode);
+int jfa_get_block_schedule(void);
+
+/*
  * Optional kernel timing (no counterpart on the pages; measurement support).
  * jfa_profile_enable(1) starts counting every library kernel launch and
  * bracketing it with CUDA events on its stream (and forgets earlier records);
  * jfa_profile_enable(0) stops it.  jfa_profile_select(mask) limits the events
  * to the kinds whose bit is set in mask (launches of the other kinds are still
- * counted; the initial mask selects every kind; a mask outside [0, 2^7)
+ * counted; the initial mask selects every kind; a mask outside [0, 2^8)
  * returns JFA_ERR_INVALID_ARG), so a measurement can time one kernel without
  * adding events around the rest.  jfa_profile_read(kind, &ms, &n) synchronises
  * on the recorded events and returns the summed device time (0 for an
  * unselected kind) and the launch count of one kernel kind: 0 forward,
  * 1 backward prepass (Di), 2 backward main, 3 dQ convert, 4 block forward,
- * 5 block backward, 6 empty-sequence fill.
+ * 5 block backward, 6 empty-sequence fill, 7 top-k selection.
  */
 /*
  * Failure-path self-test (no counterpart on the pages; failure detection).

@@ -41,7 +41,35 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-def plan_fwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
+def _visible(i, L, window):
+    """Keys [lo, hi) that query i sees under window (left, right); None = open."""
+    left, right = window
+    lo = 0 if left is None else max(0, i - left)
+    hi = L if right is None else min(L, i + right + 1)
+    return lo, hi
+
+
+def _window_fwd_cost(m, rows, L, window):
+    # blocks from the first one any row of the unit sees to the last one
+    first = min(_visible(r, L, window)[0] // KV_BLOCK for r in range(FWD_ROWS * m, min(FWD_ROWS * (m + 1), rows)))
+    last = max((_visible(r, L, window)[1] - 1) // KV_BLOCK
+               for r in range(FWD_ROWS * m, min(FWD_ROWS * (m + 1), rows)))
+    return last - first + 1
+
+
+def _window_bwd_cost(n, rows, L, window):
+    # query tiles from the first one holding a row that sees some key of block n
+    # to the last one; key k is seen by rows k-right .. k+left
+    left, right = window
+    keys = range(KV_BLOCK * n, min(KV_BLOCK * (n + 1), L))
+    first = min((0 if right is None else max(0, k - right)) // KV_BLOCK for k in keys)
+    last = max(((rows if left is None else min(rows, k + left + 1)) - 1) // KV_BLOCK for k in keys)
+    return last - first + 1
+
+
+def plan_fwd(offsets, num_heads, n_cta, *, causal=False, nq=0, window=None):
+    """``window`` = (left, right), self-attention only: the unit's cost counts
+    the K/V blocks its rows see inside the window."""
     B = len(offsets) - 1
     units = []
     for b in range(B):
@@ -51,7 +79,9 @@ def plan_fwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
         rows = nq if nq > 0 else L
         for h in range(num_heads):
             for m in range(_cdiv(rows, FWD_ROWS)):
-                if causal:
+                if window is not None:
+                    cost = _window_fwd_cost(m, rows, L, window)
+                elif causal:
                     last_row = min(FWD_ROWS * (m + 1), rows)
                     cost = _cdiv(min(last_row, L), KV_BLOCK)
                 else:
@@ -66,7 +96,7 @@ def plan_fwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
     return _flatten(per_cta)
 
 
-def plan_bwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
+def plan_bwd(offsets, num_heads, n_cta, *, causal=False, nq=0, window=None):
     B = len(offsets) - 1
     units = []
     for b in range(B):
@@ -74,7 +104,9 @@ def plan_bwd(offsets, num_heads, n_cta, *, causal=False, nq=0):
         rows = nq if nq > 0 else L
         for h in range(num_heads):
             for n in range(_cdiv(L, KV_BLOCK)):
-                if causal:
+                if window is not None:
+                    cost = _window_bwd_cost(n, rows, L, window)
+                elif causal:
                     cost = _cdiv(rows, FWD_ROWS // 2) - (KV_BLOCK * n) // (FWD_ROWS // 2)
                 else:
                     cost = _cdiv(rows, FWD_ROWS // 2)

@@ -57,13 +57,14 @@ def gpu_inputs(w, device="cuda"):
     return [t.to(device) for t in (q, k, v, do)], offs, (q, k, v, do)
 
 
-def check_fwd(w, sel=None, nthreads=0):
-    """Runs jfa_fwd and compares O and LSE with the oracle.  Returns a dict of errors."""
+def check_fwd(w, sel=None, nthreads=0, window=None):
+    """Runs jfa_fwd (jfa_fwd_window if ``window`` is given) and compares O and
+    LSE with the oracle.  Returns a dict of errors."""
     (q, k, v, do), offs, cpu = gpu_inputs(w)
-    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale)
+    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale, window=window)
     torch.cuda.synchronize()
     o_ref, lse_ref, _ = oracle.attn_fwd(to64(cpu[0]), to64(cpu[1]), to64(cpu[2]), w.offsets, scale=w.scale,
-                                        causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads)
+                                        causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads, window=window)
     o_g, lse_g = to64(o), to64(lse)
     if sel is not None:
         m = rows_of(w.offsets, sel, w.num_heads, w.nq)
@@ -97,15 +98,16 @@ def kv_rows_of(offsets, sel, H):
     return mask
 
 
-def check_bwd(w, sel=None, nthreads=0):
-    """Runs jfa_fwd then jfa_bwd on the GPU and compares dQ, dK, dV with the oracle."""
+def check_bwd(w, sel=None, nthreads=0, window=None):
+    """Runs jfa_fwd then jfa_bwd on the GPU (the window entry points if ``window``
+    is given) and compares dQ, dK, dV with the oracle."""
     (q, k, v, do), offs, cpu = gpu_inputs(w)
-    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale)
+    o, lse = V.jfa_fwd(q, k, v, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq, scale=w.scale, window=window)
     dq, dk, dv = V.jfa_bwd(q, k, v, o, do, lse, offs, w.offsets, causal=w.causal, nq_broadcast=w.nq,
-                           scale=w.scale)
+                           scale=w.scale, window=window)
     torch.cuda.synchronize()
     ref = oracle.attn_bwd(to64(cpu[0]), to64(cpu[1]), to64(cpu[2]), to64(cpu[3]), w.offsets, scale=w.scale,
-                          causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads)
+                          causal=w.causal, nq=w.nq, sel=sel, nthreads=nthreads, window=window)
     got = [to64(dq), to64(dk), to64(dv)]
     want = list(ref[:3])
     if sel is not None:

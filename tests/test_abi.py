@@ -67,6 +67,29 @@ def test_fwd_argument_errors(kwargs, status):
     assert _fwd([0, 17, 40], **kwargs) == status
 
 
+@pytest.mark.parametrize("left,right", [(-2, 0), (0, -2), (-5, -5)])
+@pytest.mark.parametrize("bwd", [False, True])
+def test_window_bounds_below_minus_one_rejected(left, right, bwd):
+    # -1 leaves a side open; anything lower is an argument error, found before
+    # any device work
+    lib = J.load()
+    h = np.array([0, 17, 40], dtype=np.int32)
+    hp = h.ctypes.data_as(ctypes.c_void_p)
+    if bwd:
+        st = lib.jfa_bwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, hp, 2, 23, 2, 2, 128,
+                                0.1, left, right, FAKE, 1 << 20, None)
+    else:
+        st = lib.jfa_fwd_window(FAKE, FAKE, FAKE, FAKE, None, FAKE, hp, 2, 23, 2, 2, 128, 0.1, left, right, FAKE,
+                                1 << 20, None)
+    assert st == 1
+
+
+def test_window_plan_rejects_bad_bounds():
+    h = np.array([0, 17, 40], dtype=np.int32)
+    assert J.load().jfa_plan_window(0, h.ctypes.data_as(ctypes.c_void_p), 2, 2, -2, 0, 4, None, None) == -1
+    assert J.load().jfa_plan_window(2, h.ctypes.data_as(ctypes.c_void_p), 2, 2, 0, 0, 4, None, None) == -1
+
+
 def test_broadcast_row_count_overflow_rejected():
     # batch * nq broadcast output rows past the 32-bit row index range: rejected
     # before any device work (the empty sequences need no data)
@@ -142,7 +165,7 @@ def test_block_bwd_buffer_errors_before_device_work(kwargs):
     assert _block(True, **kwargs) == 1
 
 
-@pytest.mark.parametrize("which", ["schedule", "bwd_schedule"])
+@pytest.mark.parametrize("which", ["schedule", "bwd_schedule", "block_schedule"])
 def test_schedule_switches(which):
     # host-side state only: no device work
     lib = J.load()
@@ -202,3 +225,12 @@ def test_binding_rejects_host_tensors(by_keyword):
             V.jfa_fwd(q=q, k=q, v=q, offsets=offs, offsets_host=[0, 4])
         else:
             V.jfa_fwd(q, q, q, offs, [0, 4])
+
+
+def test_topk_rows_count_query_blocks():
+    # one row per (sequence with keys, query head, 256-row query block)
+    import oracle
+    from variable_length_attention_gb300 import workloads as W
+    for w in (W.custom([1, 63, 128, 129, 255, 256, 257, 513, 1000], 2, 64), W.custom([300, 0, 900, 129], 3, 128, nq=300),
+              W.jagged()):
+        assert V.jfa_topk_rows(w.offsets, w.num_heads, w.nq) == len(oracle._topk_units(w.offsets, w.num_heads, w.nq))

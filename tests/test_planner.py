@@ -43,6 +43,29 @@ def test_bwd_plan_bit_exact(name, w, n_cta):
     assert u.tolist() == fu and s.tolist() == fs
 
 
+WINDOW_CASES = [(w, win) for w in (W.tiny(), W.jagged(False), CASES[5][1], CASES[6][1])
+                for win in ((0, 0), (127, 0), (255, 0), (300, 40), (None, 129), (1000, None), (None, 0))]
+
+
+@pytest.mark.parametrize("w,window", WINDOW_CASES, ids=[f"{w.name}-{win}" for w, win in WINDOW_CASES])
+def test_window_plans_bit_exact(w, window):
+    # under a window the costs count the blocks / tiles the unit's rows or keys
+    # see; the entries and their order follow the same rules as without one
+    if w.nq:
+        pytest.skip("windows are for self-attention")
+    offs = w.offsets.tolist()
+    for which, n_cta in ((0, 152), (0, 7), (1, 152), (1, 1)):
+        u, s = V.jfa_plan_window(which, offs, w.num_heads, n_cta, window)
+        fn = P.plan_fwd if which == 0 else P.plan_bwd
+        fu, fs = fn(offs, w.num_heads, n_cta, window=window)
+        assert u.tolist() == fu and s.tolist() == fs
+    if window == (None, 0):  # the causal window is causal attention
+        assert V.jfa_plan_window(0, offs, w.num_heads, 152, window)[0].tolist() == \
+            V.jfa_plan_fwd(offs, w.num_heads, 152, causal=True)[0].tolist()
+        assert V.jfa_plan_window(1, offs, w.num_heads, 152, window)[0].tolist() == \
+            V.jfa_plan_bwd(offs, w.num_heads, 152, causal=True)[0].tolist()
+
+
 @pytest.mark.parametrize("name,w", CASES, ids=[c[0] for c in CASES])
 def test_fwd_plan_covers_every_query_row_once(name, w):
     offs = w.offsets

@@ -17,6 +17,7 @@
 #include "host.h"
 #include "plan.h"
 #include "profile.h"
+#include "topk.h"
 
 namespace jfa {
 
@@ -141,15 +142,72 @@ static int stage_to_device(void* dst, const void* src, size_t bytes, cudaStream_
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct FwdLayout {
-  size_t err = 0, units = 0, cta = 0, empty = 0, total = 0;
+  size_t err = 0, units = 0, cta = 0, empty = 0, qb = 0, total = 0;
 };
-static FwdLayout fwd_layout(int n_units, int n_cta, int batch) {
+// qb: the block-sparse forward's query-block prefix [batch+1] (topk only)
+static FwdLayout fwd_layout(int n_units, int n_cta, int batch, bool topk = false) {
   FwdLayout l;
   l.err = 0;
   l.units = 256;
   l.cta = l.units + align256(static_cast<size_t>(n_units) * 16);
   l.empty = l.cta + align256(static_cast<size_t>(n_cta + 1) * 4);
-  l.total = l.empty + align256(static_cast<size_t>(batch) * 4);
+  l.qb = l.empty + align256(static_cast<size_t>(batch) * 4);
+  l.total = l.qb + (topk ? align256(static_cast<size_t>(batch + 1) * 4) : 0);
+  return l;
+}
+
+// The first stage of the block-sparse forward (topk.cu): the blocks to average
+// -- query blocks of 256 rows (b, h, m), in that order, then key blocks of 128
+// keys (b, g, n) -- and, per query block, where its mean and its sequence's key
+// means are.  Returns the number of query blocks.
+static int topk_tasks(const int32_t* offs, int batch, int nq, int H, int Hkv, std::vector<int4>* mean_tasks,
+                      std::vector<int4>* sel_tasks, int* nk_max) {
+  mean_tasks->clear();
+  sel_tasks->clear();
+  *nk_max = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int L = offs[b + 1] - offs[b];
+    if (L == 0) continue;
+    const int rows = nq > 0 ? nq : L;
+    for (int h = 0; h < H; ++h)
+      for (int m = 0; m * kFwdRows < rows; ++m)
+        mean_tasks->push_back(make_int4((nq > 0 ? 0 : offs[b]) + kFwdRows * m, std::min(kFwdRows, rows - kFwdRows * m),
+                                        h, 0));
+  }
+  const int n_units = static_cast<int>(mean_tasks->size());
+  std::vector<int> kb_first(batch + 1, 0);
+  for (int b = 0; b < batch; ++b) {
+    const int L = offs[b + 1] - offs[b];
+    const int nblk = (L + kKvBlock - 1) / kKvBlock;
+    kb_first[b] = static_cast<int>(mean_tasks->size()) - n_units;
+    *nk_max = std::max(*nk_max, nblk);
+    for (int g = 0; g < Hkv; ++g)
+      for (int n = 0; n < nblk; ++n)
+        mean_tasks->push_back(make_int4(offs[b] + kKvBlock * n, std::min(kKvBlock, L - kKvBlock * n), g, 1));
+  }
+  const int G = H / Hkv;
+  for (int b = 0; b < batch; ++b) {
+    const int L = offs[b + 1] - offs[b];
+    if (L == 0) continue;
+    const int rows = nq > 0 ? nq : L;
+    const int nblk = (L + kKvBlock - 1) / kKvBlock;
+    for (int h = 0; h < H; ++h)
+      for (int m = 0; m * kFwdRows < rows; ++m)
+        sel_tasks->push_back(make_int4(static_cast<int>(sel_tasks->size()), n_units + kb_first[b] + (h / G) * nblk,
+                                       nblk, 0));
+  }
+  return n_units;
+}
+
+struct TopkLayout {
+  size_t err = 0, mean_tasks = 0, sel_tasks = 0, means = 0, total = 0;
+};
+static TopkLayout topk_layout(int n_tasks, int n_units, int D) {
+  TopkLayout l;
+  l.mean_tasks = 256;
+  l.sel_tasks = l.mean_tasks + align256(static_cast<size_t>(n_tasks) * 16);
+  l.means = l.sel_tasks + align256(static_cast<size_t>(n_units) * 16);
+  l.total = l.means + align256(static_cast<size_t>(n_tasks) * D * 4);
   return l;
 }
 
@@ -228,6 +286,19 @@ int sched_mode() {
     const char* e = std::getenv("JFA_SCHED");
     m = (e != nullptr && std::strcmp(e, "static") == 0) ? 0 : (e != nullptr && std::strcmp(e, "clc") == 0 ? 1 : kDefaultSched);
     g_sched_mode.store(m, std::memory_order_relaxed);
+  }
+  return m;
+}
+
+static std::atomic<int> g_block_sched_mode{-1};
+
+int block_sched_mode() {
+  int m = g_block_sched_mode.load(std::memory_order_relaxed);
+  if (m < 0) {
+    const char* e = std::getenv("JFA_SCHED_BLOCK");
+    m = (e != nullptr && std::strcmp(e, "static") == 0) ? 0
+        : (e != nullptr && std::strcmp(e, "clc") == 0 ? 1 : kDefaultBlockSched);
+    g_block_sched_mode.store(m, std::memory_order_relaxed);
   }
   return m;
 }
@@ -313,6 +384,18 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
     const int o_rows = broadcast_q ? batch * nq : offsets_host[batch];
     return bwd_layout(n, plan_ctas(dev, n), q_rows, o_rows, num_heads, head_dim).total;
   }
+  if (op == JFA_OP_TOPK_SELECT) {
+    if (head_dim != 64 && head_dim != 128) return 0;
+    std::vector<int4> mt, stasks;
+    int nk_max = 0;
+    // key blocks counted for num_heads key/value heads: an upper bound under GQA
+    const int n_units = topk_tasks(offsets_host, batch, nq, num_heads, num_heads, &mt, &stasks, &nk_max);
+    return topk_layout(static_cast<int>(mt.size()), n_units, head_dim).total;
+  }
+  if (op == JFA_OP_FWD_TOPK) {
+    const int n = plan_fwd_topk(offsets_host, batch, num_heads, nq, 1, 1, nullptr, nullptr);
+    return fwd_layout(n, plan_ctas(dev, n), batch, true).total;
+  }
   if (op == JFA_OP_BLOCK_FWD || op == JFA_OP_BLOCK_BWD) {
     const int P = plan_block(offsets_host, batch, num_heads, dev.num_sms, nullptr, nullptr);
     return block_layout(batch, P).total;
@@ -320,27 +403,49 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
   return 0;
 }
 
-extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
-                       const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
-                       int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* workspace,
-                       size_t workspace_bytes, void* stream_) {
+// The key window of a call: causal is (-1, 0); a window needs self-attention
+// and bounds of at least -1 (-1 leaves a side open).
+static int window_of(int causal, int window_left, int window_right, int broadcast_q, int* left, int* right,
+                     int* mask) {
+  if (window_left < -1 || window_right < -1) return JFA_ERR_INVALID_ARG;
+  *left = window_left;
+  *right = causal ? (window_right < 0 ? 0 : std::min(window_right, 0)) : window_right;
+  if (*left < 0 && *right < 0) {
+    *mask = kMaskNone;
+  } else if (*left < 0 && *right == 0) {
+    *mask = kMaskCausal;
+  } else {
+    *mask = kMaskWindow;
+  }
+  if (broadcast_q && *mask != kMaskNone) return JFA_ERR_UNSUPPORTED;
+  return JFA_OK;
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+                    const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
+                    int num_kv_heads, int head_dim, float scale, int causal, int window_left, int window_right,
+                    int broadcast_q, void* workspace, size_t workspace_bytes, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Common c;
   const int nq = broadcast_q ? nq_broadcast : 0;
   int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
                            head_dim, scale, causal, broadcast_q, &c);
   if (st != JFA_OK) return st;
+  int left = -1, right = -1, mask = kMaskNone;
+  st = window_of(causal, window_left, window_right, broadcast_q, &left, &right, &mask);
+  if (st != JFA_OK) return st;
   if (workspace == nullptr && workspace_bytes > 0) return JFA_ERR_INVALID_ARG;
   st = current_device(&c.dev);
   if (st != JFA_OK) return st;
 
   std::vector<int32_t> units, cta_start;
-  const int n_probe = plan_fwd(offsets_host, batch, num_heads, nq, causal, 1, nullptr, nullptr);
+  const int n_probe = plan_fwd_window(offsets_host, batch, num_heads, nq, left, right, 1, nullptr, nullptr);
   const int n_cta = plan_ctas(c.dev, n_probe);
   const int clc = sched_mode();
   int n = 0;
   // Cluster Launch Control takes the units in plain cost order (the plan dealt to one CTA)
-  if (n_cta > 0) n = plan_fwd(offsets_host, batch, num_heads, nq, causal, clc ? 1 : n_cta, &units, &cta_start);
+  if (n_cta > 0)
+    n = plan_fwd_window(offsets_host, batch, num_heads, nq, left, right, clc ? 1 : n_cta, &units, &cta_start);
   std::vector<int32_t> empty;
   if (broadcast_q)
     for (int b = 0; b < batch; ++b)
@@ -384,7 +489,13 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.D = head_dim;
   a.nq = nq;
   a.scale = scale;
-  a.causal = causal ? 1 : 0;
+  a.causal = mask == kMaskCausal ? 1 : 0;
+  a.mask = mask;
+  a.win_left = left;
+  a.win_right = right;
+  a.topk_sel = nullptr;
+  a.topk_qb = nullptr;
+  a.topk = 0;
   a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
   a.n_cta = n_cta;
@@ -395,15 +506,169 @@ extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, flo
   return launch_fwd(a);
 }
 
-extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                       void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
-                       int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale,
-                       int causal, int broadcast_q, void* workspace, size_t workspace_bytes, void* stream_) {
+extern "C" int jfa_topk_rows(const int32_t* offsets_host, int batch, int nq_broadcast, int num_heads,
+                             int broadcast_q) {
+  if (offsets_host == nullptr || batch < 0 || num_heads <= 0) return -JFA_ERR_INVALID_ARG;
+  if (check_offsets(offsets_host, batch, -1) != JFA_OK) return -JFA_ERR_BAD_OFFSETS;
+  if (broadcast_q && nq_broadcast <= 0) return -JFA_ERR_INVALID_ARG;
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(offsets_host[b + 1]) - offsets_host[b];
+    if (L > 0) n += static_cast<int64_t>(num_heads) * (((broadcast_q ? nq_broadcast : L) + kFwdRows - 1) / kFwdRows);
+  }
+  return n > INT32_MAX ? -JFA_ERR_UNSUPPORTED : static_cast<int>(n);
+}
+
+extern "C" int jfa_topk_select(const void* q, const void* k, const int32_t* offsets_dev, const int32_t* offsets_host,
+                               int batch, int max_len, int nq_broadcast, int num_heads, int num_kv_heads,
+                               int head_dim, int topk, int broadcast_q, int32_t* selection, void* workspace,
+                               size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Common c;
+  const int nq = broadcast_q ? nq_broadcast : 0;
+  int st = validate_common(q, k, k, q, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
+                           head_dim, 1.0f, 0, broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  if (topk < 1) return JFA_ERR_INVALID_ARG;
+  std::vector<int4> mt, stasks;
+  int nk_max = 0;
+  const int n_units = topk_tasks(offsets_host, batch, nq, num_heads, num_kv_heads, &mt, &stasks, &nk_max);
+  if (n_units > 0 && selection == nullptr) return JFA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(nk_max) * 4 * sizeof(float) > 48 * 1024) return JFA_ERR_UNSUPPORTED;  // > 393,216 keys
+  const TopkLayout lay = topk_layout(static_cast<int>(mt.size()), n_units, head_dim);
+  if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // the cleared error word and both task lists in one copy
+  std::vector<uint8_t> blob(lay.means - lay.err, 0);
+  std::memcpy(blob.data() + lay.mean_tasks, mt.data(), mt.size() * 16);
+  std::memcpy(blob.data() + lay.sel_tasks, stasks.data(), stasks.size() * 16);
+  st = stage_to_device(ws, blob.data(), blob.size(), stream);
+  if (st != JFA_OK) return st;
+  TopkArgs a;
+  a.q = q;
+  a.k = k;
+  a.H = num_heads;
+  a.Hkv = num_kv_heads;
+  a.D = head_dim;
+  a.mean_tasks = reinterpret_cast<const int4*>(ws + lay.mean_tasks);
+  a.n_tasks = static_cast<int>(mt.size());
+  a.means = reinterpret_cast<float*>(ws + lay.means);
+  a.sel_tasks = reinterpret_cast<const int4*>(ws + lay.sel_tasks);
+  a.n_units = n_units;
+  a.topk = topk;
+  a.nk_max = nk_max;
+  a.selection = selection;
+  a.stream = stream;
+  return launch_topk_select(a);
+}
+
+extern "C" int jfa_fwd_topk(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* selection,
+                            int topk, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                            int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim,
+                            float scale, int broadcast_q, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Common c;
+  const int nq = broadcast_q ? nq_broadcast : 0;
+  int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
+                           head_dim, scale, 0, broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  if (topk < 1) return JFA_ERR_INVALID_ARG;
+  if (workspace == nullptr && workspace_bytes > 0) return JFA_ERR_INVALID_ARG;
+  st = current_device(&c.dev);
+  if (st != JFA_OK) return st;
+  std::vector<int32_t> units, cta_start;
+  const int n_probe = plan_fwd_topk(offsets_host, batch, num_heads, nq, topk, 1, nullptr, nullptr);
+  if (n_probe > 0 && selection == nullptr) return JFA_ERR_INVALID_ARG;
+  const int n_cta = plan_ctas(c.dev, n_probe);
+  const int clc = sched_mode();
+  int n = 0;
+  if (n_cta > 0) n = plan_fwd_topk(offsets_host, batch, num_heads, nq, topk, clc ? 1 : n_cta, &units, &cta_start);
+  std::vector<int32_t> empty, qb(batch + 1, 0);
+  for (int b = 0; b < batch; ++b) {
+    const int L = offsets_host[b + 1] - offsets_host[b];
+    if (broadcast_q && L == 0) empty.push_back(b);
+    qb[b + 1] = qb[b] + (L > 0 ? ((broadcast_q ? nq : L) + kFwdRows - 1) / kFwdRows : 0);
+  }
+  const FwdLayout lay = fwd_layout(n, n_cta, batch, true);
+  if (workspace_bytes < lay.total || workspace == nullptr) return JFA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // the cleared error word, units, CTA starts, empty sequences and the
+  // query-block prefix in one copy
+  std::vector<uint8_t> blob(lay.total - lay.err, 0);
+  std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
+  std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
+  std::memcpy(blob.data() + (lay.empty - lay.err), empty.data(), empty.size() * 4);
+  std::memcpy(blob.data() + (lay.qb - lay.err), qb.data(), qb.size() * 4);
+  st = stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
+  if (st != JFA_OK) return st;
+  if (!empty.empty()) {
+    st = launch_fill_empty(reinterpret_cast<const int32_t*>(ws + lay.empty), static_cast<int>(empty.size()), nq,
+                           num_heads, head_dim, c.o_rows, o, lse, stream);
+    if (st != JFA_OK) return st;
+  }
+  if (n == 0) return JFA_OK;
+  FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.offsets_dev = offsets_dev;
+  a.q_rows = c.q_rows;
+  a.kv_rows = c.kv_rows;
+  a.o_rows = c.o_rows;
+  a.H = num_heads;
+  a.Hkv = num_kv_heads;
+  a.D = head_dim;
+  a.nq = nq;
+  a.scale = scale;
+  a.causal = 0;
+  a.mask = kMaskTopK;
+  a.win_left = a.win_right = -1;
+  a.topk_sel = selection;
+  a.topk_qb = reinterpret_cast<const int32_t*>(ws + lay.qb);
+  a.topk = topk;
+  a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
+  a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
+  a.n_cta = n_cta;
+  a.n_units = n;
+  a.use_clc = clc;
+  a.err = reinterpret_cast<int*>(ws + lay.err);
+  a.stream = stream;
+  return launch_fwd(a);
+}
+
+extern "C" int jfa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* offsets_dev,
+                       const int32_t* offsets_host, int batch, int max_len, int nq_broadcast, int num_heads,
+                       int num_kv_heads, int head_dim, float scale, int causal, int broadcast_q, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, offsets_dev, offsets_host, batch, max_len, nq_broadcast, num_heads, num_kv_heads,
+                  head_dim, scale, causal, -1, -1, broadcast_q, workspace, workspace_bytes, stream);
+}
+
+extern "C" int jfa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int32_t* offsets_dev, const int32_t* offsets_host, int batch, int max_len,
+                              int num_heads, int num_kv_heads, int head_dim, float scale, int window_left,
+                              int window_right, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, offsets_dev, offsets_host, batch, max_len, 0, num_heads, num_kv_heads, head_dim,
+                  scale, 0, window_left, window_right, 0, workspace, workspace_bytes, stream);
+}
+
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                    int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale,
+                    int causal, int window_left, int window_right, int broadcast_q, void* workspace,
+                    size_t workspace_bytes, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Common c;
   const int nq = broadcast_q ? nq_broadcast : 0;
   int st = validate_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, nq, num_heads, num_kv_heads,
                            head_dim, scale, causal, broadcast_q, &c);
+  if (st != JFA_OK) return st;
+  int left = -1, right = -1, mask = kMaskNone;
+  st = window_of(causal, window_left, window_right, broadcast_q, &left, &right, &mask);
   if (st != JFA_OK) return st;
   if (c.o_rows > 0 && (dout == nullptr || lse == nullptr || dq == nullptr)) return JFA_ERR_INVALID_ARG;
   if (c.kv_rows > 0 && (dk == nullptr || dv == nullptr)) return JFA_ERR_INVALID_ARG;
@@ -413,12 +678,13 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
 
   std::vector<int32_t> units, cta_start;
   // units run over the K/V heads; each loops over its group's query heads
-  const int n_probe = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, 1, nullptr, nullptr);
+  const int n_probe = plan_bwd_window(offsets_host, batch, num_kv_heads, nq, left, right, 1, nullptr, nullptr);
   const int n_cta = plan_ctas(c.dev, n_probe);
   const int clc = bwd_sched_mode();
   int n = 0;
   // Cluster Launch Control takes the units in plain cost order (the plan dealt to one CTA)
-  if (n_cta > 0) n = plan_bwd(offsets_host, batch, num_kv_heads, nq, causal, clc ? 1 : n_cta, &units, &cta_start);
+  if (n_cta > 0)
+    n = plan_bwd_window(offsets_host, batch, num_kv_heads, nq, left, right, clc ? 1 : n_cta, &units, &cta_start);
   const BwdLayout lay = bwd_layout(n, n_cta, c.q_rows, c.o_rows, num_heads, head_dim);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -442,7 +708,10 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   a.D = head_dim;
   a.nq = nq;
   a.scale = scale;
-  a.causal = causal ? 1 : 0;
+  a.causal = mask == kMaskCausal ? 1 : 0;
+  a.mask = mask;
+  a.win_left = left;
+  a.win_right = right;
   a.units = reinterpret_cast<const int32_t*>(ws + lay.units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + lay.cta);
   a.n_cta = n_cta;
@@ -476,6 +745,24 @@ extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* 
   return launch_dq_convert(a, c.dev.num_sms);
 }
 
+extern "C" int jfa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                       void* dq, void* dk, void* dv, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                       int max_len, int nq_broadcast, int num_heads, int num_kv_heads, int head_dim, float scale,
+                       int causal, int broadcast_q, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, offsets_dev, offsets_host, batch, max_len, nq_broadcast,
+                  num_heads, num_kv_heads, head_dim, scale, causal, -1, -1, broadcast_q, workspace, workspace_bytes,
+                  stream);
+}
+
+extern "C" int jfa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, const int32_t* offsets_dev,
+                              const int32_t* offsets_host, int batch, int max_len, int num_heads, int num_kv_heads,
+                              int head_dim, float scale, int window_left, int window_right, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, offsets_dev, offsets_host, batch, max_len, 0, num_heads,
+                  num_kv_heads, head_dim, scale, 0, window_left, window_right, 0, workspace, workspace_bytes, stream);
+}
+
 // Shared by the two block-diagonal entry points: checks, host plan, staging.
 static int block_common(const void* q, const void* k, const void* v, const void* out0, const int32_t* offsets_dev,
                         const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
@@ -504,6 +791,10 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   a->D = head_dim;
   a->n_blocks = bpb[batch];
   a->n_prog = P;
+  a->use_clc = block_sched_mode();
+  a->chunk = kBlockChunk;
+  a->n_tiles = static_cast<int>((static_cast<int64_t>(a->n_blocks) + 1) / 2 * num_heads);
+  a->n_chunks = (a->n_tiles + kBlockChunk - 1) / kBlockChunk;
   a->scale = scale;
   a->stream = stream;
   if (P == 0) return cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
@@ -524,6 +815,58 @@ extern "C" int block_attn_fwd(const void* q, const void* k, const void* v, void*
   if (st != JFA_OK || a.n_prog == 0) return st;
   a.o = o;
   return launch_block_fwd(a);
+}
+
+// The rotary tables of the rotary block entry points: both given, 16-byte
+// aligned, with a row for every position a sequence of max_len tokens has.
+static int check_rope(const float* rope_cos, const float* rope_sin, int rope_rows, int max_len) {
+  if (rope_cos == nullptr || rope_sin == nullptr || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return JFA_ERR_INVALID_ARG;
+  if (rope_rows < max_len || rope_rows < 0) return JFA_ERR_INVALID_ARG;
+  return JFA_OK;
+}
+
+extern "C" int block_attn_fwd_rope(const void* q, const void* k, const void* v, void* o, const float* rope_cos,
+                                   const float* rope_sin, int rope_rows, const int32_t* offsets_dev,
+                                   const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim,
+                                   float scale, void* workspace, size_t workspace_bytes, void* stream_) {
+  int st = check_rope(rope_cos, rope_sin, rope_rows, max_len);
+  if (st != JFA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  BlockArgs a{};
+  st = block_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
+                    workspace_bytes, stream, &a);
+  if (st != JFA_OK || a.n_prog == 0) return st;
+  a.o = o;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  return launch_block_fwd(a);
+}
+
+extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                   void* dq, void* dk, void* dv, const float* rope_cos, const float* rope_sin,
+                                   int rope_rows, const int32_t* offsets_dev, const int32_t* offsets_host, int batch,
+                                   int max_len, int num_heads, int head_dim, float scale, void* workspace,
+                                   size_t workspace_bytes, void* stream_) {
+  (void)o;  // Di is formed inline as rowsum(P o dP); O itself is not read
+  int st = check_rope(rope_cos, rope_sin, rope_rows, max_len);
+  if (st != JFA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (offsets_host != nullptr && batch >= 0 && offsets_host[batch] > 0 &&
+      (dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
+  BlockArgs a{};
+  st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
+                    workspace_bytes, stream, &a);
+  if (st != JFA_OK || a.n_prog == 0) return st;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  return launch_block_bwd(a);
 }
 
 extern "C" int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,
@@ -562,6 +905,14 @@ extern "C" int jfa_set_bwd_schedule(int mode) {
 }
 
 extern "C" int jfa_get_bwd_schedule(void) { return bwd_sched_mode(); }
+
+extern "C" int jfa_set_block_schedule(int mode) {
+  if (mode != 0 && mode != 1) return JFA_ERR_INVALID_ARG;
+  g_block_sched_mode.store(mode, std::memory_order_relaxed);
+  return JFA_OK;
+}
+
+extern "C" int jfa_get_block_schedule(void) { return block_sched_mode(); }
 
 extern "C" int jfa_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return JFA_ERR_INVALID_ARG;

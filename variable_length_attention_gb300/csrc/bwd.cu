@@ -47,8 +47,10 @@
 // tile's S^T = K Q^T, then dK += dS^T Q: the next tile's P phase overlaps dK and
 // the next dP^T, and no S^T waits for the dQ drain.
 // Masks: keys past the sequence end and query rows past it are zeroed per thread
-// (a key flag and L = +inf), so only the causal diagonal tile needs an
-// element-wise mask, and it is peeled into its own code path.
+// (a key flag and L = +inf), so only the causal diagonal tile -- or, under a
+// sliding window, a tile that straddles the window's edge -- needs an
+// element-wise mask, and it is peeled into its own code path.  Under a window
+// a unit visits only the query tiles that see its keys.
 #include <algorithm>
 #include <type_traits>
 
@@ -113,6 +115,7 @@ struct Params {
   float scale, scale_log2;
   int use_clc;  // 1: one CTA per unit in cost order, CTAs take over units of CTAs not yet launched
   int n_units;
+  int win_left, win_right;  // sliding window (kMaskWindow): keys [row - left, row + right], -1 = open
 };
 
 struct Unit {
@@ -123,7 +126,7 @@ struct Unit {
   int q_base, o_base;  // row of query 0 in q / in o
 };
 
-template <bool CAUSAL>
+template <int MASK>
 __device__ __forceinline__ Unit decode(const Params& p, int idx) {
   const int4 e = p.units[idx];
   Unit u;
@@ -141,9 +144,29 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
     u.q_base = u.kv0;
     u.o_base = u.kv0;
   }
-  u.i0 = CAUSAL ? u.n : 0;
-  u.i1 = (u.rows + BQ - 1) / BQ;
+  if (MASK == kMaskWindow) {  // the query rows that see some key of this block
+    const int k_last = min(BK * (u.n + 1), u.L) - 1;
+    const int lo = p.win_right < 0 ? 0 : max(0, BK * u.n - p.win_right);
+    const int hi = p.win_left < 0 ? u.rows : min(u.rows, k_last + p.win_left + 1);
+    u.i0 = lo / BQ;
+    u.i1 = (hi + BQ - 1) / BQ;
+  } else {
+    u.i0 = MASK == kMaskCausal ? u.n : 0;
+    u.i1 = (u.rows + BQ - 1) / BQ;
+  }
   return u;
+}
+
+// Whether query tile i sees some but not all of the keys of block n (so its P
+// needs the element mask): the causal diagonal tile, or a tile across a
+// window edge.
+template <int MASK>
+__device__ __forceinline__ bool edge_tile(const Params& p, int i, int n) {
+  if (MASK == kMaskCausal) return i == n;
+  if (MASK == kMaskWindow)
+    return (p.win_left >= 0 && BK * n < BQ * i + BQ - 1 - p.win_left) ||
+           (p.win_right >= 0 && BK * n + BK - 1 > BQ * i + p.win_right);
+  return false;
 }
 
 // TMEM column of this tile's S^T (and later of its dQ); dP^T takes the other
@@ -168,7 +191,7 @@ struct Bars {
 
 constexpr int kSchedConsumers = 13;  // 8 P/dS warps + 4 drain warps + the MMA thread
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -248,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
       if (ui < 0) break;
-      const Unit u = decode<CAUSAL>(p, ui);
+      const Unit u = decode<MASK>(p, ui);
       const bool key_ok = BK * u.n + k < u.L;
       const bool all_keys_ok = __all_sync(0xffffffffu, key_ok);  // the same in the whole warp
       for (int hg = 0; hg < p.G; ++hg)
@@ -263,12 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tDP = tmem + lane_addr + rd + 64 * wg;
         if (!mbar_wait(&bars->s_full, ph, ab)) goto done;
         tc_fence_after();
-        const bool diag = CAUSAL && i == u.n;
+        const bool diag = edge_tile<MASK>(p, i, u.n);
         // P^T first: the dV MMA can start while dS^T is being formed.  Only the
         // causal diagonal tile carries the element mask, and only warps with keys
         // past the sequence end the key select (both choices are the same for the
         // whole warp, as the TMEM accesses need).
         float pf[64];
+        const int d_base = BQ * (i - u.n) - k;  // query position - key position at column 0
         auto p_phase = [&](auto diag_tile, auto key_mask) {
 #pragma unroll
           for (int pass = 0; pass < 2; ++pass) {
@@ -285,7 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 float pe = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, -lv[e]));
                 if constexpr (decltype(diag_tile)::value) {
-                  if ((64 * wg + 32 * pass + c + e) < k) pe = 0.f;
+                  if (MASK == kMaskCausal) {
+                    if ((64 * wg + 32 * pass + c + e) < k) pe = 0.f;
+                  } else {  // query minus key position against the window's bounds
+                    const int dq_k = d_base + 64 * wg + 32 * pass + c + e;
+                    if ((p.win_left >= 0 && dq_k > p.win_left) || (p.win_right >= 0 && -dq_k > p.win_right))
+                      pe = 0.f;
+                  }
                 }
                 if constexpr (decltype(key_mask)::value) pe = key_ok ? pe : 0.f;
                 pf[32 * pass + c + e] = pe;
@@ -356,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
       if (ui < 0) break;
-      const Unit u = decode<CAUSAL>(p, ui);
+      const Unit u = decode<MASK>(p, ui);
       for (int hg = 0; hg < p.G; ++hg)
       for (int i = u.i0; i < u.i1; ++i, ++q_it) {
         const uint32_t tQ = tmem + lane_addr + region_s(q_it);  // dQ sits where this tile's S^T was
@@ -372,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // are untouched.  The buffer is taken over from the dQ reduction once its
           // boxes have been read.  Causal attention keeps the row stores: its query
           // loads are DRAM-heavy and the stores' TMA traffic measured slower there.
-          const bool full_blk = !CAUSAL && BK * (u.n + 1) <= u.L;
+          const bool full_blk = MASK == kMaskNone && BK * (u.n + 1) <= u.L;
           const bool key_ok = BK * u.n + r < u.L;
           const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.Hkv + u.h) * D;
           const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
@@ -528,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ui = sched_pop(bars, it, ab, false);
           if (ui == -2) goto mma_done;
           if (ui < 0) break;
-          const Unit u = decode<CAUSAL>(p, ui);
+          const Unit u = decode<MASK>(p, ui);
           if (!mbar_wait(&bars->kv_full, kv_ph, ab)) goto mma_done;
           kv_ph ^= 1;
           if (!issue_s(q_it)) goto mma_done;  // the unit's first tile
@@ -621,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (cur < 0) break;
-        const Unit u = decode<CAUSAL>(p, cur);
+        const Unit u = decode<MASK>(p, cur);
         if (!mbar_wait(&bars->kv_empty, kv_ph ^ 1, ab)) break;
         kv_ph ^= 1;
         if (lane == 0) {
@@ -774,7 +804,7 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 int launch_main(const BwdArgs& a) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -788,7 +818,7 @@ int launch_main(const BwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st != JFA_OK) return st;
-  auto kern = bwd_kernel<D, CAUSAL>;
+  auto kern = bwd_kernel<D, MASK>;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([&]() -> int {
     cudaFuncAttributes fa;
@@ -818,6 +848,8 @@ int launch_main(const BwdArgs& a) {
   p.scale_log2 = a.scale * kLog2e;
   p.use_clc = a.use_clc;
   p.n_units = a.n_units;
+  p.win_left = a.win_left;
+  p.win_right = a.win_right;
   ProfileScope prof(kKindBwdMain, a.stream);
   kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
@@ -849,8 +881,12 @@ int launch_bwd_prep(const BwdArgs& a, int num_sms) {
 }
 
 int launch_bwd_main(const BwdArgs& a) {
-  if (a.D == 128) return a.causal ? bwd::launch_main<128, true>(a) : bwd::launch_main<128, false>(a);
-  return a.causal ? bwd::launch_main<64, true>(a) : bwd::launch_main<64, false>(a);
+  if (a.D == 128) {
+    if (a.mask == kMaskWindow) return bwd::launch_main<128, kMaskWindow>(a);
+    return a.mask == kMaskCausal ? bwd::launch_main<128, kMaskCausal>(a) : bwd::launch_main<128, kMaskNone>(a);
+  }
+  if (a.mask == kMaskWindow) return bwd::launch_main<64, kMaskWindow>(a);
+  return a.mask == kMaskCausal ? bwd::launch_main<64, kMaskCausal>(a) : bwd::launch_main<64, kMaskNone>(a);
 }
 
 int launch_dq_convert(const BwdArgs& a, int num_sms) {

@@ -15,6 +15,8 @@ struct BwdArgs {
   int H, Hkv, D, nq;  // query heads, K/V heads (H % Hkv == 0)
   float scale;
   int causal;
+  int mask;                 // MaskKind (host.h)
+  int win_left, win_right;  // kMaskWindow: keys [row - win_left, row + win_right] are visible
   const int32_t* units;
   const int32_t* cta_start;
   int n_cta;

@@ -23,9 +23,12 @@
 // The running maximum is only moved (and O rescaled) when it grows by more than
 // 2^8; otherwise the stale maximum is kept, which is exact because numerator and
 // denominator share it.
-// Keys past the end of a sequence and, for causal attention, keys past the
-// query row are masked in separate, peeled iterations so the main loop has no
-// mask (aixai.ru summary, "Loop peeling against register spills").
+// Keys past the end of a sequence and, for causal attention or a sliding
+// window, keys outside the row's window are masked in separate, peeled
+// iterations so the main loop has no mask (aixai.ru summary, "Loop peeling
+// against register spills").  With a window each query tile visits only the
+// K/V blocks its rows can see: tile 1 may start a block later than tile 0 and
+// tile 0 may stop a block earlier.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,9 +47,15 @@ constexpr int kThreads = 512;
 // warpgroups, the epilogue warpgroup, the MMA/loader warpgroup.  Their sum must
 // not exceed what the CTA is launched with (128 per thread at 512 threads), or
 // setmaxnreg.inc would wait forever; the launcher checks the compiled count.
-constexpr int kRegSoftmax = 176, kRegEpilogue = 64, kRegIssue = 96;
-constexpr int kRegTotal = 2 * 128 * kRegSoftmax + 128 * kRegEpilogue + 128 * kRegIssue;
-static_assert(kRegTotal <= kThreads * 128, "register split exceeds the launch allocation");
+// The sliding-window softmax keeps its window bounds as well and takes 8 more.
+template <int MASK>
+struct RegSplit {
+  static constexpr int kSoftmax = MASK == kMaskWindow ? 184 : 176;
+  static constexpr int kEpilogue = MASK == kMaskWindow ? 56 : 64;
+  static constexpr int kIssue = MASK == kMaskWindow ? 88 : 96;
+  static constexpr int kTotal = 2 * 128 * kSoftmax + 128 * kEpilogue + 128 * kIssue;
+  static_assert(kTotal <= kThreads * 128, "register split exceeds the launch allocation");
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -73,6 +82,10 @@ struct Params {
   int H, Hkv, nq, o_rows;
   int n_units;
   int use_clc;               // 1: one CTA per unit in cost order, idle CTAs claim pending ones
+  int win_left, win_right;   // sliding window (kMaskWindow): keys [row - left, row + right], -1 = open
+  const int32_t* topk_sel;   // block-sparse (kMaskTopK): chosen key blocks [query blocks, topk]
+  const int32_t* topk_qb;    // query blocks before each sequence [batch+1]
+  int topk;
   float scale_log2;
 };
 
@@ -82,14 +95,30 @@ struct Unit {
   int rows;         // query rows of the sequence (self) or of the shared Q (broadcast)
   int q_row0;       // first query row of the unit in q
   int o_row0;       // first output row of the unit in o
-  int n_kv;         // K/V blocks visited
-  int n_plain;      // leading blocks that need no mask
-  int n_kv0;        // blocks query tile 0 needs (causal: it skips the unit's last block when
+  int j0, n_kv;     // K/V blocks loaded: j0 .. j0 + n_kv - 1
+  int je0;          // tile 0 visits blocks [j0, je0) (causal: it skips the unit's last block when
                     // that block lies wholly in its masked future)
+  int jb1, je1;     // tile 1 visits blocks [jb1, je1)
+  int pb0, pe0;     // tile 0: blocks in [pb0, pe0) need no mask
+  int pb1, pe1;     // tile 1: the same
   int nt;           // query tiles of the unit: 1 when the second tile lies wholly past the last row
+  const int32_t* sel;  // block-sparse: the unit's chosen key blocks (block j of the loop is sel[j])
+  int tail_hi;         // block-sparse: valid keys of the sequence's last block
 };
 
-template <bool CAUSAL>
+// Block range [*jb, *je) a query tile whose rows are [r, last] sees under a
+// window, and the range [*pb, *pe) of those blocks that every row sees whole.
+__device__ __forceinline__ void window_blocks(int r, int last, int L, int left, int right, int* jb, int* je,
+                                              int* pb, int* pe) {
+  const int lo = left < 0 ? 0 : max(0, r - left);
+  const int hi = right < 0 ? L : min(L, last + right + 1);
+  *jb = lo / BN;
+  *je = (hi + BN - 1) / BN;
+  *pb = (left < 0 || last - left <= 0) ? 0 : (last - left + BN - 1) / BN;
+  *pe = right < 0 ? L / BN : min(L / BN, (r + right + 1) / BN);
+}
+
+template <int MASK>
 __device__ __forceinline__ Unit decode(const Params& p, int idx) {
   const int4 e = p.units[idx];
   Unit u;
@@ -109,15 +138,39 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
     u.o_row0 = u.q_row0;
   }
   u.nt = 2 * BM * u.m + BM < u.rows ? 2 : 1;
-  if (CAUSAL) {
+  u.j0 = 0;
+  u.jb1 = 0;
+  u.pb0 = u.pb1 = 0;
+  if (MASK == kMaskCausal) {
     const int last = min(2 * BM * (u.m + 1), u.rows);
     u.n_kv = (min(last, u.L) + BN - 1) / BN;
-    u.n_plain = min(u.L / BN, 2 * u.m);
-    u.n_kv0 = min(u.n_kv, 2 * u.m + 1);
+    u.pe0 = u.pe1 = min(u.L / BN, 2 * u.m);
+    u.je0 = min(u.n_kv, 2 * u.m + 1);
+    u.je1 = u.n_kv;
+  } else if (MASK == kMaskWindow) {  // self-attention only: rows = L
+    const int r0 = 2 * BM * u.m;
+    int je1 = 0;
+    window_blocks(r0, min(r0 + BM, u.L) - 1, u.L, p.win_left, p.win_right, &u.j0, &u.je0, &u.pb0, &u.pe0);
+    if (u.nt == 2)
+      window_blocks(r0 + BM, min(r0 + 2 * BM, u.L) - 1, u.L, p.win_left, p.win_right, &u.jb1, &je1, &u.pb1,
+                    &u.pe1);
+    u.je1 = je1;
+    u.n_kv = max(u.je0, je1) - u.j0;
+  } else if (MASK == kMaskTopK) {  // the chosen blocks, in ascending order
+    const int nblk = (u.L + BN - 1) / BN;
+    const int q0 = p.topk_qb[u.b];
+    const int row = p.H * q0 + u.h * (p.topk_qb[u.b + 1] - q0) + u.m;
+    u.sel = p.topk_sel + static_cast<size_t>(row) * p.topk;
+    u.n_kv = min(p.topk, nblk);
+    u.je0 = u.je1 = u.n_kv;
+    // only the sequence's last block can be short; chosen, it is the last in the list
+    const bool tail = (u.L % BN) != 0 && u.sel[u.n_kv - 1] == nblk - 1;
+    u.pe0 = u.pe1 = tail ? u.n_kv - 1 : u.n_kv;
+    u.tail_hi = u.L - (nblk - 1) * BN;
   } else {
     u.n_kv = (u.L + BN - 1) / BN;
-    u.n_plain = u.L / BN;
-    u.n_kv0 = u.n_kv;
+    u.pe0 = u.pe1 = u.L / BN;
+    u.je0 = u.je1 = u.n_kv;
   }
   return u;
 }
@@ -149,7 +202,7 @@ struct Bars {
 constexpr int kSchedConsumers = 13;  // MMA thread + 8 softmax warps + 4 epilogue warps
 
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params p) {
@@ -204,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    setmaxnreg_inc<kRegSoftmax>();
+    setmaxnreg_inc<RegSplit<MASK>::kSoftmax>();
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = threadIdx.x & 127;       // TMEM lane == row of the tile
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -216,12 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
       if (ui < 0) break;
-      const Unit u = decode<CAUSAL>(p, ui);
+      const Unit u = decode<MASK>(p, ui);
       if (t >= u.nt) continue;                     // a single-tile unit: nothing for tile 1
       const int qi = 2 * BM * u.m + BM * t + row;  // query index inside the sequence / shared Q
       float m_run = -INFINITY, l_run = 0.f;
-      const int n_kv_t = t == 0 ? u.n_kv0 : u.n_kv;
-      for (int j = 0; j < n_kv_t; ++j) {
+      // blocks [jb, je) of the tile; those in [pb, pe) need no mask (without a
+      // window every tile starts at block 0 and only trailing blocks are masked)
+      constexpr bool kRanged = MASK == kMaskWindow || MASK == kMaskTopK;
+      const int jb = kRanged ? (t == 0 ? u.j0 : u.jb1) : 0, je = t == 0 ? u.je0 : u.je1;
+      const int pb = MASK == kMaskWindow ? (t == 0 ? u.pb0 : u.pb1) : 0, pe = t == 0 ? u.pe0 : u.pe1;
+      for (int j = jb; j < je; ++j) {
         if (!mbar_wait(&bars->s_full[t], s_phase, ab)) goto done;
         s_phase ^= 1;
         tc_fence_after();
@@ -235,12 +292,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[BN];
 #pragma unroll
         for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j >= u.n_plain) {  // peeled tail / diagonal iterations
-          int limit = u.L - j * BN;
-          if (CAUSAL) limit = min(limit, qi - j * BN + 1);
+        if ((MASK == kMaskWindow && j < pb) || j >= pe) {  // peeled tail / diagonal / window-edge iterations
+          // visible key columns of this block: [lo, hi)
+          const int wr = MASK == kMaskCausal ? 0 : (MASK == kMaskWindow ? p.win_right : -1);
+          const int hi = MASK == kMaskTopK ? u.tail_hi : (wr < 0 ? u.L : min(u.L, qi + wr + 1)) - j * BN;
+          if (MASK == kMaskWindow) {
+            const int lo = p.win_left < 0 ? -BN : qi - p.win_left - j * BN;
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c >= limit) s[c] = -INFINITY;
+            for (int c = 0; c < BN; ++c)
+              if (c >= hi || c < lo) s[c] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (c >= hi) s[c] = -INFINITY;
+          }
         }
         // row maximum: 4 independent partial maxima, two new values per step
         float pm[4];
@@ -257,8 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // executed by all 32 lanes together; moving a maximum that grew by
         // less is exact all the same.
         if (__any_sync(0xffffffffu, m_new > m_run + kRescaleThreshold)) {
-          if (j > 0) {
-            const float alpha = ex2(m_run - m_new);
+          if (j > jb) {
+            // a row that has seen no key yet (window) has nothing to rescale
+            const float alpha = (MASK == kMaskWindow && m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
             l_run *= alpha;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -275,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // s * scale * log2(e) - m two columns per instruction, and the row sum
         // kept as two paired partial sums
-        const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-m_run, -m_run);
+        // (under a window a row may not have seen any key yet: its maximum is
+        // still -inf, and every score of the block is -inf too)
+        const float neg_m = (MASK == kMaskWindow && m_run == -INFINITY) ? 0.f : -m_run;
+        const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(neg_m, neg_m);
         uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
         uint32_t pk[BN / 2];
 #pragma unroll
@@ -308,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ epilogue
-    setmaxnreg_dec<kRegEpilogue>();
+    setmaxnreg_dec<RegSplit<MASK>::kEpilogue>();
     const int row = threadIdx.x & 127;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t tph0 = 0, tph1 = 0, sf_ph = 0, sr_ph = 0;  // o_full / st_full phase of each tile
@@ -317,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ui = sched_pop(bars, it, ab, true);
       if (ui == -2) goto done;
       if (ui < 0) break;
-      const Unit u = decode<CAUSAL>(p, ui);
+      const Unit u = decode<MASK>(p, ui);
       for (int t = 0; t < u.nt; ++t) {
         const uint32_t phase = t == 0 ? tph0 : tph1;
         if (t == 0)
@@ -396,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 256) bulk_wait_all();  // every store has landed before the CTA exits
   } else {
-    setmaxnreg_dec<kRegIssue>();
+    setmaxnreg_dec<RegSplit<MASK>::kIssue>();
     if (warp == 12 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
@@ -451,85 +520,186 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars->s_full[0]);
         s0_early = true;
       };
-      for (uint32_t it = 0;; ++it) {
-        const int ui = sched_pop(bars, it, ab, false);
-        if (ui < 0) break;
-        const Unit u = decode<CAUSAL>(p, ui);
-        const uint32_t kv_next = kv_it + 2 * u.n_kv;  // the next unit's first K block in the ring
-        uint32_t ks = stage_of(kv_it);
-        if (!mbar_wait(&bars->kv_full[ks], phase_of(kv_it), ab)) goto mma_done;
-        if (!s0_early) {
-          if (!mbar_wait(&bars->q_full[0], q_ph[0], ab)) goto mma_done;
-          tc_fence_after();
-          issue_s(0, ks);
-          mma_commit(&bars->s_full[0]);
-        }
-        q_ph[0] ^= 1;
-        s0_early = false;
-        if (u.nt == 2) {
-          if (!mbar_wait(&bars->q_full[1], q_ph[1], ab)) goto mma_done;
-          q_ph[1] ^= 1;
-          tc_fence_after();
-          issue_s(1, ks);
-          mma_commit(&bars->s_full[1]);
-        }
-        mma_commit(&bars->kv_empty[ks]);
-        if (u.n_kv == 1) mma_commit(&bars->q_empty);
-        ++kv_it;
-        for (int j = 0; j < u.n_kv; ++j) {
-          const uint32_t vs = stage_of(kv_it);
-          if (!mbar_wait(&bars->kv_full[vs], phase_of(kv_it), ab)) goto mma_done;
-          ++kv_it;
-          const bool more = j + 1 < u.n_kv;
-          uint32_t ks2 = 0;
-          if (more) {  // K_{j+1}
-            ks2 = stage_of(kv_it);
-            if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
-            ++kv_it;
-          }
-          // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop one block early;
-          // a single-tile unit visits every block with tile 0)
-          if (j < u.n_kv0) {
-            if (j == 0) {
-              if (!mbar_wait(&bars->o_empty[0], (o_cnt[0] & 1) ^ 1, ab)) goto mma_done;
-              ++o_cnt[0];
-            }
-            if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
-            p_phase[0] ^= 1;
+      if constexpr (MASK == kMaskNone || MASK == kMaskCausal) {
+        // every query tile starts at block 0 and tile 0 may stop one block early:
+        // the loop as measured fastest for these two
+        for (uint32_t it = 0;; ++it) {
+          const int ui = sched_pop(bars, it, ab, false);
+          if (ui < 0) break;
+          const Unit u = decode<MASK>(p, ui);
+          const uint32_t kv_next = kv_it + 2 * u.n_kv;  // the next unit's first K block in the ring
+          uint32_t ks = stage_of(kv_it);
+          if (!mbar_wait(&bars->kv_full[ks], phase_of(kv_it), ab)) goto mma_done;
+          if (!s0_early) {
+            if (!mbar_wait(&bars->q_full[0], q_ph[0], ab)) goto mma_done;
             tc_fence_after();
-            issue_pv(0, vs, j > 0);
-            if (j + 1 == u.n_kv0) {
-              mma_commit(&bars->o_full[0]);
-              if (u.nt == 1) mma_commit(&bars->kv_empty[vs]);
-              try_early_s0(it + 1, kv_next);
-            } else {
-              issue_s(0, ks2);
-              mma_commit(&bars->s_full[0]);
-              if (u.nt == 1) {
-                mma_commit(&bars->kv_empty[vs]);
-                mma_commit(&bars->kv_empty[ks2]);
-                if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+            issue_s(0, ks);
+            mma_commit(&bars->s_full[0]);
+          }
+          q_ph[0] ^= 1;
+          s0_early = false;
+          if (u.nt == 2) {
+            if (!mbar_wait(&bars->q_full[1], q_ph[1], ab)) goto mma_done;
+            q_ph[1] ^= 1;
+            tc_fence_after();
+            issue_s(1, ks);
+            mma_commit(&bars->s_full[1]);
+          }
+          mma_commit(&bars->kv_empty[ks]);
+          if (u.n_kv == 1) mma_commit(&bars->q_empty);
+          ++kv_it;
+          for (int j = 0; j < u.n_kv; ++j) {
+            const uint32_t vs = stage_of(kv_it);
+            if (!mbar_wait(&bars->kv_full[vs], phase_of(kv_it), ab)) goto mma_done;
+            ++kv_it;
+            const bool more = j + 1 < u.n_kv;
+            uint32_t ks2 = 0;
+            if (more) {  // K_{j+1}
+              ks2 = stage_of(kv_it);
+              if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
+              ++kv_it;
+            }
+            // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop one block early;
+            // a single-tile unit visits every block with tile 0)
+            if (j < u.je0) {
+              if (j == 0) {
+                if (!mbar_wait(&bars->o_empty[0], (o_cnt[0] & 1) ^ 1, ab)) goto mma_done;
+                ++o_cnt[0];
+              }
+              if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
+              p_phase[0] ^= 1;
+              tc_fence_after();
+              issue_pv(0, vs, j > 0);
+              if (j + 1 == u.je0) {
+                mma_commit(&bars->o_full[0]);
+                if (u.nt == 1) mma_commit(&bars->kv_empty[vs]);
+                try_early_s0(it + 1, kv_next);
+              } else {
+                issue_s(0, ks2);
+                mma_commit(&bars->s_full[0]);
+                if (u.nt == 1) {
+                  mma_commit(&bars->kv_empty[vs]);
+                  mma_commit(&bars->kv_empty[ks2]);
+                  if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+                }
               }
             }
+            if (u.nt == 1) continue;
+            // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+            if (j == 0) {
+              if (!mbar_wait(&bars->o_empty[1], (o_cnt[1] & 1) ^ 1, ab)) goto mma_done;
+              ++o_cnt[1];
+            }
+            if (!more) try_early_s0(it + 1, kv_next);  // a second chance before the last wait
+            if (!mbar_wait(&bars->p_full[1], p_phase[1], ab)) goto mma_done;
+            p_phase[1] ^= 1;
+            tc_fence_after();
+            issue_pv(1, vs, j > 0);
+            mma_commit(&bars->kv_empty[vs]);
+            if (!more) mma_commit(&bars->o_full[1]);
+            if (more) {
+              issue_s(1, ks2);
+              mma_commit(&bars->s_full[1]);
+              mma_commit(&bars->kv_empty[ks2]);
+              if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+            }
           }
-          if (u.nt == 1) continue;
-          // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-          if (j == 0) {
-            if (!mbar_wait(&bars->o_empty[1], (o_cnt[1] & 1) ^ 1, ab)) goto mma_done;
-            ++o_cnt[1];
+        }
+      } else {
+        // sliding window and block-sparse: each tile visits its own block range
+        for (uint32_t it = 0;; ++it) {
+          const int ui = sched_pop(bars, it, ab, false);
+          if (ui < 0) break;
+          const Unit u = decode<MASK>(p, ui);
+          const uint32_t kv_next = kv_it + 2 * u.n_kv;  // the next unit's first K block in the ring
+          const int j1 = u.j0 + u.n_kv;                 // blocks j0 .. j1-1 are in the ring, K then V
+          const int jb1 = u.nt == 2 ? u.jb1 : j1, je1 = u.nt == 2 ? u.je1 : j1;  // tile 1's blocks
+          // score GEMMs still to issue for this unit; Q is free once they are
+          int s_left = (u.je0 - u.j0) + (je1 - jb1);
+          auto s_issued = [&]() {
+            if (--s_left == 0) mma_commit(&bars->q_empty);
+          };
+          uint32_t ks = stage_of(kv_it);
+          if (!mbar_wait(&bars->kv_full[ks], phase_of(kv_it), ab)) goto mma_done;
+          if (!s0_early) {
+            if (!mbar_wait(&bars->q_full[0], q_ph[0], ab)) goto mma_done;
+            tc_fence_after();
+            issue_s(0, ks);
+            mma_commit(&bars->s_full[0]);
           }
-          if (!more) try_early_s0(it + 1, kv_next);  // a second chance before the last wait
-          if (!mbar_wait(&bars->p_full[1], p_phase[1], ab)) goto mma_done;
-          p_phase[1] ^= 1;
-          tc_fence_after();
-          issue_pv(1, vs, j > 0);
-          mma_commit(&bars->kv_empty[vs]);
-          if (!more) mma_commit(&bars->o_full[1]);
-          if (more) {
-            issue_s(1, ks2);
+          q_ph[0] ^= 1;
+          s0_early = false;
+          if (u.nt == 2) {
+            if (!mbar_wait(&bars->q_full[1], q_ph[1], ab)) goto mma_done;
+            q_ph[1] ^= 1;
+            tc_fence_after();
+          }
+          if (jb1 == u.j0) {
+            issue_s(1, ks);
             mma_commit(&bars->s_full[1]);
-            mma_commit(&bars->kv_empty[ks2]);
-            if (j + 2 == u.n_kv) mma_commit(&bars->q_empty);
+            s_issued();
+          }
+          mma_commit(&bars->kv_empty[ks]);
+          s_issued();  // tile 0's first S
+          ++kv_it;
+          for (int j = u.j0; j < j1; ++j) {
+            const uint32_t vs = stage_of(kv_it);
+            if (!mbar_wait(&bars->kv_full[vs], phase_of(kv_it), ab)) goto mma_done;
+            ++kv_it;
+            const bool more = j + 1 < j1;
+            uint32_t ks2 = 0;
+            if (more) {  // K_{j+1}
+              ks2 = stage_of(kv_it);
+              if (!mbar_wait(&bars->kv_full[ks2], phase_of(kv_it), ab)) goto mma_done;
+              ++kv_it;
+            }
+            const bool t1_now = jb1 <= j && j < je1, t1_next = more && jb1 <= j + 1 && j + 1 < je1;
+            // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (tile 0 may stop early)
+            if (j < u.je0) {
+              if (j == u.j0) {
+                if (!mbar_wait(&bars->o_empty[0], (o_cnt[0] & 1) ^ 1, ab)) goto mma_done;
+                ++o_cnt[0];
+              }
+              if (!mbar_wait(&bars->p_full[0], p_phase[0], ab)) goto mma_done;
+              p_phase[0] ^= 1;
+              tc_fence_after();
+              issue_pv(0, vs, j > u.j0);
+              if (j + 1 == u.je0) {
+                mma_commit(&bars->o_full[0]);
+                if (!t1_now) mma_commit(&bars->kv_empty[vs]);
+                try_early_s0(it + 1, kv_next);
+              } else {
+                issue_s(0, ks2);
+                mma_commit(&bars->s_full[0]);
+                s_issued();
+                if (!t1_now) mma_commit(&bars->kv_empty[vs]);
+                if (!t1_next) mma_commit(&bars->kv_empty[ks2]);
+              }
+            }
+            // tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
+            if (t1_now) {
+              if (j == jb1) {
+                if (!mbar_wait(&bars->o_empty[1], (o_cnt[1] & 1) ^ 1, ab)) goto mma_done;
+                ++o_cnt[1];
+              }
+              if (!more) try_early_s0(it + 1, kv_next);  // a second chance before the last wait
+              if (!mbar_wait(&bars->p_full[1], p_phase[1], ab)) goto mma_done;
+              p_phase[1] ^= 1;
+              tc_fence_after();
+              issue_pv(1, vs, j > jb1);
+              mma_commit(&bars->kv_empty[vs]);
+              if (j + 1 == je1) mma_commit(&bars->o_full[1]);
+            }
+            if (t1_next) {
+              issue_s(1, ks2);
+              mma_commit(&bars->s_full[1]);
+              s_issued();
+              mma_commit(&bars->kv_empty[ks2]);
+            }
+            // (the two tiles' block ranges overlap or touch, so every block has a
+            // reader; the releases below only guard the ring against a gap)
+            if (j >= u.je0 && !t1_now) mma_commit(&bars->kv_empty[vs]);
+            if (more && j + 1 >= u.je0 && !t1_next) mma_commit(&bars->kv_empty[ks2]);
           }
         }
       }
@@ -559,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bars->clc_bar, 16);
           clc_try_cancel(&bars->clc_resp, &bars->clc_bar);
         }
-        const Unit u = decode<CAUSAL>(p, cur);
+        const Unit u = decode<MASK>(p, cur);
         if (!mbar_wait(&bars->q_empty, u_phase ^ 1, ab)) break;
         for (int t = 0; t < u.nt; ++t) {
           mbar_expect_tx(&bars->q_full[t], C::TILE_BYTES);
@@ -581,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_2d(tm, &bars->kv_full[s], sKV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, u.g * D + c * 64,
-                          u.kv0 + BN * j);
+                          u.kv0 + BN * (MASK == kMaskTopK ? u.sel[j] : u.j0 + j));
             ++kv_it;
           }
         }
@@ -614,7 +784,7 @@ done:
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 int launch_impl(const FwdArgs& a) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
@@ -624,12 +794,12 @@ int launch_impl(const FwdArgs& a) {
   CUtensorMap to;  // O, for the epilogue's TMA stores of full tiles
   if (st == JFA_OK) st = make_map_2d(&to, a.o, static_cast<uint64_t>(a.H) * D, a.o_rows, 64, BM);
   if (st != JFA_OK) return st;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, MASK>;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([&]() -> int {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return JFA_ERR_CUDA;
-    if (fa.numRegs * kThreads < kRegTotal) return JFA_ERR_UNSUPPORTED;  // the split could never be granted
+    if (fa.numRegs * kThreads < RegSplit<MASK>::kTotal) return JFA_ERR_UNSUPPORTED;  // never granted otherwise
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) != cudaSuccess)
       return JFA_ERR_CUDA;
     return JFA_OK;
@@ -649,6 +819,11 @@ int launch_impl(const FwdArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.n_units = a.n_units;
   p.use_clc = a.use_clc;
+  p.win_left = a.win_left;
+  p.win_right = a.win_right;
+  p.topk_sel = a.topk_sel;
+  p.topk_qb = a.topk_qb;
+  p.topk = a.topk;
   ProfileScope prof(kKindFwd, a.stream);
   kern<<<a.use_clc ? a.n_units : a.n_cta, kThreads, C::SMEM_ALLOC, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
@@ -657,8 +832,14 @@ int launch_impl(const FwdArgs& a) {
 }  // namespace fwd
 
 int launch_fwd(const FwdArgs& a) {
-  if (a.D == 128) return a.causal ? fwd::launch_impl<128, true>(a) : fwd::launch_impl<128, false>(a);
-  return a.causal ? fwd::launch_impl<64, true>(a) : fwd::launch_impl<64, false>(a);
+  if (a.D == 128) {
+    if (a.mask == kMaskWindow) return fwd::launch_impl<128, kMaskWindow>(a);
+    if (a.mask == kMaskTopK) return fwd::launch_impl<128, kMaskTopK>(a);
+    return a.mask == kMaskCausal ? fwd::launch_impl<128, kMaskCausal>(a) : fwd::launch_impl<128, kMaskNone>(a);
+  }
+  if (a.mask == kMaskWindow) return fwd::launch_impl<64, kMaskWindow>(a);
+  if (a.mask == kMaskTopK) return fwd::launch_impl<64, kMaskTopK>(a);
+  return a.mask == kMaskCausal ? fwd::launch_impl<64, kMaskCausal>(a) : fwd::launch_impl<64, kMaskNone>(a);
 }
 
 }  // namespace jfa

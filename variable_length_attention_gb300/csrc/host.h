@@ -55,6 +55,13 @@ int make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Which keys a query row sees inside its sequence: all of them, those up to
+// the row (causal), or those within [row - win_left, row + win_right] (a
+// sliding window; a negative bound leaves its side open).
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2, kMaskTopK = 3 };
+// kMaskTopK: each 256-row query unit attends over the key blocks a first
+// stage chose for it (block-sparse forward; see topk.cu).
+
 // Kernel launchers (one per .cu file).  They assume validated arguments.
 struct FwdArgs {
   const void *q, *k, *v;
@@ -65,6 +72,11 @@ struct FwdArgs {
   int H, Hkv, D, nq;            // nq > 0: broadcast-Q
   float scale;
   int causal;
+  int mask;                     // MaskKind
+  int win_left, win_right;      // kMaskWindow: visible keys [row - win_left, row + win_right]
+  const int32_t* topk_sel;      // kMaskTopK: chosen key blocks [query blocks, topk], ascending, -1 padded
+  const int32_t* topk_qb;       // kMaskTopK: query blocks before each sequence [batch+1]
+  int topk;
   const int32_t* units;         // device, 4 ints per unit
   const int32_t* cta_start;     // device, n_cta + 1 (static plan only)
   int n_cta;                    // static plan: CTAs launched
@@ -84,5 +96,12 @@ int sched_mode();
 // jfa_set_bwd_schedule() changes it.
 constexpr int kDefaultBwdSched = 1;  // measured faster on the jagged, broadcast-Q and dense backward
 int bwd_sched_mode();
+// The same choice for the block-diagonal kernels: JFA_SCHED_BLOCK, else
+// kDefaultBlockSched; jfa_set_block_schedule() changes it.  Under Cluster
+// Launch Control a CTA's unit of work is a chunk of kBlockChunk consecutive
+// (block pair, head) tiles.
+constexpr int kDefaultBlockSched = 1;  // measured faster (D=128 forward and backward, D=64 backward)
+constexpr int kBlockChunk = 16;
+int block_sched_mode();
 
 }  // namespace jfa

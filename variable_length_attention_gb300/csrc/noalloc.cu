@@ -140,6 +140,12 @@ extern "C" int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void
   a.nq = nq;
   a.scale = scale;
   a.causal = causal ? 1 : 0;
+  a.mask = causal ? kMaskCausal : kMaskNone;
+  a.win_left = -1;
+  a.win_right = causal ? 0 : -1;
+  a.topk_sel = nullptr;
+  a.topk_qb = nullptr;
+  a.topk = 0;
   a.units = reinterpret_cast<const int32_t*>(ws + off_units);
   a.cta_start = reinterpret_cast<const int32_t*>(ws + off_cta);
   a.n_cta = n_cta;

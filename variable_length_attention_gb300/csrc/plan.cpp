@@ -103,8 +103,32 @@ static int deal_sorted(Enumerate&& each, int64_t n, int n_cta, std::vector<int32
   return static_cast<int>(n);
 }
 
+// Visible keys of query row i: [i - left, i + right] inside the sequence, a
+// negative bound leaving its side open (causal: left < 0, right = 0).
+// K/V blocks the 256-row forward unit m visits: from the first block its first
+// row sees to the last block its last row sees.
+static int64_t fwd_unit_blocks(int64_t m, int64_t rows, int64_t L, int left, int right) {
+  const int64_t r0 = kFwdRows * m, last = std::min<int64_t>(kFwdRows * (m + 1), rows) - 1;
+  const int64_t lo = left < 0 ? 0 : std::max<int64_t>(0, r0 - left);
+  const int64_t hi = right < 0 ? L : std::min<int64_t>(L, last + right + 1);
+  return cdiv(hi, kKvBlock) - lo / kKvBlock;
+}
+
+// 128-row query tiles that the keys of 128-key block n meet.
+static int64_t bwd_unit_tiles(int64_t n, int64_t rows, int64_t L, int left, int right) {
+  const int64_t k_last = std::min<int64_t>(kKvBlock * (n + 1), L) - 1;
+  const int64_t lo = right < 0 ? 0 : std::max<int64_t>(0, kKvBlock * n - right);
+  const int64_t hi = left < 0 ? rows : std::min<int64_t>(rows, k_last + left + 1);
+  return cdiv(hi, kKvBlock) - lo / kKvBlock;
+}
+
 int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
+  return plan_fwd_window(offsets, batch, H, nq, -1, causal ? 0 : -1, n_cta, units, cta_start);
+}
+
+int plan_fwd_window(const int32_t* offsets, int batch, int H, int nq, int left, int right, int n_cta,
+                    std::vector<int32_t>* units, std::vector<int32_t>* cta_start) {
   // enumeration order: sequence, head, 256-row unit; cost = K/V blocks visited
   auto each = [&](auto&& fn) {
     for (int b = 0; b < batch; ++b) {
@@ -113,16 +137,29 @@ int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
       const int64_t rows = nq > 0 ? nq : L;
       const int64_t nm = cdiv(rows, kFwdRows);
       for (int h = 0; h < H; ++h)
-        for (int64_t m = 0; m < nm; ++m) {
-          int64_t cost;
-          if (causal) {
-            const int64_t last_row = std::min<int64_t>(kFwdRows * (m + 1), rows);
-            cost = cdiv(std::min(last_row, L), kKvBlock);
-          } else {
-            cost = cdiv(L, kKvBlock);
-          }
-          fn(b, h, static_cast<int32_t>(m), static_cast<int32_t>(cost));
-        }
+        for (int64_t m = 0; m < nm; ++m)
+          fn(b, h, static_cast<int32_t>(m), static_cast<int32_t>(fwd_unit_blocks(m, rows, L, left, right)));
+    }
+  };
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+    if (L > 0) n += static_cast<int64_t>(H) * cdiv(nq > 0 ? nq : L, kFwdRows);
+  }
+  return deal_sorted(each, n, n_cta, units, cta_start);
+}
+
+int plan_fwd_topk(const int32_t* offsets, int batch, int H, int nq, int topk, int n_cta, std::vector<int32_t>* units,
+                  std::vector<int32_t>* cta_start) {
+  // the forward's units and order; a unit visits its min(topk, blocks) chosen blocks
+  auto each = [&](auto&& fn) {
+    for (int b = 0; b < batch; ++b) {
+      const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
+      if (L == 0) continue;
+      const int64_t nm = cdiv(nq > 0 ? nq : L, kFwdRows);
+      const int32_t cost = static_cast<int32_t>(std::min<int64_t>(topk, cdiv(L, kKvBlock)));
+      for (int h = 0; h < H; ++h)
+        for (int64_t m = 0; m < nm; ++m) fn(b, h, static_cast<int32_t>(m), cost);
     }
   };
   int64_t n = 0;
@@ -135,6 +172,11 @@ int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
 
 int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start) {
+  return plan_bwd_window(offsets, batch, H, nq, -1, causal ? 0 : -1, n_cta, units, cta_start);
+}
+
+int plan_bwd_window(const int32_t* offsets, int batch, int H, int nq, int left, int right, int n_cta,
+                    std::vector<int32_t>* units, std::vector<int32_t>* cta_start) {
   // enumeration order: sequence, head (key/value head), 128-key block; cost =
   // query tiles visited per query head.
   // Equal costs (broadcast-Q) keep this order; unequal ones (self-attention,
@@ -143,11 +185,11 @@ int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
   auto each = [&](auto&& fn) {
     for (int b = 0; b < batch; ++b) {
       const int64_t L = static_cast<int64_t>(offsets[b + 1]) - offsets[b];
-      const int64_t q_tiles = cdiv(nq > 0 ? nq : L, kKvBlock);
+      const int64_t rows = nq > 0 ? nq : L;
       const int64_t nblk = cdiv(L, kKvBlock);
       for (int h = 0; h < H; ++h)
         for (int64_t blk = 0; blk < nblk; ++blk)
-          fn(b, h, static_cast<int32_t>(blk), static_cast<int32_t>(causal ? q_tiles - blk : q_tiles));
+          fn(b, h, static_cast<int32_t>(blk), static_cast<int32_t>(bwd_unit_tiles(blk, rows, L, left, right)));
     }
   };
   int64_t n = 0;
@@ -198,6 +240,25 @@ extern "C" int jfa_plan_bwd(const int32_t* offsets_host, int batch, int num_head
   std::vector<int32_t> u, s;
   const int n = jfa::plan_bwd(offsets_host, batch, num_heads, nq_broadcast, causal, n_cta, units ? &u : nullptr,
                               cta_start ? &s : nullptr);
+  if (units) std::copy(u.begin(), u.end(), units);
+  if (cta_start) std::copy(s.begin(), s.end(), cta_start);
+  return n;
+}
+
+extern "C" int jfa_plan_window(int which, const int32_t* offsets_host, int batch, int num_heads, int window_left,
+                               int window_right, int n_cta, int32_t* units, int32_t* cta_start) {
+  if (num_heads <= 0 || n_cta <= 0 || window_left < -1 || window_right < -1 || which < 0 || which > 1)
+    return -JFA_ERR_INVALID_ARG;
+  const int st = jfa::check_offsets(offsets_host, batch, -1);
+  if (st != JFA_OK) return -st;
+  std::vector<int32_t> u, s;
+  int n;
+  if (which == 0)
+    n = jfa::plan_fwd_window(offsets_host, batch, num_heads, 0, window_left, window_right, n_cta,
+                             units ? &u : nullptr, cta_start ? &s : nullptr);
+  else
+    n = jfa::plan_bwd_window(offsets_host, batch, num_heads, 0, window_left, window_right, n_cta,
+                             units ? &u : nullptr, cta_start ? &s : nullptr);
   if (units) std::copy(u.begin(), u.end(), units);
   if (cta_start) std::copy(s.begin(), s.end(), cta_start);
   return n;

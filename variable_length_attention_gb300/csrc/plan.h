@@ -18,6 +18,16 @@ int plan_fwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n
              std::vector<int32_t>* cta_start);
 int plan_bwd(const int32_t* offsets, int batch, int H, int nq, int causal, int n_cta, std::vector<int32_t>* units,
              std::vector<int32_t>* cta_start);
+// The same under a window: query i sees keys [i - left, i + right] of its
+// sequence (a negative bound leaves its side open; causal is (-1, 0)).
+int plan_fwd_window(const int32_t* offsets, int batch, int H, int nq, int left, int right, int n_cta,
+                    std::vector<int32_t>* units, std::vector<int32_t>* cta_start);
+int plan_bwd_window(const int32_t* offsets, int batch, int H, int nq, int left, int right, int n_cta,
+                    std::vector<int32_t>* units, std::vector<int32_t>* cta_start);
+// Block-sparse forward: the forward's units, each costing the blocks it visits
+// (min(topk, key blocks of its sequence)).
+int plan_fwd_topk(const int32_t* offsets, int batch, int H, int nq, int topk, int n_cta, std::vector<int32_t>* units,
+                  std::vector<int32_t>* cta_start);
 // Returns the number of programs P.
 int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<int32_t>* bpb,
                std::vector<int32_t>* prog_start);

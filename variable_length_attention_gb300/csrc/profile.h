@@ -13,7 +13,8 @@ enum KernelKind : int {
   kKindBlockFwd = 4,
   kKindBlockBwd = 5,
   kKindFill = 6,
-  kNumKernelKinds = 7
+  kKindTopk = 7,
+  kNumKernelKinds = 8
 };
 
 class ProfileScope {

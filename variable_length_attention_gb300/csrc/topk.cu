@@ -1,0 +1,167 @@
+// topk.cu -- first stage of the block-sparse forward: block means and the
+// top-k key blocks of every query block.
+//
+// The aixai.ru summary ("MXFP8 and sparsity") describes a two-stage variant for
+// long histories: a cheap kernel averages blocks of Q and K and picks the top-k
+// most relevant key blocks, and the attention kernel then attends over those
+// blocks only.  Here a query block is 256 rows (the forward kernel's unit: its
+// two 128-row tiles share every K/V block they load) and a key block is 128 keys
+// (the forward's K/V block); a block's mean is over the rows it really has; the
+// score of (query block, key block) is mean query . mean key, with key/value
+// head h / (H / Hkv); the k highest scores win, ties to the lower block index.
+//
+// Kernels, in launch order:
+//   block_mean_kernel  one warp per block: the fp32 mean of its rows (query
+//                      blocks of every head, then key blocks of every key/value
+//                      head), rows read once, 16 bytes per lane
+//   select_kernel      one warp per query block: the scores against every key
+//                      block of its sequence, then k rounds of a warp arg-max;
+//                      the chosen block indices are written in ascending order,
+//                      -1 after the last one
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "host.h"
+#include "profile.h"
+#include "ptx.cuh"
+#include "topk.h"
+
+namespace jfa {
+namespace topk {
+
+// One block of rows to average: rows [row0, row0 + n) of head `head` in a
+// [rows, heads, D] tensor; the mean goes to out[D].
+struct MeanTask {
+  int row0, n, head, tensor;  // tensor 0: q, 1: k
+};
+
+template <int D>
+__global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int H,
+                                  int Hkv, const int4* __restrict__ tasks, int n_tasks, float* __restrict__ out) {
+  constexpr int PER = D / 32;  // columns per lane: 4 (D = 128) or 2 (D = 64)
+  const int lane = threadIdx.x & 31;
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (w >= n_tasks) return;
+  const int4 t = tasks[w];
+  const __nv_bfloat16* base = t.w == 0 ? q : k;
+  const int heads = t.w == 0 ? H : Hkv;
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int r = 0; r < t.y; ++r) {
+    const __nv_bfloat16* row = base + (static_cast<size_t>(t.x + r) * heads + t.z) * D + lane * PER;
+    if constexpr (PER == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(row);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      acc[0] += a.x;
+      acc[1] += a.y;
+      acc[2] += b.x;
+      acc[3] += b.y;
+    } else {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(row));
+      acc[0] += a.x;
+      acc[1] += a.y;
+    }
+  }
+  const float inv = t.y > 0 ? 1.0f / static_cast<float>(t.y) : 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) out[static_cast<size_t>(w) * D + lane * PER + e] = acc[e] * inv;
+}
+
+// One query block: its mean (row `qmean` of the means), the first key-block
+// mean of its sequence and key/value head, and how many key blocks there are.
+template <int D>
+__global__ void select_kernel(const float* __restrict__ means, const int4* __restrict__ sel_tasks, int n_units,
+                              int topk, int nk_max, int32_t* __restrict__ selection) {
+  extern __shared__ float s_scores[];  // [warps][nk_max]
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (u >= n_units) return;
+  const int4 t = sel_tasks[u];  // x: row of the query mean, y: row of the first key mean, z: key blocks
+  float* sc = s_scores + wib * nk_max;
+  constexpr int PER = D / 32;
+  float qm[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) qm[e] = means[static_cast<size_t>(t.x) * D + lane * PER + e];
+  for (int n = 0; n < t.z; ++n) {
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) d = fmaf(qm[e], means[static_cast<size_t>(t.y + n) * D + lane * PER + e], d);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) sc[n] = d;
+  }
+  __syncwarp();
+  // k rounds of arg-max (ties to the lower index); chosen blocks are marked
+  // with -inf, and a score is never -inf otherwise (finite inputs)
+  const int cnt = min(topk, t.z);
+  for (int round = 0; round < cnt; ++round) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int n = lane; n < t.z; n += 32) {
+      const float v = sc[n];
+      if (v > best || (v == best && n < bi)) {
+        best = v;
+        bi = n;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) sc[bi] = -INFINITY;
+    __syncwarp();
+  }
+  // the chosen blocks in ascending order, then -1
+  int32_t* out = selection + static_cast<size_t>(u) * topk;
+  int written = 0;
+  for (int n0 = 0; n0 < t.z; n0 += 32) {
+    const int n = n0 + lane;
+    const bool chosen = n < t.z && sc[n] == -INFINITY;
+    const uint32_t mask = __ballot_sync(0xffffffffu, chosen);
+    if (chosen) out[written + __popc(mask & ((1u << lane) - 1u))] = n;
+    written += __popc(mask);
+  }
+  for (int i = written + lane; i < topk; i += 32) out[i] = -1;
+}
+
+}  // namespace topk
+
+int launch_topk_select(const TopkArgs& a) {
+  if (a.n_tasks == 0) return JFA_OK;
+  const int threads = 256;
+  {
+    const int blocks = static_cast<int>((static_cast<long>(a.n_tasks) * 32 + threads - 1) / threads);
+    ProfileScope prof(kKindTopk, a.stream);
+    if (a.D == 128)
+      topk::block_mean_kernel<128><<<blocks, threads, 0, a.stream>>>(
+          static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.H, a.Hkv, a.mean_tasks,
+          a.n_tasks, a.means);
+    else
+      topk::block_mean_kernel<64><<<blocks, threads, 0, a.stream>>>(
+          static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.H, a.Hkv, a.mean_tasks,
+          a.n_tasks, a.means);
+    if (cudaGetLastError() != cudaSuccess) return JFA_ERR_CUDA;
+  }
+  if (a.n_units == 0) return JFA_OK;
+  const int sel_threads = 128;  // 4 warps, nk_max scores each
+  const size_t smem = static_cast<size_t>(sel_threads / 32) * a.nk_max * sizeof(float);
+  const int blocks = static_cast<int>((static_cast<long>(a.n_units) * 32 + sel_threads - 1) / sel_threads);
+  ProfileScope prof(kKindTopk, a.stream);
+  if (a.D == 128)
+    topk::select_kernel<128><<<blocks, sel_threads, smem, a.stream>>>(a.means, a.sel_tasks, a.n_units, a.topk,
+                                                                     a.nk_max, a.selection);
+  else
+    topk::select_kernel<64><<<blocks, sel_threads, smem, a.stream>>>(a.means, a.sel_tasks, a.n_units, a.topk,
+                                                                    a.nk_max, a.selection);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // namespace jfa

@@ -20,7 +20,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libjfa.so")
 
-JFA_OP_FWD, JFA_OP_BWD, JFA_OP_BLOCK_FWD, JFA_OP_BLOCK_BWD = 0, 1, 2, 3
+JFA_OP_FWD, JFA_OP_BWD, JFA_OP_BLOCK_FWD, JFA_OP_BLOCK_BWD, JFA_OP_TOPK_SELECT, JFA_OP_FWD_TOPK = 0, 1, 2, 3, 4, 5
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_BAD_OFFSETS",
           4: "JFA_ERR_WORKSPACE_TOO_SMALL", 5: "JFA_ERR_ARCH", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT",
           8: "JFA_ERR_TOO_LARGE"}
@@ -30,8 +30,18 @@ _P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "jfa_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S, _P]),
     "jfa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S, _P]),
+    "jfa_fwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S, _P]),
+    "jfa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _S,
+                            _P]),
+    "jfa_plan_window": (_I, [_I, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "jfa_topk_rows": (_I, [_P, _I, _I, _I, _I]),
+    "jfa_topk_select": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _S, _P]),
+    "jfa_fwd_topk": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "block_attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _S, _P]),
     "block_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "block_attn_fwd_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "block_attn_bwd_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _F, _P, _S,
+                                 _P]),
     "jfa_workspace_size": (_S, [_I, _P, _I, _I, _I, _I, _I, _I]),
     "jfa_status_string": (ctypes.c_char_p, [_I]),
     "jfa_device_status": (_I, [_P, _P]),
@@ -46,13 +56,15 @@ SIGNATURES = {
     "jfa_get_schedule": (_I, []),
     "jfa_set_bwd_schedule": (_I, [_I]),
     "jfa_get_bwd_schedule": (_I, []),
+    "jfa_set_block_schedule": (_I, [_I]),
+    "jfa_get_block_schedule": (_I, []),
     "jfa_profile_enable": (_I, [_I]),
     "jfa_selftest_wait_timeout": (_I, [_P, _S, _P]),
     "jfa_profile_select": (_I, [_I]),
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
 KERNEL_KINDS = {"fwd": 0, "bwd_prep": 1, "bwd_main": 2, "dq_convert": 3, "block_fwd": 4, "block_bwd": 5,
-                "fill": 6}
+                "fill": 6, "topk_select": 7}
 
 _lock = threading.Lock()
 _lib = None
@@ -188,10 +200,18 @@ def jfa_device_status(workspace) -> int:
     return load().jfa_device_status(_ptr(workspace), _stream())
 
 
+def _window_args(window):
+    """(left, right) of a sliding window; None or a negative side is open (-1)."""
+    left, right = window
+    return (-1 if left is None or left < 0 else int(left)), (-1 if right is None or right < 0 else int(right))
+
+
 @_on_tensor_device
 def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False, scale=None,
-            out=None, lse=None, return_lse=True, workspace=None):
-    """Forward.  Returns (o, lse); lse is None if return_lse is False."""
+            out=None, lse=None, return_lse=True, workspace=None, window=None):
+    """Forward.  Returns (o, lse); lse is None if return_lse is False.
+    ``window=(left, right)``: query i sees keys i-left .. i+right of its
+    sequence (jfa_fwd_window; self-attention; causal closes the right side)."""
     L = load()
     offs_h = _host_offsets(offsets, offsets_host)
     batch = len(offs_h) - 1
@@ -211,6 +231,17 @@ def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0
         lse = None
     _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
     workspace = _workspace(JFA_OP_FWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    if window is not None:
+        if bq:
+            raise ValueError("a window applies to self-attention only")
+        wl, wr = _window_args(window)
+        if causal:
+            wr = 0 if wr < 0 else min(wr, 0)
+        st = L.jfa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets), offs_h.ctypes.data,
+                              batch, int(max_len), H, Hkv, D, float(scale), wl, wr, workspace.data_ptr(),
+                              workspace.nbytes, _stream())
+        _check("jfa_fwd_window", st)
+        return out, lse
     st = L.jfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(offsets),
                    offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast), H, Hkv, D,
                    float(scale), int(causal), int(bq), workspace.data_ptr(), workspace.nbytes, _stream())
@@ -220,8 +251,8 @@ def jfa_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0
 
 @_on_tensor_device
 def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, nq_broadcast=0, causal=False,
-            scale=None, dq=None, dk=None, dv=None, workspace=None):
-    """Backward.  Returns (dq, dk, dv)."""
+            scale=None, dq=None, dk=None, dv=None, workspace=None, window=None):
+    """Backward.  Returns (dq, dk, dv).  ``window`` as in jfa_fwd."""
     L = load()
     offs_h = _host_offsets(offsets, offsets_host)
     batch = len(offs_h) - 1
@@ -237,6 +268,17 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, 
     dv = torch.empty_like(v) if dv is None else dv
     _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv)
     workspace = _workspace(JFA_OP_BWD, offs_h, batch, nq_broadcast, H, D, causal, bq, workspace, q.device)
+    if window is not None:
+        if bq:
+            raise ValueError("a window applies to self-attention only")
+        wl, wr = _window_args(window)
+        if causal:
+            wr = 0 if wr < 0 else min(wr, 0)
+        st = L.jfa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), H, Hkv, D,
+                              float(scale), wl, wr, workspace.data_ptr(), workspace.nbytes, _stream())
+        _check("jfa_bwd_window", st)
+        return dq, dk, dv
     st = L.jfa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                    _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast),
                    H, Hkv, D, float(scale), int(causal), int(bq), workspace.data_ptr(), workspace.nbytes, _stream())
@@ -244,9 +286,91 @@ def jfa_bwd(q, k, v, o, dout, lse, offsets, offsets_host=None, *, max_len=None, 
     return dq, dk, dv
 
 
+def _rope_tables(rope, D, device):
+    if rope is None:
+        return None
+    cos, sin = rope
+    for name, t in (("rope cos", cos), ("rope sin", sin)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2 or \
+                t.shape[1] != D // 2 or t.device != device:
+            raise ValueError(f"{name}: expected a contiguous float32 CUDA tensor [positions, {D // 2}] on {device}")
+    if cos.shape != sin.shape:
+        raise ValueError("rope cos and sin must have the same shape")
+    return cos, sin
+
+
+def jfa_topk_rows(offsets_host, num_heads, nq_broadcast=0) -> int:
+    """Query blocks (rows of a top-k selection) of a problem."""
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    n = load().jfa_topk_rows(h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, int(nq_broadcast), int(num_heads),
+                             int(nq_broadcast > 0))
+    if n < 0:
+        raise JfaError("jfa_topk_rows", -n)
+    return n
+
+
 @_on_tensor_device
-def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=None, out=None, workspace=None):
-    """Block-diagonal (64-token blocks) forward.  Returns o."""
+def jfa_topk_select(q, k, offsets, offsets_host=None, *, topk, max_len=None, nq_broadcast=0, selection=None,
+                    workspace=None):
+    """First stage of the block-sparse forward: int32 [query blocks, topk],
+    each row's chosen key blocks ascending, -1 padded."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    bq = nq_broadcast > 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    rows = jfa_topk_rows(offs_h, H, nq_broadcast)
+    if selection is None:
+        selection = torch.empty((rows, topk), dtype=torch.int32, device=q.device)
+    _expect("selection", selection, (rows, topk), torch.int32, device=q.device)
+    _check_problem(q, k, k, offsets, offs_h, nq_broadcast)
+    workspace = _workspace(JFA_OP_TOPK_SELECT, offs_h, batch, nq_broadcast, H, D, False, bq, workspace, q.device)
+    st = L.jfa_topk_select(_ptr(q), _ptr(k), _ptr(offsets), offs_h.ctypes.data, batch, int(max_len),
+                           int(nq_broadcast), H, Hkv, D, int(topk), int(bq), _ptr(selection), workspace.data_ptr(),
+                           workspace.nbytes, _stream())
+    _check("jfa_topk_select", st)
+    return selection
+
+
+@_on_tensor_device
+def jfa_fwd_topk(q, k, v, offsets, selection, offsets_host=None, *, topk, max_len=None, nq_broadcast=0, scale=None,
+                 out=None, lse=None, workspace=None):
+    """Second stage of the block-sparse forward: attention over each query
+    block's chosen key blocks.  Returns (o, lse)."""
+    L = load()
+    offs_h = _host_offsets(offsets, offsets_host)
+    batch = len(offs_h) - 1
+    bq = nq_broadcast > 0
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    if max_len is None:
+        max_len = int(np.max(np.diff(offs_h))) if batch > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o_rows = batch * nq_broadcast if bq else int(offs_h[-1])
+    if out is None:
+        out = torch.empty((o_rows, H, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, o_rows), dtype=torch.float32, device=q.device)
+    _expect("selection", selection, (jfa_topk_rows(offs_h, H, nq_broadcast), topk), torch.int32, device=q.device)
+    _check_problem(q, k, v, offsets, offs_h, nq_broadcast, o=out, lse=lse)
+    workspace = _workspace(JFA_OP_FWD_TOPK, offs_h, batch, nq_broadcast, H, D, False, bq, workspace, q.device)
+    st = L.jfa_fwd_topk(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(selection), int(topk), _ptr(offsets),
+                        offs_h.ctypes.data, batch, int(max_len), int(nq_broadcast), H, Hkv, D, float(scale), int(bq),
+                        workspace.data_ptr(), workspace.nbytes, _stream())
+    _check("jfa_fwd_topk", st)
+    return out, lse
+
+
+@_on_tensor_device
+def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=None, out=None, workspace=None,
+                   rope=None):
+    """Block-diagonal (64-token blocks) forward.  Returns o.  ``rope=(cos, sin)``
+    (fp32 [positions, D/2]) fuses the rotary embedding of q and k
+    (block_attn_fwd_rope)."""
     L = load()
     offs_h = _host_offsets(offsets, offsets_host)
     batch = len(offs_h) - 1
@@ -258,6 +382,13 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
     out = torch.empty_like(q) if out is None else out
     _check_problem(q, k, v, offsets, offs_h, 0, o=out)
     workspace = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    tables = _rope_tables(rope, D, q.device)
+    if tables is not None:
+        st = L.block_attn_fwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(tables[0]), _ptr(tables[1]),
+                                   tables[0].shape[0], _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), H, D,
+                                   float(scale), workspace.data_ptr(), workspace.nbytes, _stream())
+        _check("block_attn_fwd_rope", st)
+        return out
     st = L.block_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(offsets), offs_h.ctypes.data,
                           batch, int(max_len), H, D, float(scale), workspace.data_ptr(), workspace.nbytes, _stream())
     _check("block_attn_fwd", st)
@@ -266,8 +397,9 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
 
 @_on_tensor_device
 def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None, scale=None, dq=None, dk=None,
-                   dv=None, workspace=None):
-    """Block-diagonal backward.  Returns (dq, dk, dv)."""
+                   dv=None, workspace=None, rope=None):
+    """Block-diagonal backward.  Returns (dq, dk, dv); with ``rope`` (as in
+    block_attn_fwd) dq and dk are with respect to the unrotated q and k."""
     L = load()
     offs_h = _host_offsets(offsets, offsets_host)
     batch = len(offs_h) - 1
@@ -281,6 +413,14 @@ def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None
     dv = torch.empty_like(v) if dv is None else dv
     _check_problem(q, k, v, offsets, offs_h, 0, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
     workspace = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
+    tables = _rope_tables(rope, D, q.device)
+    if tables is not None:
+        st = L.block_attn_bwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                   _ptr(tables[0]), _ptr(tables[1]), tables[0].shape[0], _ptr(offsets),
+                                   offs_h.ctypes.data, batch, int(max_len), H, D, float(scale),
+                                   workspace.data_ptr(), workspace.nbytes, _stream())
+        _check("block_attn_bwd_rope", st)
+        return dq, dk, dv
     st = L.block_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                           _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), H, D,
                           float(scale), workspace.data_ptr(), workspace.nbytes, _stream())
@@ -311,6 +451,23 @@ def jfa_plan_fwd(offsets_host, num_heads, n_cta, *, nq=0, causal=False):
 def jfa_plan_bwd(offsets_host, num_heads, n_cta, *, nq=0, causal=False):
     """Host backward plan: (units int32[4n], cta_start int32[n_cta+1])."""
     return _plan("jfa_plan_bwd", offsets_host, num_heads, nq, causal, n_cta)
+
+
+def jfa_plan_window(which, offsets_host, num_heads, n_cta, window):
+    """Window planners (0 forward, 1 backward): (units int32[4n], cta_start
+    int32[n_cta+1])."""
+    L = load()
+    h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int32))
+    wl, wr = _window_args(window)
+    n = L.jfa_plan_window(which, h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, wl, wr, n_cta, None,
+                          None)
+    if n < 0:
+        raise JfaError("jfa_plan_window", -n)
+    units = np.zeros(4 * n, dtype=np.int32)
+    start = np.zeros(n_cta + 1, dtype=np.int32)
+    L.jfa_plan_window(which, h.ctypes.data_as(ctypes.c_void_p), len(h) - 1, num_heads, wl, wr, n_cta,
+                      units.ctypes.data_as(ctypes.c_void_p), start.ctypes.data_as(ctypes.c_void_p))
+    return units, start
 
 
 def block_plan(offsets_host, num_heads, n_sm):
@@ -347,6 +504,17 @@ def jfa_set_bwd_schedule(mode):
 
 def jfa_get_bwd_schedule() -> int:
     return load().jfa_get_bwd_schedule()
+
+
+def jfa_set_block_schedule(mode):
+    """Work distribution of the block-diagonal kernels: 0 / "static" (closed-form
+    ranges, one CTA per SM) or 1 / "clc" (Cluster Launch Control over chunks)."""
+    m = {"static": 0, "clc": 1}.get(mode, mode)
+    _check("jfa_set_block_schedule", load().jfa_set_block_schedule(int(m)))
+
+
+def jfa_get_block_schedule() -> int:
+    return load().jfa_get_block_schedule()
 
 
 @_on_tensor_device
