@@ -44,8 +44,12 @@ def _args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["jagged", "broadcast", "dense", "block"], default="jagged",
-                    help="jagged (default) is the headline step; the others are diagnostic lines")
+    ap.add_argument("--workload", choices=["jagged", "broadcast", "dense", "block", "window", "topk"],
+                    default="jagged", help="jagged (default) is the headline step; the others are diagnostic lines")
+    ap.add_argument("--window", type=int, default=1024,
+                    help="window: keys a query sees (a causal sliding window over the jagged workload)")
+    ap.add_argument("--topk", type=int, default=8, help="topk: key blocks of 128 each 256-row query block keeps")
+    ap.add_argument("--rope", action="store_true", help="block: with the rotary embedding fused")
     ap.add_argument("--block-batch", type=int, default=1152)
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--copy-streams", type=int, default=4,
@@ -337,16 +341,13 @@ def main():
     # separate passes afterwards
     V.jfa_profile_select([job["dominant"]])
     V.jfa_profile_enable(True)
-    host_enqueue = 0.0
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
         for i in range(args.steps):
             for r in range(passes):
                 flush.zero_()  # L2 flush between timed passes, outside the events
                 evs[i][r][0].record()
-                h0 = time.perf_counter()
                 step(job["dev_inputs"])
-                host_enqueue += time.perf_counter() - h0
                 evs[i][r][1].record()
         barrier()
     step_ms = [sum(a.elapsed_time(b) for a, b in row) for row in evs]
@@ -372,20 +373,31 @@ def main():
     breakdown = {kind: V.jfa_profile_read(kind) for kind in V.jfa.KERNEL_KINDS}
     V.jfa_profile_enable(False)
     calls = {}
+    # A ~1 ms spin kernel ahead of each timed call keeps the GPU busy while the
+    # host plans and enqueues it, so the events bracket the call's device work
+    # (its copies and kernels) and not the host's latency; the host time of
+    # the call is measured on its own.
+    spin = getattr(torch.cuda, "_sleep", None)
+    host_call = {}
     for c in job["calls"]:
-        ms_call, ms_main = [], []
+        ms_call, ms_main, ms_host = [], [], []
         for i in range(n_bd):
             flush.zero_()
             V.jfa_profile_select([c["main"]])
             V.jfa_profile_enable(True)
+            if spin is not None:
+                spin(2_000_000)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
+            h0 = time.perf_counter()
             c["run"](job["dev_inputs"])
+            ms_host.append((time.perf_counter() - h0) * 1e3)
             b.record()
             torch.cuda.synchronize()
             ms_call.append(a.elapsed_time(b))
             ms_main.append(V.jfa_profile_read(c["main"])[0])
             V.jfa_profile_enable(False)
+        host_call[c["name"]] = statistics.median(ms_host)
         mc, mm = statistics.median(ms_call), statistics.median(ms_main)
         ent = {"median_call_ms": mc, "median_kernel_ms": mm, "kernel": c["main"]}
         if job["bound"] == "tensor":
@@ -505,11 +517,14 @@ def main():
             "kernel_ms_note": f"per kind, summed over {n_bd} passes after the timed region",
             "calls": calls,
             "calls_note": f"each entry-point call of a pass alone, median of {n_bd} after an L2 flush: the whole "
-                          "call (CUDA events around it) and its main kernel (the library's events)",
+                          "call's device time (CUDA events around it, the GPU kept busy while the host enqueues "
+                          "it) and its main kernel (the library's events)",
             "host_plan_ms": plan_ms,
             "host_plan_note": "host planning of one pass (every planner call the pass's entry points make), "
                               "timed on the host; it overlaps the previous kernels",
-            "host_enqueue_ms_per_pass": host_enqueue * 1e3 / n_passes,
+            "host_call_ms": host_call,
+            "host_call_note": "host time of each entry-point call (Python binding, planning, enqueue) while the "
+                              "GPU is busy, median",
             "roofline": roofline, "clocks": clocks, "gpu_launches": int(sum(n for _, n in prof.values())),
             "e2e": e2e}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == "jagged":
@@ -613,6 +628,9 @@ def build_job(args, dev):
                 "host_inputs": host, "flops": flops, "bytes": {}, "dominant": "bwd_main", "bound": "tensor",
                 "config": cfg, "calls": calls, "plans": plans}
 
+    if args.workload in ("window", "topk"):
+        return build_sparse_job(args, dev)
+
     # block-diagonal: inputs drawn on the device (the full workload is 4.8 GB per tensor)
     w = W.block(args.head_dim, batch=args.block_batch)
     offs_h = w.offsets
@@ -629,25 +647,29 @@ def build_job(args, dev):
 
     new_slot()
 
-    def step(inp, slot=0):
-        q, k, v, do, offs = inp
-        o, grads, wsb = slots[slot]
-        V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=o, workspace=wsb)
-        V.block_attn_bwd(q, k, v, o, do, offs, offs_h, max_len=w.max_len, dq=grads[0], dk=grads[1], dv=grads[2],
-                         workspace=wsb)
 
     f, b = W.flops(w)
     t_bytes = dev_in[0].numel() * 2
 
+    rope = None
+    if args.rope:  # rotate-half tables, angle p * 10000^(-2i/D), fp32
+        ang = np.arange(w.max_len)[:, None] * 10000.0 ** (-2.0 * np.arange(w.head_dim // 2) / w.head_dim)[None, :]
+        rope = (torch.from_numpy(np.cos(ang)).float().to(dev), torch.from_numpy(np.sin(ang)).float().to(dev))
+
     def run_fwd(inp, slot=0):
         q, k, v, do, offs = inp
-        V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=slots[slot][0], workspace=slots[slot][2])
+        V.block_attn_fwd(q, k, v, offs, offs_h, max_len=w.max_len, out=slots[slot][0], workspace=slots[slot][2],
+                         rope=rope)
 
     def run_bwd(inp, slot=0):
         q, k, v, do, offs = inp
         o, grads, wsb = slots[slot]
         V.block_attn_bwd(q, k, v, o, do, offs, offs_h, max_len=w.max_len, dq=grads[0], dk=grads[1], dv=grads[2],
-                         workspace=wsb)
+                         workspace=wsb, rope=rope)
+
+    def step(inp, slot=0):
+        run_fwd(inp, slot)
+        run_bwd(inp, slot)
 
     calls = [{"name": "block_fwd", "run": run_fwd, "flops": float(f), "bytes": 4.0 * t_bytes, "main": "block_fwd"},
              {"name": "block_bwd", "run": run_bwd, "flops": float(b), "bytes": 7.0 * t_bytes, "main": "block_bwd"}]
@@ -659,8 +681,93 @@ def build_job(args, dev):
             "flops": {"block_fwd": float(f), "block_bwd": float(b)},
             "bytes": {"block_fwd": 4.0 * t_bytes, "block_bwd": 7.0 * t_bytes}, "dominant": "block_bwd",
             "bound": "hbm", "calls": calls, "plans": [],
-            "config": {"workload": w.name + " fwd+bwd", "batch": w.batch, "heads": w.num_heads,
-                       "head_dim": w.head_dim, "tokens": w.total_tokens, "block": 64}}
+            "config": {"workload": w.name + (" rotary" if args.rope else "") + " fwd+bwd", "batch": w.batch,
+                       "heads": w.num_heads, "head_dim": w.head_dim, "tokens": w.total_tokens, "block": 64}}
+
+
+
+def build_sparse_job(args, dev):
+    """Diagnostic lines on the jagged workload's inputs: a causal sliding window
+    (forward + backward over the pairs inside the window), or the two-stage
+    block-sparse forward (selection + attention over the chosen blocks)."""
+    import variable_length_attention_gb300 as V
+    from variable_length_attention_gb300 import workloads as W
+
+    w = W.jagged(False)
+    offs_h = w.offsets
+    host = [t.pin_memory() for t in w.tensors("cpu")] + [torch.from_numpy(offs_h.copy()).pin_memory()]
+    dev_in = [t.to(dev) for t in host]
+    o = torch.empty((w.o_rows, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.num_heads, w.o_rows), dtype=torch.float32, device=dev)
+    grads = [torch.empty_like(dev_in[i]) for i in range(3)]
+    if args.workload == "window":
+        left = args.window - 1
+        L = w.lengths.astype(np.int64)
+        pairs = sum(int(np.sum(np.minimum(np.arange(n) + 1, args.window))) for n in L) * w.num_heads
+        f = 4.0 * w.head_dim * pairs
+        wsb = torch.empty(max(V.jfa_workspace_size(0, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
+                              V.jfa_workspace_size(1, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0)),
+                          dtype=torch.uint8, device=dev)
+
+        def run_fwd(inp, slot=0):
+            V.jfa_fwd(inp[0], inp[1], inp[2], inp[-1], offs_h, max_len=w.max_len, window=(left, 0), out=o,
+                      lse=lse, workspace=wsb)
+
+        def run_bwd(inp, slot=0):
+            V.jfa_bwd(inp[0], inp[1], inp[2], o, inp[3], lse, inp[-1], offs_h, max_len=w.max_len, window=(left, 0),
+                      dq=grads[0], dk=grads[1], dv=grads[2], workspace=wsb)
+
+        calls = [{"name": "fwd_window", "run": run_fwd, "flops": f, "main": "fwd"},
+                 {"name": "bwd_window", "run": run_bwd, "flops": 2.5 * f, "main": "bwd_main"}]
+        flops = {"fwd": f, "bwd_main": 2.5 * f}
+        outputs = [o] + grads
+        cfg = {"workload": f"{w.name} causal sliding window of {args.window} keys fwd+bwd", "batch": w.batch,
+               "heads": w.num_heads, "head_dim": w.head_dim, "tokens": w.total_tokens, "window": args.window}
+        dominant = "bwd_main"
+    else:
+        k_sel = args.topk
+        rows = V.jfa_topk_rows(offs_h, w.num_heads)
+        sel = torch.empty((rows, k_sel), dtype=torch.int32, device=dev)
+        ws1 = torch.empty(V.jfa_workspace_size(4, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
+                          dtype=torch.uint8, device=dev)
+        ws2 = torch.empty(V.jfa_workspace_size(5, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
+                          dtype=torch.uint8, device=dev)
+        V.jfa_topk_select(dev_in[0], dev_in[1], dev_in[-1], offs_h, topk=k_sel, selection=sel, workspace=ws1)
+        # valid pairs: each query block's rows times the keys of its chosen blocks
+        chosen = sel.cpu().numpy()
+        pairs, u = 0, 0
+        for b in range(w.batch):
+            L = int(w.lengths[b])
+            for _h in range(w.num_heads):
+                for m in range(-(-L // 256)):
+                    nrow = min(256, L - 256 * m)
+                    keys = sum(min(128, L - 128 * int(j)) for j in chosen[u] if j >= 0)
+                    pairs += nrow * keys
+                    u += 1
+        f = 4.0 * w.head_dim * pairs
+
+        def run_select(inp, slot=0):
+            V.jfa_topk_select(inp[0], inp[1], inp[-1], offs_h, topk=k_sel, selection=sel, workspace=ws1)
+
+        def run_fwd(inp, slot=0):
+            V.jfa_fwd_topk(inp[0], inp[1], inp[2], inp[-1], sel, offs_h, topk=k_sel, out=o, lse=lse, workspace=ws2)
+
+        calls = [{"name": "topk_select", "run": run_select, "flops": 0.0, "main": "topk_select"},
+                 {"name": "fwd_topk", "run": run_fwd, "flops": f, "main": "fwd"}]
+        flops = {"fwd": f}
+        outputs = [o]
+        cfg = {"workload": f"{w.name} block-sparse top-{k_sel} of 128-key blocks per 256-row query block, fwd "
+                           "(selection + attention)", "batch": w.batch, "heads": w.num_heads,
+               "head_dim": w.head_dim, "tokens": w.total_tokens, "topk": k_sel}
+        dominant = "fwd"
+
+    def step(inp, slot=0):
+        for c in calls:
+            c["run"](inp, slot)
+
+    return {"step": step, "new_slot": lambda: 0, "outputs": lambda slot: outputs, "dev_inputs": dev_in,
+            "host_inputs": None, "flops": flops, "bytes": {}, "dominant": dominant, "bound": "tensor",
+            "config": cfg, "calls": calls, "plans": []}
 
 
 if __name__ == "__main__":
