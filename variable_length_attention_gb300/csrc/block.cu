@@ -483,20 +483,31 @@ done:
 // share one buffer (dS is written once the dV GEMM has read P).
 template <int D>
 struct BwdCfg {
+  // D = 64 runs a separate epilogue warpgroup (warps 8-11) on accumulators of
+  // their own in TMEM, so one tile's stores overlap the next tile's GEMMs and
+  // softmax; at D = 128 the accumulators share TMEM with S and dP (no room for
+  // both) and the softmax warps run the epilogue themselves.
+  static constexpr bool SPLIT = D == 64;
+  static constexpr int THREADS = SPLIT ? 384 : 256;
   static constexpr int TILE = 128 * D * 2;
   static constexpr int CHUNK = 128 * 128;
-  static constexpr int NQK = 2;
-  static constexpr int OFF_V = NQK * 2 * TILE;
-  static constexpr int OFF_DO = OFF_V + TILE;
-  static constexpr int OFF_PDS = OFF_DO + TILE;     // P, then dS: [128 q][128 keys] bf16
+  static constexpr int NQK = SPLIT ? 3 : 2;         // Q,K slots
+  static constexpr int NVD = SPLIT ? 2 : 1;         // V,dO slots
+  static constexpr int OFF_V = NQK * 2 * TILE;      // slot s: V at OFF_V + 2 s TILE, dO one TILE later
+  static constexpr int OFF_PDS = OFF_V + NVD * 2 * TILE;  // P, then dS: [128 q][128 keys] bf16
   static constexpr int OFF_BAR = OFF_PDS + 32768;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  // TMEM columns: S [0,128), dP [128,256), dV [256, 256+D); dK and dQ go into
+  // the dP and S columns (D = 128) or after dV (D = 64)
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256;
+  static constexpr uint32_t COL_DK = SPLIT ? 256 + D : COL_DP, COL_DQ = SPLIT ? 256 + 2 * D : COL_S;
+  static constexpr int SCHED_CONSUMERS = SPLIT ? 9 : 5;  // the MMA thread and the 4 (or 8) consumer warps
 };
 
 struct BwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
-  uint64_t qk_full[2], qk_empty[2], vdo_full, vdo_empty;
-  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
+  uint64_t qk_full[3], qk_empty[3], vdo_full[2], vdo_empty[2];
+  uint64_t qk_rot[3];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
   uint64_t drain;
@@ -505,7 +516,6 @@ struct BwdBars {
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr int kBwdSchedConsumers = 5;  // the MMA thread and the 4 softmax / dS / epilogue warps
 
 // Row q of a [128][128] bf16 tile stored as two swizzled 64-column boxes:
 // 16-byte piece j (columns 8j..8j+7) of box c.
@@ -516,7 +526,7 @@ __device__ __forceinline__ void st_row_piece(uint8_t* tile, int q, int c, int j,
 }
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
@@ -527,13 +537,12 @@ __global__ void __launch_bounds__(256, 1)
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
   static_assert(sizeof(BwdBars) <= 512, "barrier block");
   const int warp = warp_id(), lane = lane_id();
-  // TMEM columns: S (then dQ) [0,128), dP (then dK) [128,256), dV [256, 256+D)
-  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256;
+  constexpr uint32_t COL_S = C::COL_S, COL_DP = C::COL_DP, COL_DV = C::COL_DV, COL_DK = C::COL_DK, COL_DQ = C::COL_DQ;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->sched_full[s], 1);
-      mbar_init(&bars->sched_empty[s], kBwdSchedConsumers);
+      mbar_init(&bars->sched_empty[s], C::SCHED_CONSUMERS);
     }
     mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
@@ -541,8 +550,10 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&bars->qk_empty[s], 1);
       mbar_init(&bars->qk_rot[s], 4);
     }
-    mbar_init(&bars->vdo_full, 1);
-    mbar_init(&bars->vdo_empty, 1);
+    for (int s = 0; s < C::NVD; ++s) {
+      mbar_init(&bars->vdo_full[s], 1);
+      mbar_init(&bars->vdo_empty[s], 1);
+    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_used, 1);
@@ -600,15 +611,17 @@ __global__ void __launch_bounds__(256, 1)
       return true;
     };
     auto load_vdo = [&](int i, int t) -> bool {
-      if (!mbar_wait(&bars->vdo_empty, (i & 1) ^ 1, ab)) return false;
+      const int sv = i % C::NVD;
+      if (!mbar_wait(&bars->vdo_empty[sv], ((i / C::NVD) & 1) ^ 1, ab)) return false;
       Blk a, b;
       int h;
       rows(t, a, b, h);
-      mbar_expect_tx(&bars->vdo_full, 2 * C::TILE);
-      load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 0, h, a.row0);
-      load_half<D>(&tm_v, &bars->vdo_full, smem + C::OFF_V, 1, h, b.row0);
-      load_half<D>(&tm_do, &bars->vdo_full, smem + C::OFF_DO, 0, h, a.row0);
-      load_half<D>(&tm_do, &bars->vdo_full, smem + C::OFF_DO, 1, h, b.row0);
+      uint8_t* base = smem + C::OFF_V + sv * 2 * C::TILE;
+      mbar_expect_tx(&bars->vdo_full[sv], 2 * C::TILE);
+      load_half<D>(&tm_v, &bars->vdo_full[sv], base, 0, h, a.row0);
+      load_half<D>(&tm_v, &bars->vdo_full[sv], base, 1, h, b.row0);
+      load_half<D>(&tm_do, &bars->vdo_full[sv], base + C::TILE, 0, h, a.row0);
+      load_half<D>(&tm_do, &bars->vdo_full[sv], base + C::TILE, 1, h, b.row0);
       return true;
     };
     int cur = p.use_clc ? static_cast<int>(blockIdx.x) : 0;
@@ -629,14 +642,17 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t id_kv = idesc_bf16(128, D, 1, 1);    // dV = P^T dO, dK = dS^T Q
     const uint32_t id_q = idesc_bf16(128, D, 0, 1);     // dQ = dS K
     const uint32_t sP = smem_u32(smem + C::OFF_PDS), sDS = sP;
-    const uint32_t v = smem_u32(smem + C::OFF_V), dO = smem_u32(smem + C::OFF_DO);
     TileCursor cur;
     for (int i = 0;; ++i) {
       if (next_tile(cur, bars, p, ab, false) < 0) break;
-      const int st = i % C::NQK;
+      const int st = i % C::NQK, sv = i % C::NVD;
       const uint32_t q = smem_u32(smem + st * 2 * C::TILE), k = q + C::TILE;
+      const uint32_t v = smem_u32(smem + C::OFF_V + sv * 2 * C::TILE), dO = v + C::TILE;
       if (!mbar_wait(ROPE ? &bars->qk_rot[st] : &bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
-      if (!mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
+      // S and dP reuse their columns once the softmax warps have read the
+      // previous tile's (p_full and ds_full, waited below for that tile); with
+      // the accumulators in the same columns, the epilogue must also be done
+      if (!C::SPLIT && !mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -644,7 +660,7 @@ __global__ void __launch_bounds__(256, 1)
         mma_ss(tmem + COL_S, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_s, kk > 0);
       }
       mma_commit(&bars->s_full);
-      if (!mbar_wait(&bars->vdo_full, i & 1, ab)) break;
+      if (!mbar_wait(&bars->vdo_full[sv], (i / C::NVD) & 1, ab)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -654,24 +670,26 @@ __global__ void __launch_bounds__(256, 1)
       mma_commit(&bars->dp_full);
       // dV = P^T dO: A = P^T (P stored query-major: MN-major), B = dO (MN-major)
       if (!mbar_wait(&bars->p_full, i & 1, ab)) break;
+      // separate accumulators: the previous tile's epilogue has read them out
+      if (C::SPLIT && !mbar_wait(&bars->t_free, (i & 1) ^ 1, ab)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tmem + COL_DV, sdesc_sw128(sP + kk * 2048, C::CHUNK, 1024), sdesc_sw128(dO + kk * 2048, C::CHUNK, 1024),
                id_kv, kk > 0);
-      mma_commit(&bars->vdo_empty);  // V and dO are read: the next tile's may load
+      mma_commit(&bars->vdo_empty[sv]);  // V and dO are read: the slot may load again
       mma_commit(&bars->p_used);     // P is read: the dS phase may overwrite it
-      // dK = dS^T Q into the dP columns, dQ = dS K into the S columns
+      // dK = dS^T Q, dQ = dS K
       if (!mbar_wait(&bars->ds_full, i & 1, ab)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + COL_DP, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(q + kk * 2048, C::CHUNK, 1024),
+        mma_ss(tmem + COL_DK, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024), sdesc_sw128(q + kk * 2048, C::CHUNK, 1024),
                id_kv, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-        mma_ss(tmem + COL_S, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(k + kk * 2048, C::CHUNK, 1024), id_q,
+        mma_ss(tmem + COL_DQ, sdesc_sw128(sDS + off, 16, 1024), sdesc_sw128(k + kk * 2048, C::CHUNK, 1024), id_q,
                kk > 0);
       }
       mma_commit(&bars->acc_full);
@@ -681,8 +699,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint64_t tw = global_timer_ns();
     while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
     }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------------- softmax, dS, epilogue
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------------- softmax, dS (and the epilogue at D = 128)
     const int r = threadIdx.x & 127;
     const int half = r >> 6, rr = r & 63;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -739,7 +757,10 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) pr[c] *= inv_l;
       }
-      // P row into shared memory (zeros in the other block's columns)
+      // P row into shared memory (zeros in the other block's columns); with the
+      // separate epilogue the buffer still holds the previous tile's dS until its
+      // dK and dQ GEMMs are done
+      if (C::SPLIT && i > 0 && !mbar_wait(&bars->acc_full, (i - 1) & 1, ab)) goto done;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint32_t w[4];
@@ -900,79 +921,92 @@ __global__ void __launch_bounds__(256, 1)
           if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
           stg_free_ph ^= 1;
         }
-      } else {
-        // epilogue (D=64): row r is query r for dQ and key r for dK, dV; each thread
-        // writes its rows directly (at this head size the staged path measured slower)
-        if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
-        tc_fence_after();
-        {
-          const bool valid = rr < blk.len;
-          const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
-  #pragma unroll 1
-          for (int which = 0; which < 3; ++which) {
-            const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
-            const float mul = which == 2 ? 1.0f : p.scale;
-            __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
-            // columns c..c+31 of the result row, as fp32, stored
-            auto put = [&](int c, const float* f) {
-              if (!valid) return;
-              uint32_t w[16];
-  #pragma unroll
-              for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
-  #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-            };
-            if (ROPE && which < 2) {
-              // dQ and dK of the rotated rows go back through the transposed
-              // rotation: columns c and c + 32 form the pairs
-              uint32_t v1[32], v2[32];
-              tmem_ld32(tmem + lane_addr + col, v1);
-              tmem_ld32(tmem + lane_addr + col + 32, v2);
-              tmem_wait_ld();
-              reg_fence<32>(v1);
-              reg_fence<32>(v2);
-              float f1[32], f2[32];
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                f1[e] = __uint_as_float(v1[e]) * mul;
-                f2[e] = __uint_as_float(v2[e]) * mul;
-              }
-              if (valid) {
-                const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
-  #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                  const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
-                  const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
-                  rope_back(f1[e], f2[e], cs.x, sn.x);
-                  rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
-                  rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
-                  rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
-                }
-              }
-              put(0, f1);
-              put(32, f2);
-            } else {
-  #pragma unroll 1
-              for (int c = 0; c < D; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + col + c, v);
-                tmem_wait_ld();
-                reg_fence<32>(v);
-                float f[32];
-  #pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
-                put(c, f);
-              }
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->t_free);
-        }
       }
     }
     if (threadIdx.x == 128) bulk_wait_all();  // every store has landed before the CTA exits
+  } else if (C::SPLIT && warp >= 8) {
+    // ---------------------------------------------------------------- epilogue (D = 64)
+    // Row r is query r for dQ and key r for dK, dV (same block, same token); each
+    // thread writes its rows directly (at this head size the staged path measured
+    // slower), while the softmax warps already work on the next tile.
+    const int r = threadIdx.x & 127;
+    const int half = r >> 6, rr = r & 63;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    TileCursor cur;
+    for (int i = 0;; ++i) {
+      const int t = next_tile(cur, bars, p, ab, true);
+      if (t == -2) goto done;
+      if (t < 0) break;
+      const int pair = t / p.H, h = t % p.H;
+      const Blk blk = locate(p, 2 * pair + half);
+      if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
+      tc_fence_after();
+      {
+        const bool valid = rr < blk.len;
+        const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+#pragma unroll 1
+        for (int which = 0; which < 3; ++which) {
+          const uint32_t col = which == 0 ? COL_DQ : (which == 1 ? COL_DK : COL_DV);
+          const float mul = which == 2 ? 1.0f : p.scale;
+          __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+          // columns c..c+31 of the result row, as fp32, stored
+          auto put = [&](int c, const float* f) {
+            if (!valid) return;
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          };
+          if (ROPE && which < 2) {
+            // dQ and dK of the rotated rows go back through the transposed
+            // rotation: columns c and c + 32 form the pairs
+            uint32_t v1[32], v2[32];
+            tmem_ld32(tmem + lane_addr + col, v1);
+            tmem_ld32(tmem + lane_addr + col + 32, v2);
+            tmem_wait_ld();
+            reg_fence<32>(v1);
+            reg_fence<32>(v2);
+            float f1[32], f2[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              f1[e] = __uint_as_float(v1[e]) * mul;
+              f2[e] = __uint_as_float(v2[e]) * mul;
+            }
+            if (valid) {
+              const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
+                const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
+                rope_back(f1[e], f2[e], cs.x, sn.x);
+                rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
+                rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
+                rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
+              }
+            }
+            put(0, f1);
+            put(32, f2);
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_addr + col + c, v);
+              tmem_wait_ld();
+              reg_fence<32>(v);
+              float f[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+              put(c, f);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->t_free);
+      }
+    }
   }
 done:
   __syncwarp();
@@ -1065,8 +1099,8 @@ int launch_bwd_impl(const BlockArgs& a) {
   p.rope_cos = a.rope_cos;
   p.rope_sin = a.rope_sin;
   ProfileScope prof(kKindBlockBwd, a.stream);
-  block_bwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 256, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq,
-                                                                                             tdk, tdv, p);
+  block_bwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, C::THREADS, C::SMEM, a.stream>>>(
+      tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

@@ -55,6 +55,25 @@ int make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Launches `kernel` on `stream` as a programmatic dependent of the previous
+// kernel there: it may be scheduled while that one finishes and must call
+// griddepcontrol.wait before it reads the previous kernel's results.
+template <class... KArgs, class... Args>
+int launch_dependent(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
 // Which keys a query row sees inside its sequence: all of them, those up to
 // the row (causal), or those within [row - win_left, row + win_right] (a
 // sliding window; a negative bound leaves its side open).

@@ -317,6 +317,14 @@ __device__ __forceinline__ int sched_pop(Bars* bars, uint32_t it, const Abort& a
   return ui;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// launch (it waits in griddep_wait for this grid to finish), and wait for the
+// previous kernel's grid to finish and its memory to be visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
