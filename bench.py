@@ -513,6 +513,13 @@ def main():
                            "timed region lasts long enough for the clock samples",
             "pct_of_peak": value / ws / peaks["bf16_tflops"] * 100.0,
             "kernel_tflops": per_kind,
+            "kernel_frac_by_call": ({n: e["kernel_tflops"] / peaks["bf16_tflops"] for n, e in calls.items()
+                                     if e.get("kernel_tflops")} if job["bound"] == "tensor" else
+                                    {n: e["kernel_gbs"] / peaks["hbm_gbs"] for n, e in calls.items()
+                                     if e.get("kernel_gbs")}),
+            "kernel_frac_note": "each entry point's main kernel (the 'calls' entries: non-causal and causal "
+                                "separately) as a fraction of the measured bf16 burst peak (HBM copy peak for "
+                                "the block kernels)",
             "kernel_ms": {k: v for k, v in kind_ms.items() if v > 0},
             "kernel_ms_note": f"per kind, summed over {n_bd} passes after the timed region",
             "calls": calls,

@@ -48,20 +48,34 @@ __global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __n
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int r = 0; r < t.y; ++r) {
-    const __nv_bfloat16* row = base + (static_cast<size_t>(t.x + r) * heads + t.z) * D + lane * PER;
-    if constexpr (PER == 4) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(row);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+  // eight rows' loads in flight at a time (a block is up to 256 rows, so one
+  // row at a time would leave the warp waiting on memory latency)
+  constexpr int U = 8;
+  const size_t stride = static_cast<size_t>(heads) * D;
+  const __nv_bfloat16* row0 = base + (static_cast<size_t>(t.x) * heads + t.z) * D + lane * PER;
+  for (int r0 = 0; r0 < t.y; r0 += U) {
+    uint2 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      raw[u] = make_uint2(0u, 0u);  // bf16 zeros past the block's end
+      if (r0 + u < t.y) {
+        const __nv_bfloat16* row = row0 + static_cast<size_t>(r0 + u) * stride;
+        if constexpr (PER == 4)
+          raw[u] = *reinterpret_cast<const uint2*>(row);
+        else
+          raw[u].x = *reinterpret_cast<const uint32_t*>(row);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
       acc[0] += a.x;
       acc[1] += a.y;
-      acc[2] += b.x;
-      acc[3] += b.y;
-    } else {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(row));
-      acc[0] += a.x;
-      acc[1] += a.y;
+      if constexpr (PER == 4) {
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
+        acc[2] += b.x;
+        acc[3] += b.y;
+      }
     }
   }
   const float inv = t.y > 0 ? 1.0f / static_cast<float>(t.y) : 0.f;
@@ -84,13 +98,24 @@ __global__ void select_kernel(const float* __restrict__ means, const int4* __res
   float qm[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) qm[e] = means[static_cast<size_t>(t.x) * D + lane * PER + e];
-  for (int n = 0; n < t.z; ++n) {
-    float d = 0.f;
+  // eight key blocks' means loaded at a time, then their dot products
+  constexpr int U = 8;
+  for (int n0 = 0; n0 < t.z; n0 += U) {
+    float km[U][PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) d = fmaf(qm[e], means[static_cast<size_t>(t.y + n) * D + lane * PER + e], d);
+    for (int u = 0; u < U; ++u)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    if (lane == 0) sc[n] = d;
+      for (int e = 0; e < PER; ++e)
+        km[u][e] = n0 + u < t.z ? means[static_cast<size_t>(t.y + n0 + u) * D + lane * PER + e] : 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) d = fmaf(qm[e], km[u][e], d);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (lane == 0 && n0 + u < t.z) sc[n0 + u] = d;
+    }
   }
   __syncwarp();
   // k rounds of arg-max (ties to the lower index); chosen blocks are marked
