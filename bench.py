@@ -647,8 +647,9 @@ def build_job(args, dev):
     def new_slot():
         o = torch.empty_like(dev_in[0])
         grads = [torch.empty_like(dev_in[i]) for i in range(3)]
-        wsb = torch.empty(V.jfa_workspace_size(2, offs_h, w.batch, 0, w.num_heads, w.head_dim, 0, 0),
-                          dtype=torch.uint8, device=dev)
+        # the rotary variants also hold rotated copies of q and k (op 6 instead of 2)
+        wsb = torch.empty(V.jfa_workspace_size(6 if args.rope else 2, offs_h, w.batch, 0, w.num_heads, w.head_dim,
+                                               0, 0), dtype=torch.uint8, device=dev)
         slots.append((o, grads, wsb))
         return len(slots) - 1
 

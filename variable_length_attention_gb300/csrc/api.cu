@@ -17,6 +17,7 @@
 #include "host.h"
 #include "plan.h"
 #include "profile.h"
+#include "rope.h"
 #include "topk.h"
 
 namespace jfa {
@@ -226,13 +227,16 @@ static BwdLayout bwd_layout(int n_units, int n_cta, int q_rows, int o_rows, int 
 }
 
 struct BlockLayout {
-  size_t err = 0, bpb = 0, prog = 0, total = 0;
+  size_t err = 0, bpb = 0, prog = 0, rot = 0, total = 0;
 };
-static BlockLayout block_layout(int batch, int n_prog) {
+// rot_bytes: the rotary variants' rotated copies of q and k (two tensors of that
+// many bytes each), else 0
+static BlockLayout block_layout(int batch, int n_prog, size_t rot_bytes = 0) {
   BlockLayout l;
   l.bpb = 256;
   l.prog = l.bpb + align256(static_cast<size_t>(batch + 1) * 4);
-  l.total = l.prog + align256(static_cast<size_t>(n_prog + 1) * 4);
+  l.rot = l.prog + align256(static_cast<size_t>(n_prog + 1) * 4);
+  l.total = l.rot + 2 * align256(rot_bytes);
   return l;
 }
 
@@ -396,9 +400,12 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
     const int n = plan_fwd_topk(offsets_host, batch, num_heads, nq, 1, 1, nullptr, nullptr);
     return fwd_layout(n, plan_ctas(dev, n), batch, true).total;
   }
-  if (op == JFA_OP_BLOCK_FWD || op == JFA_OP_BLOCK_BWD) {
+  if (op == JFA_OP_BLOCK_FWD || op == JFA_OP_BLOCK_BWD || op == JFA_OP_BLOCK_FWD_ROPE ||
+      op == JFA_OP_BLOCK_BWD_ROPE) {
     const int P = plan_block(offsets_host, batch, num_heads, dev.num_sms, nullptr, nullptr);
-    return block_layout(batch, P).total;
+    const bool rope = op == JFA_OP_BLOCK_FWD_ROPE || op == JFA_OP_BLOCK_BWD_ROPE;
+    const size_t rot = rope ? static_cast<size_t>(offsets_host[batch]) * num_heads * head_dim * 2 : 0;
+    return block_layout(batch, P, rot).total;
   }
   return 0;
 }
@@ -764,9 +771,12 @@ extern "C" int jfa_bwd_window(const void* q, const void* k, const void* v, const
 }
 
 // Shared by the two block-diagonal entry points: checks, host plan, staging.
+// With `rot` (the rotary variants) the workspace also holds rotated copies of q
+// and k, returned in rot[0], rot[1].
 static int block_common(const void* q, const void* k, const void* v, const void* out0, const int32_t* offsets_dev,
                         const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream, BlockArgs* a) {
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream, BlockArgs* a,
+                        void** rot = nullptr, int* num_sms = nullptr) {
   Common c;
   int st = validate_common(q, k, v, out0, offsets_dev, offsets_host, batch, max_len, 0, num_heads, num_heads,
                            head_dim, scale, 0, 0, &c);
@@ -775,9 +785,15 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   if (st != JFA_OK) return st;
   std::vector<int32_t> bpb, prog;
   const int P = plan_block(offsets_host, batch, num_heads, c.dev.num_sms, &bpb, &prog);
-  const BlockLayout lay = block_layout(batch, P);
+  const size_t rot_bytes = rot ? static_cast<size_t>(c.kv_rows) * num_heads * head_dim * 2 : 0;
+  const BlockLayout lay = block_layout(batch, P, rot_bytes);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (rot) {
+    rot[0] = ws + lay.rot;
+    rot[1] = ws + lay.rot + align256(rot_bytes);
+  }
+  if (num_sms) *num_sms = c.dev.num_sms;
   a->q = q;
   a->k = k;
   a->v = v;
@@ -798,8 +814,9 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   a->scale = scale;
   a->stream = stream;
   if (P == 0) return cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
-  // the cleared error word and both lists in one copy
-  std::vector<uint8_t> blob(lay.total - lay.err, 0);
+  // the cleared error word and both lists in one copy (the rotated copies that
+  // follow them are written by the rotation pass)
+  std::vector<uint8_t> blob(lay.rot - lay.err, 0);
   std::memcpy(blob.data() + (lay.bpb - lay.err), bpb.data(), bpb.size() * 4);
   std::memcpy(blob.data() + (lay.prog - lay.err), prog.data(), prog.size() * 4);
   return stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
@@ -834,12 +851,18 @@ extern "C" int block_attn_fwd_rope(const void* q, const void* k, const void* v, 
   if (st != JFA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   BlockArgs a{};
+  void* rot[2] = {nullptr, nullptr};
+  int num_sms = 0;
   st = block_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
-                    workspace_bytes, stream, &a);
+                    workspace_bytes, stream, &a, rot, &num_sms);
   if (st != JFA_OK || a.n_prog == 0) return st;
+  // q and k rotated into the workspace, then the block forward on the copies
+  RopeArgs r{q, rot[0], k, rot[1], rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 0, stream};
+  st = launch_rope(r, num_sms);
+  if (st != JFA_OK) return st;
+  a.q = rot[0];
+  a.k = rot[1];
   a.o = o;
-  a.rope_cos = rope_cos;
-  a.rope_sin = rope_sin;
   return launch_block_fwd(a);
 }
 
@@ -857,16 +880,27 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
     return JFA_ERR_INVALID_ARG;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
   BlockArgs a{};
+  void* rot[2] = {nullptr, nullptr};
+  int num_sms = 0;
   st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
-                    workspace_bytes, stream, &a);
+                    workspace_bytes, stream, &a, rot, &num_sms);
   if (st != JFA_OK || a.n_prog == 0) return st;
+  // q and k rotated into the workspace, the block backward on the copies (its dq
+  // and dk are with respect to the rotated rows), then dq and dk carried back in
+  // place through the transposed rotation
+  RopeArgs r{q, rot[0], k, rot[1], rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 0, stream};
+  st = launch_rope(r, num_sms);
+  if (st != JFA_OK) return st;
+  a.q = rot[0];
+  a.k = rot[1];
   a.dout = dout;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.rope_cos = rope_cos;
-  a.rope_sin = rope_sin;
-  return launch_block_bwd(a);
+  st = launch_block_bwd(a);
+  if (st != JFA_OK) return st;
+  RopeArgs back{dq, dq, dk, dk, rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 1, stream};
+  return launch_rope(back, num_sms);
 }
 
 extern "C" int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,

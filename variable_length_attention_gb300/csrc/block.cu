@@ -9,12 +9,8 @@
 // recomputes P from Q and K, forms Di = rowsum(P o dP) inline, and every block
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
-// Rotary embedding (the "with rotary fused" variant of "TLX Block Attention",
-// introduction): when the caller passes cos/sin tables, Q and K are rotated in
-// shared memory right after they land -- the rotate-half form, row position =
-// index inside its sequence -- and the backward carries dQ and dK back through
-// the transposed rotation before storing them, so no separate pass over Q, K,
-// dQ or dK is needed.
+// The rotary variants run these kernels on rotated copies of Q and K and carry
+// dQ and dK back through the transposed rotation afterwards (rope.cu).
 //
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
@@ -54,8 +50,6 @@ struct Params {
   float scale, scale_log2;
   int use_clc;                // 1: one CTA per chunk of `chunk` tiles, Cluster Launch Control
   int chunk, n_tiles, n_chunks;
-  const float* rope_cos;      // rotary tables [positions, D/2] (rotary variant only)
-  const float* rope_sin;
 };
 
 // Tiles [*tb, *te) of schedule entry `ch`: chunk ch under Cluster Launch
@@ -138,61 +132,6 @@ __device__ __forceinline__ Blk locate(const Params& p, int g) {
   return r;
 }
 
-// Rotates row r of a 128-row bf16 tile stored as D/64 128-byte-swizzled
-// 64-column boxes, in place: for i < D/2 the pair (x_i, x_{i+D/2}) becomes
-// (x_i c_i - x_{i+D/2} s_i, x_{i+D/2} c_i + x_i s_i), c and s being the row's
-// cosine and sine table rows.
-template <int D>
-__device__ __forceinline__ void rope_smem_row(uint8_t* tile, int r, const float* __restrict__ cs,
-                                              const float* __restrict__ sn) {
-  constexpr int HC = D / 16;  // 16-byte pieces (8 columns) in half a row
-#pragma unroll
-  for (int j = 0; j < HC; ++j) {
-    const int j2 = j + HC;
-    const uint32_t a1 = smem_u32(tile + (j / 8) * 16384 + r * 128 + (((j % 8) ^ (r & 7)) << 4));
-    const uint32_t a2 = smem_u32(tile + (j2 / 8) * 16384 + r * 128 + (((j2 % 8) ^ (r & 7)) << 4));
-    uint32_t x[4], y[4];
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1));
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2));
-    const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + 8 * j));
-    const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + 8 * j + 4));
-    const float4 s0 = __ldg(reinterpret_cast<const float4*>(sn + 8 * j));
-    const float4 s1 = __ldg(reinterpret_cast<const float4*>(sn + 8 * j + 4));
-    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
-      const float2 w = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y[e]));
-      x[e] = pack_bf16(u.x * c[2 * e] - w.x * sv[2 * e], u.y * c[2 * e + 1] - w.y * sv[2 * e + 1]);
-      y[e] = pack_bf16(w.x * c[2 * e] + u.x * sv[2 * e], w.y * c[2 * e + 1] + u.y * sv[2 * e + 1]);
-    }
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
-                 : "memory");
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a2), "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3])
-                 : "memory");
-  }
-}
-
-// The rotation of one Q/K tile pair by a warpgroup (thread r takes row r of
-// both): rows past their block's end are left alone (their scores are masked).
-template <int D>
-__device__ __forceinline__ void rope_tile(const Params& p, uint8_t* q_tile, uint8_t* k_tile, int r, const Blk& blk) {
-  const int rr = r & 63;
-  if (rr >= blk.len) return;
-  const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
-  rope_smem_row<D>(q_tile, r, p.rope_cos + at, p.rope_sin + at);
-  rope_smem_row<D>(k_tile, r, p.rope_cos + at, p.rope_sin + at);
-}
-
-// (g1, g2) <- (g1 c + g2 s, g2 c - g1 s): the transposed rotation of one column
-// pair of a gradient row, in fp32 before it is rounded.
-__device__ __forceinline__ void rope_back(float& g1, float& g2, float c, float s) {
-  const float a = g1 * c + g2 * s, b = g2 * c - g1 * s;
-  g1 = a;
-  g2 = b;
-}
-
 // Operands come in two rings: Q and K of a tile together (released as soon as
 // its score GEMM has read them) and V on its own (released after the PV GEMM),
 // so more bytes are in flight from HBM than with whole Q/K/V stages.
@@ -212,7 +151,6 @@ struct FwdCfg {
 struct FwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[2], qk_empty[2], v_full[6], v_empty[6];
-  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
   uint64_t drain;
   uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
@@ -230,7 +168,7 @@ __device__ __forceinline__ void load_half(const CUtensorMap* tm, uint64_t* bar, 
   for (int c = 0; c < D / 64; ++c) tma_load_2d(tm, bar, tile + c * 16384 + half * 8192, h * D + c * 64, row0);
 }
 
-template <int D, bool ROPE>
+template <int D>
 __global__ void __launch_bounds__(384, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -250,7 +188,6 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
-      mbar_init(&bars->qk_rot[s], 4);
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -367,7 +304,7 @@ __global__ void __launch_bounds__(384, 1)
       const int t = next_tile(cur, bars, p, ab, false);
       if (t == -2) break;
       if (t >= 0) {  // S of tile i, once its operands landed (and are rotated) and its TMEM buffer is free
-        if (!mbar_wait(ROPE ? &bars->qk_rot[i % C::NQK] : &bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
+        if (!mbar_wait(&bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
         if (!mbar_wait(&bars->t_free[i & 1], ((i >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after();
         issue_s(i);
@@ -403,14 +340,6 @@ __global__ void __launch_bounds__(384, 1)
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
       const int rr = r & 63;
-      if constexpr (ROPE) {  // this warpgroup rotates its own tile's Q and K (slot i % 2 == b)
-        const int st = i % C::NQK;
-        if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) goto done;
-        rope_tile<D>(p, smem + st * 2 * C::TILE, smem + st * 2 * C::TILE + C::TILE, r, blk);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
-      }
       if (!mbar_wait(&bars->s_full[b], (i >> 1) & 1, ab)) goto done;
       tc_fence_after();
       uint32_t sr[64];
@@ -507,7 +436,6 @@ struct BwdCfg {
 struct BwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[3], qk_empty[3], vdo_full[2], vdo_empty[2];
-  uint64_t qk_rot[3];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
   uint64_t drain;
@@ -525,7 +453,7 @@ __device__ __forceinline__ void st_row_piece(uint8_t* tile, int q, int c, int j,
                : "memory");
 }
 
-template <int D, bool ROPE>
+template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -548,7 +476,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
-      mbar_init(&bars->qk_rot[s], 4);
     }
     for (int s = 0; s < C::NVD; ++s) {
       mbar_init(&bars->vdo_full[s], 1);
@@ -648,7 +575,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int st = i % C::NQK, sv = i % C::NVD;
       const uint32_t q = smem_u32(smem + st * 2 * C::TILE), k = q + C::TILE;
       const uint32_t v = smem_u32(smem + C::OFF_V + sv * 2 * C::TILE), dO = v + C::TILE;
-      if (!mbar_wait(ROPE ? &bars->qk_rot[st] : &bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
+      if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
       // S and dP reuse their columns once the softmax warps have read the
       // previous tile's (p_full and ds_full, waited below for that tile); with
       // the accumulators in the same columns, the epilogue must also be done
@@ -710,27 +637,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
     uint32_t stg_full_ph = 0, stg_free_ph = 0;
     TileCursor cur;
-    int rot_ahead = -1;  // rotary: the tile whose Q and K were rotated while the previous one finished
-    // rotary: rotate the Q and K rows of tile counter j (tile id tj) in their slot
-    auto rotate = [&](int j, int tj) -> bool {
-      const int st = j % C::NQK;
-      if (!mbar_wait(&bars->qk_full[st], (j / C::NQK) & 1, ab)) return false;
-      rope_tile<D>(p, smem + st * 2 * C::TILE, smem + st * 2 * C::TILE + C::TILE, r,
-                   locate(p, 2 * (tj / p.H) + half));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
-      return true;
-    };
     for (int i = 0;; ++i) {
       const int t = next_tile(cur, bars, p, ab, true);
       if (t == -2) goto done;
       if (t < 0) break;
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
-      if constexpr (ROPE) {
-        if (rot_ahead != i && !rotate(i, t)) goto done;
-      }
       if (!mbar_wait(&bars->s_full, i & 1, ab)) goto done;
       tc_fence_after();
       float pr[64];
@@ -799,14 +711,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full);
-      if constexpr (ROPE) {
-        // while the tensor core computes this tile's dK and dQ, rotate the next
-        // tile's Q and K if it is already known (not at the end of a chunk)
-        if (cur.t < cur.te) {
-          if (!rotate(i + 1, cur.t)) goto done;
-          rot_ahead = i + 1;
-        }
-      }
       if constexpr (D == 128) {
         // epilogue: row r is query r for dQ and key r for dK, dV (same block, same token).
         // Each result is staged as bf16 rows in the P/dS buffer (free once dK and dQ
@@ -848,49 +752,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
               }
             };
-            if (ROPE && which < 2) {
-              // dQ and dK of the rotated rows go back through the transposed rotation
-  #pragma unroll 1
-              for (int c = 0; c < D / 2; c += 32) {
-                uint32_t v1[32], v2[32];
-                tmem_ld32(tmem + lane_addr + col + c, v1);
-                tmem_ld32(tmem + lane_addr + col + c + D / 2, v2);
-                tmem_wait_ld();
-                reg_fence<32>(v1);
-                reg_fence<32>(v2);
-                float f1[32], f2[32];
-  #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  f1[e] = __uint_as_float(v1[e]) * mul;
-                  f2[e] = __uint_as_float(v2[e]) * mul;
-                }
-                if (valid) {
-                  const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2) + c;
-  #pragma unroll
-                  for (int e = 0; e < 32; e += 4) {
-                    const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
-                    const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
-                    rope_back(f1[e], f2[e], cs.x, sn.x);
-                    rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
-                    rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
-                    rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
-                  }
-                }
-                put(c, f1);
-                put(c + D / 2, f2);
-              }
-            } else {
-  #pragma unroll 1
-              for (int c = 0; c < D; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + col + c, v);
-                tmem_wait_ld();
-                reg_fence<32>(v);
-                float f[32];
-  #pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
-                put(c, f);
-              }
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_addr + col + c, v);
+              tmem_wait_ld();
+              reg_fence<32>(v);
+              float f[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+              put(c, f);
             }
             if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
               tc_fence_before();
@@ -959,47 +830,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             for (int e = 0; e < 4; ++e)
               st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           };
-          if (ROPE && which < 2) {
-            // dQ and dK of the rotated rows go back through the transposed
-            // rotation: columns c and c + 32 form the pairs
-            uint32_t v1[32], v2[32];
-            tmem_ld32(tmem + lane_addr + col, v1);
-            tmem_ld32(tmem + lane_addr + col + 32, v2);
-            tmem_wait_ld();
-            reg_fence<32>(v1);
-            reg_fence<32>(v2);
-            float f1[32], f2[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              f1[e] = __uint_as_float(v1[e]) * mul;
-              f2[e] = __uint_as_float(v2[e]) * mul;
-            }
-            if (valid) {
-              const size_t at = static_cast<size_t>(blk.pos0 + rr) * (D / 2);
-#pragma unroll
-              for (int e = 0; e < 32; e += 4) {
-                const float4 cs = __ldg(reinterpret_cast<const float4*>(p.rope_cos + at + e));
-                const float4 sn = __ldg(reinterpret_cast<const float4*>(p.rope_sin + at + e));
-                rope_back(f1[e], f2[e], cs.x, sn.x);
-                rope_back(f1[e + 1], f2[e + 1], cs.y, sn.y);
-                rope_back(f1[e + 2], f2[e + 2], cs.z, sn.z);
-                rope_back(f1[e + 3], f2[e + 3], cs.w, sn.w);
-              }
-            }
-            put(0, f1);
-            put(32, f2);
-          } else {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_addr + col + c, v);
-              tmem_wait_ld();
-              reg_fence<32>(v);
-              float f[32];
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + col + c, v);
+            tmem_wait_ld();
+            reg_fence<32>(v);
+            float f[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
-              put(c, f);
-            }
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+            put(c, f);
           }
         }
         tc_fence_before();
@@ -1017,7 +857,7 @@ done:
   }
 }
 
-template <int D, bool ROPE>
+template <int D>
 int launch_fwd_impl(const BlockArgs& a) {
   using C = FwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -1029,7 +869,7 @@ int launch_fwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_fwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -1050,14 +890,12 @@ int launch_fwd_impl(const BlockArgs& a) {
   p.chunk = a.chunk;
   p.n_tiles = a.n_tiles;
   p.n_chunks = a.n_chunks;
-  p.rope_cos = a.rope_cos;
-  p.rope_sin = a.rope_sin;
   ProfileScope prof(kKindBlockFwd, a.stream);
-  block_fwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
+  block_fwd_kernel<D><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
-template <int D, bool ROPE>
+template <int D>
 int launch_bwd_impl(const BlockArgs& a) {
   using C = BwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -1073,7 +911,7 @@ int launch_bwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_bwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -1096,10 +934,8 @@ int launch_bwd_impl(const BlockArgs& a) {
   p.chunk = a.chunk;
   p.n_tiles = a.n_tiles;
   p.n_chunks = a.n_chunks;
-  p.rope_cos = a.rope_cos;
-  p.rope_sin = a.rope_sin;
   ProfileScope prof(kKindBlockBwd, a.stream);
-  block_bwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, C::THREADS, C::SMEM, a.stream>>>(
+  block_bwd_kernel<D><<<a.use_clc ? a.n_chunks : a.n_prog, C::THREADS, C::SMEM, a.stream>>>(
       tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -1107,14 +943,10 @@ int launch_bwd_impl(const BlockArgs& a) {
 }  // namespace blk
 
 int launch_block_fwd(const BlockArgs& a) {
-  if (a.rope_cos != nullptr)
-    return a.D == 128 ? blk::launch_fwd_impl<128, true>(a) : blk::launch_fwd_impl<64, true>(a);
-  return a.D == 128 ? blk::launch_fwd_impl<128, false>(a) : blk::launch_fwd_impl<64, false>(a);
+  return a.D == 128 ? blk::launch_fwd_impl<128>(a) : blk::launch_fwd_impl<64>(a);
 }
 int launch_block_bwd(const BlockArgs& a) {
-  if (a.rope_cos != nullptr)
-    return a.D == 128 ? blk::launch_bwd_impl<128, true>(a) : blk::launch_bwd_impl<64, true>(a);
-  return a.D == 128 ? blk::launch_bwd_impl<128, false>(a) : blk::launch_bwd_impl<64, false>(a);
+  return a.D == 128 ? blk::launch_bwd_impl<128>(a) : blk::launch_bwd_impl<64>(a);
 }
 
 }  // namespace jfa

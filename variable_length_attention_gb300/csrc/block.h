@@ -16,8 +16,6 @@ struct BlockArgs {
   int rows, batch, H, D, n_blocks, n_prog;
   int use_clc;                // 1: Cluster Launch Control over chunks of `chunk` tiles
   int chunk, n_tiles, n_chunks;
-  const float* rope_cos;      // rotary tables [positions, D/2] fp32, or null: no rotary embedding
-  const float* rope_sin;
   float scale;
   cudaStream_t stream;
 };

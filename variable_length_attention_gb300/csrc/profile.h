@@ -14,7 +14,8 @@ enum KernelKind : int {
   kKindBlockBwd = 5,
   kKindFill = 6,
   kKindTopk = 7,
-  kNumKernelKinds = 8
+  kKindRope = 8,
+  kNumKernelKinds = 9
 };
 
 class ProfileScope {

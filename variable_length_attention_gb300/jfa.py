@@ -21,6 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libjfa.so")
 
 JFA_OP_FWD, JFA_OP_BWD, JFA_OP_BLOCK_FWD, JFA_OP_BLOCK_BWD, JFA_OP_TOPK_SELECT, JFA_OP_FWD_TOPK = 0, 1, 2, 3, 4, 5
+JFA_OP_BLOCK_FWD_ROPE, JFA_OP_BLOCK_BWD_ROPE = 6, 7
 STATUS = {0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_BAD_OFFSETS",
           4: "JFA_ERR_WORKSPACE_TOO_SMALL", 5: "JFA_ERR_ARCH", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT",
           8: "JFA_ERR_TOO_LARGE"}
@@ -64,7 +65,7 @@ SIGNATURES = {
     "jfa_profile_read": (_I, [_I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
 KERNEL_KINDS = {"fwd": 0, "bwd_prep": 1, "bwd_main": 2, "dq_convert": 3, "block_fwd": 4, "block_bwd": 5,
-                "fill": 6, "topk_select": 7}
+                "fill": 6, "topk_select": 7, "rope": 8}
 
 _lock = threading.Lock()
 _lib = None
@@ -381,8 +382,9 @@ def block_attn_fwd(q, k, v, offsets, offsets_host=None, *, max_len=None, scale=N
         scale = 1.0 / math.sqrt(D)
     out = torch.empty_like(q) if out is None else out
     _check_problem(q, k, v, offsets, offs_h, 0, o=out)
-    workspace = _workspace(JFA_OP_BLOCK_FWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     tables = _rope_tables(rope, D, q.device)
+    op = JFA_OP_BLOCK_FWD if tables is None else JFA_OP_BLOCK_FWD_ROPE
+    workspace = _workspace(op, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     if tables is not None:
         st = L.block_attn_fwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(tables[0]), _ptr(tables[1]),
                                    tables[0].shape[0], _ptr(offsets), offs_h.ctypes.data, batch, int(max_len), H, D,
@@ -412,8 +414,9 @@ def block_attn_bwd(q, k, v, o, dout, offsets, offsets_host=None, *, max_len=None
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check_problem(q, k, v, offsets, offs_h, 0, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
-    workspace = _workspace(JFA_OP_BLOCK_BWD, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     tables = _rope_tables(rope, D, q.device)
+    op = JFA_OP_BLOCK_BWD if tables is None else JFA_OP_BLOCK_BWD_ROPE
+    workspace = _workspace(op, offs_h, batch, 0, H, D, False, False, workspace, q.device)
     if tables is not None:
         st = L.block_attn_bwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                                    _ptr(tables[0]), _ptr(tables[1]), tables[0].shape[0], _ptr(offsets),
