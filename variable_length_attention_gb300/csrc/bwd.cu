@@ -747,7 +747,7 @@ __global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bflo
                             int rows, int H, float4* __restrict__ acc, long acc4) {
   constexpr int TPP = D / 8;     // lanes per pair
   constexpr int PPW = 32 / TPP;  // pairs per warp per round
-  constexpr int U = 4;           // rounds whose loads are in flight together
+  constexpr int U = 2;           // rounds whose loads are in flight together
   const int lane = threadIdx.x & 31, part = lane % TPP;
   const long warp = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long n_warps = (static_cast<long>(gridDim.x) * blockDim.x) >> 5;
@@ -863,10 +863,10 @@ int launch_bwd_prep(const BwdArgs& a, int num_sms) {
   if (pairs == 0 && acc4 == 0) return JFA_OK;
   const int block = 256;
   // enough warps for every pair to be visited once where that fits, capped at
-  // 16 resident blocks per SM; larger problems loop
-  const long per_block = (block / 32) * (32 / (a.D / 8)) * 4;
+  // one wave (48 registers: 5 blocks of 256 per SM); larger problems loop
+  const long per_block = (block / 32) * (32 / (a.D / 8)) * 2;
   long grid = std::max((pairs + per_block - 1) / per_block, (acc4 + block - 1) / block);
-  grid = std::min<long>(std::max<long>(grid, 1), 16L * num_sms);
+  grid = std::min<long>(std::max<long>(grid, 1), 5L * num_sms);
   ProfileScope prof(kKindBwdPrep, a.stream);
   float4* acc = reinterpret_cast<float4*>(a.dq_acc);
   if (a.D == 128)
