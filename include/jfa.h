@@ -91,7 +91,7 @@ typedef enum {
   JFA_OP_BLOCK_BWD = 3,
   JFA_OP_TOPK_SELECT = 4,  /* jfa_topk_select (an upper bound with grouped K/V heads) */
   JFA_OP_FWD_TOPK = 5,     /* jfa_fwd_topk */
-  JFA_OP_BLOCK_FWD_ROPE = 6, /* block_attn_fwd_rope: + rotated copies of q and k */
+  JFA_OP_BLOCK_FWD_ROPE = 6, /* block_attn_fwd_rope: + the packed rotary table */
   JFA_OP_BLOCK_BWD_ROPE = 7  /* block_attn_bwd_rope: the same */
 } jfa_op;
 
@@ -227,13 +227,13 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
  * aligned, rope_rows >= max_len.  The forward attends with the rotated q and k;
  * the backward recomputes them and returns dq and dk with respect to the
  * unrotated q and k (the transposed rotation is applied before they are
- * returned).  q and k stay unrotated in memory: both calls rotate copies into
- * the workspace, whose size is jfa_workspace_size(JFA_OP_BLOCK_FWD_ROPE or
- * JFA_OP_BLOCK_BWD_ROPE, ...) (two extra tensors of rows x num_heads x head_dim
- * bf16), in one streaming pass over q and k before the attention kernel; the
- * backward carries dq and dk back in one pass after it.  Errors as
- * block_attn_*, plus JFA_ERR_INVALID_ARG for missing, misaligned or too short
- * tables.
+ * returned).  q and k stay unrotated in memory: the kernels rotate their tiles
+ * in shared memory, from the tables packed into the workspace as (cos, sin)
+ * fp16 pairs, whose size is jfa_workspace_size(JFA_OP_BLOCK_FWD_ROPE or
+ * JFA_OP_BLOCK_BWD_ROPE, ...) (the plain size plus longest sequence x
+ * head_dim/2 x 4 bytes); the backward carries dq and dk back through the
+ * transposed rotation in one pass after its kernel.  Errors as block_attn_*,
+ * plus JFA_ERR_INVALID_ARG for missing, misaligned or too short tables.
  */
 int block_attn_fwd_rope(const void* q, const void* k, const void* v, void* o, const float* rope_cos,
                         const float* rope_sin, int rope_rows, const int32_t* offsets_dev,
@@ -391,7 +391,8 @@ int jfa_get_block_schedule(void);
  * on the recorded events and returns the summed device time (0 for an
  * unselected kind) and the launch count of one kernel kind: 0 forward,
  * 1 backward prepass (Di), 2 backward main, 3 dQ convert, 4 block forward,
- * 5 block backward, 6 empty-sequence fill, 7 top-k selection, 8 rotary pass.
+ * 5 block backward, 6 empty-sequence fill, 7 top-k selection, 8 rotary table
+ * packing and the backward's transposed-rotation pass.
  */
 /*
  * Failure-path self-test (no counterpart on the pages; failure detection).

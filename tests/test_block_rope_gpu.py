@@ -115,18 +115,18 @@ def test_rope_tables_must_cover_every_position():
         V.block_attn_fwd(q, k, v, offs, w.offsets, rope=_tables(99, 64))  # positions 0..99 needed
 
 
-def test_rope_workspace_holds_the_rotated_copies():
-    """The rotary calls rotate q and k into the workspace: their size exceeds the
-    plain block calls' by two tensors (each rounded up to 256 bytes), and a
-    workspace of the plain size is refused before any work."""
+def test_rope_workspace_holds_the_packed_table():
+    """The rotary calls pack the tables as (cos, sin) half2 pairs into the
+    workspace: their size exceeds the plain block calls' by one table of
+    longest-sequence x D/2 x 4 bytes (rounded up to 256), and a workspace of the
+    plain size is refused before any work."""
     from variable_length_attention_gb300 import jfa as J
     w = W.custom([100, 0, 30, 64], 2, 64, mode="block", seed_base=1700)
-    rows = int(w.offsets[-1])
-    tensor = -(-(rows * w.num_heads * w.head_dim * 2) // 256) * 256
+    table = -(-(100 * (w.head_dim // 2) * 4) // 256) * 256
     for plain, rot in ((J.JFA_OP_BLOCK_FWD, J.JFA_OP_BLOCK_FWD_ROPE), (J.JFA_OP_BLOCK_BWD, J.JFA_OP_BLOCK_BWD_ROPE)):
         a = V.jfa_workspace_size(plain, w.offsets, w.batch, 0, w.num_heads, w.head_dim, 0, 0)
         b = V.jfa_workspace_size(rot, w.offsets, w.batch, 0, w.num_heads, w.head_dim, 0, 0)
-        assert a > 0 and b == a + 2 * tensor
+        assert a > 0 and b == a + table
     q, k, v, _ = [t.cuda() for t in w.tensors("cpu")]
     offs = torch.from_numpy(w.offsets).cuda()
     small = torch.empty(V.jfa_workspace_size(J.JFA_OP_BLOCK_FWD, w.offsets, w.batch, 0, w.num_heads, w.head_dim, 0, 0),

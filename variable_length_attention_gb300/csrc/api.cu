@@ -227,17 +227,23 @@ static BwdLayout bwd_layout(int n_units, int n_cta, int q_rows, int o_rows, int 
 }
 
 struct BlockLayout {
-  size_t err = 0, bpb = 0, prog = 0, rot = 0, total = 0;
+  size_t err = 0, bpb = 0, prog = 0, tab = 0, total = 0;
 };
-// rot_bytes: the rotary variants' rotated copies of q and k (two tensors of that
-// many bytes each), else 0
-static BlockLayout block_layout(int batch, int n_prog, size_t rot_bytes = 0) {
+// tab_bytes: the rotary variants' packed (cos, sin) table, else 0
+static BlockLayout block_layout(int batch, int n_prog, size_t tab_bytes = 0) {
   BlockLayout l;
   l.bpb = 256;
   l.prog = l.bpb + align256(static_cast<size_t>(batch + 1) * 4);
-  l.rot = l.prog + align256(static_cast<size_t>(n_prog + 1) * 4);
-  l.total = l.rot + 2 * align256(rot_bytes);
+  l.tab = l.prog + align256(static_cast<size_t>(n_prog + 1) * 4);
+  l.total = l.tab + align256(tab_bytes);
   return l;
+}
+
+// The longest sequence of a problem (the positions a rotary table must cover).
+static int64_t longest(const int32_t* offsets_host, int batch) {
+  int64_t m = 0;
+  for (int b = 0; b < batch; ++b) m = std::max<int64_t>(m, static_cast<int64_t>(offsets_host[b + 1]) - offsets_host[b]);
+  return m;
 }
 
 __global__ void fill_empty_broadcast_kernel(const int32_t* empty_seq, int n_empty, int nq, int H, int D,
@@ -404,8 +410,8 @@ extern "C" size_t jfa_workspace_size(int op, const int32_t* offsets_host, int ba
       op == JFA_OP_BLOCK_BWD_ROPE) {
     const int P = plan_block(offsets_host, batch, num_heads, dev.num_sms, nullptr, nullptr);
     const bool rope = op == JFA_OP_BLOCK_FWD_ROPE || op == JFA_OP_BLOCK_BWD_ROPE;
-    const size_t rot = rope ? static_cast<size_t>(offsets_host[batch]) * num_heads * head_dim * 2 : 0;
-    return block_layout(batch, P, rot).total;
+    const size_t tab = rope ? static_cast<size_t>(longest(offsets_host, batch)) * (head_dim / 2) * 4 : 0;
+    return block_layout(batch, P, tab).total;
   }
   return 0;
 }
@@ -771,12 +777,12 @@ extern "C" int jfa_bwd_window(const void* q, const void* k, const void* v, const
 }
 
 // Shared by the two block-diagonal entry points: checks, host plan, staging.
-// With `rot` (the rotary variants) the workspace also holds rotated copies of q
-// and k, returned in rot[0], rot[1].
+// With `tab` (the rotary variants) the workspace also holds the packed rotary
+// table, whose address and row count come back in *tab and *tab_rows.
 static int block_common(const void* q, const void* k, const void* v, const void* out0, const int32_t* offsets_dev,
                         const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream, BlockArgs* a,
-                        void** rot = nullptr, int* num_sms = nullptr) {
+                        uint32_t** tab = nullptr, int64_t* tab_rows = nullptr, int* num_sms = nullptr) {
   Common c;
   int st = validate_common(q, k, v, out0, offsets_dev, offsets_host, batch, max_len, 0, num_heads, num_heads,
                            head_dim, scale, 0, 0, &c);
@@ -785,13 +791,13 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   if (st != JFA_OK) return st;
   std::vector<int32_t> bpb, prog;
   const int P = plan_block(offsets_host, batch, num_heads, c.dev.num_sms, &bpb, &prog);
-  const size_t rot_bytes = rot ? static_cast<size_t>(c.kv_rows) * num_heads * head_dim * 2 : 0;
-  const BlockLayout lay = block_layout(batch, P, rot_bytes);
+  const int64_t rows_tab = tab ? longest(offsets_host, batch) : 0;
+  const BlockLayout lay = block_layout(batch, P, static_cast<size_t>(rows_tab) * (head_dim / 2) * 4);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (rot) {
-    rot[0] = ws + lay.rot;
-    rot[1] = ws + lay.rot + align256(rot_bytes);
+  if (tab) {
+    *tab = reinterpret_cast<uint32_t*>(ws + lay.tab);
+    *tab_rows = rows_tab;
   }
   if (num_sms) *num_sms = c.dev.num_sms;
   a->q = q;
@@ -814,9 +820,9 @@ static int block_common(const void* q, const void* k, const void* v, const void*
   a->scale = scale;
   a->stream = stream;
   if (P == 0) return cudaMemsetAsync(ws + lay.err, 0, sizeof(int), stream) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
-  // the cleared error word and both lists in one copy (the rotated copies that
-  // follow them are written by the rotation pass)
-  std::vector<uint8_t> blob(lay.rot - lay.err, 0);
+  // the cleared error word and both lists in one copy (the rotary table that
+  // follows them is written by its own kernel)
+  std::vector<uint8_t> blob(lay.tab - lay.err, 0);
   std::memcpy(blob.data() + (lay.bpb - lay.err), bpb.data(), bpb.size() * 4);
   std::memcpy(blob.data() + (lay.prog - lay.err), prog.data(), prog.size() * 4);
   return stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
@@ -851,17 +857,16 @@ extern "C" int block_attn_fwd_rope(const void* q, const void* k, const void* v, 
   if (st != JFA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   BlockArgs a{};
-  void* rot[2] = {nullptr, nullptr};
-  int num_sms = 0;
+  uint32_t* tab = nullptr;
+  int64_t tab_rows = 0;
   st = block_common(q, k, v, o, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
-                    workspace_bytes, stream, &a, rot, &num_sms);
+                    workspace_bytes, stream, &a, &tab, &tab_rows);
   if (st != JFA_OK || a.n_prog == 0) return st;
-  // q and k rotated into the workspace, then the block forward on the copies
-  RopeArgs r{q, rot[0], k, rot[1], rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 0, stream};
-  st = launch_rope(r, num_sms);
+  // the packed table, then the block forward, which rotates q and k tiles in
+  // shared memory as they land
+  st = launch_rope_pack(rope_cos, rope_sin, tab, tab_rows, head_dim / 2, stream);
   if (st != JFA_OK) return st;
-  a.q = rot[0];
-  a.k = rot[1];
+  a.rope_tab = tab;
   a.o = o;
   return launch_block_fwd(a);
 }
@@ -880,19 +885,18 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
     return JFA_ERR_INVALID_ARG;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return JFA_ERR_INVALID_ARG;
   BlockArgs a{};
-  void* rot[2] = {nullptr, nullptr};
+  uint32_t* tab = nullptr;
+  int64_t tab_rows = 0;
   int num_sms = 0;
   st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
-                    workspace_bytes, stream, &a, rot, &num_sms);
+                    workspace_bytes, stream, &a, &tab, &tab_rows, &num_sms);
   if (st != JFA_OK || a.n_prog == 0) return st;
-  // q and k rotated into the workspace, the block backward on the copies (its dq
-  // and dk are with respect to the rotated rows), then dq and dk carried back in
-  // place through the transposed rotation
-  RopeArgs r{q, rot[0], k, rot[1], rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 0, stream};
-  st = launch_rope(r, num_sms);
+  // the packed table, the block backward rotating q and k tiles as they land
+  // (its dq and dk are with respect to the rotated rows), then dq and dk carried
+  // back in place through the transposed rotation
+  st = launch_rope_pack(rope_cos, rope_sin, tab, tab_rows, head_dim / 2, stream);
   if (st != JFA_OK) return st;
-  a.q = rot[0];
-  a.k = rot[1];
+  a.rope_tab = tab;
   a.dout = dout;
   a.dq = dq;
   a.dk = dk;

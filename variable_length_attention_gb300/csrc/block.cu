@@ -9,8 +9,11 @@
 // recomputes P from Q and K, forms Di = rowsum(P o dP) inline, and every block
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
-// The rotary variants run these kernels on rotated copies of Q and K and carry
-// dQ and dK back through the transposed rotation afterwards (rope.cu).
+// Rotary variants (a template parameter): two otherwise idle warps rotate each
+// tile's Q and K in shared memory as soon as TMA has landed them, from a packed
+// fp16 (cos, sin) table the entry point builds per call (rope.cu), and the score
+// GEMM waits for them; the backward's dQ and dK go back through the transposed
+// rotation in a pass after the kernel (rope.cu).
 //
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
@@ -27,6 +30,7 @@
 // branchless binary search over the per-batch block prefix sums (section 5).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "block.h"
@@ -50,6 +54,7 @@ struct Params {
   float scale, scale_log2;
   int use_clc;                // 1: one CTA per chunk of `chunk` tiles, Cluster Launch Control
   int chunk, n_tiles, n_chunks;
+  const uint32_t* rope_tab;   // rotary variant: (cos, sin) as half2, [positions, D/2]
 };
 
 // Tiles [*tb, *te) of schedule entry `ch`: chunk ch under Cluster Launch
@@ -132,6 +137,120 @@ __device__ __forceinline__ Blk locate(const Params& p, int g) {
   return r;
 }
 
+// Rotates Q and K rows [r0, r0 + NROWS) of one 64-row half of a tile pair in place, each tile
+// stored as D/64 128-byte-swizzled 64-column boxes: for i < D/2 the pair
+// (x_i, x_{i+D/2}) becomes (x_i c_i - x_{i+D/2} s_i, x_{i+D/2} c_i + x_i s_i), c and
+// s from the packed table row of the row's position.  One warp: each lane takes
+// a 16-byte chunk of the first half of a row (columns 8j..8j+7) and its partner
+// chunk of the second half, 4 rows per step at D = 128 (8 at D = 64).  Steps go
+// in batches of B: the batch's shared-memory loads are all issued before its
+// stores, and the next batch's table rows load while this one is rotated, so
+// neither the shared-memory nor the table latency is paid per row.  Rows past
+// the block's end are left alone (their scores are masked).
+template <int D>
+__device__ __forceinline__ uint32_t rot_off(int row, int c) {
+  return (c / 64) * 16384 + row * 128 + ((((c % 64) / 8) ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t rot_word(uint32_t x, uint32_t y, uint32_t t0, uint32_t t1, bool second) {
+  // element pair of word x (first half) and y (second half) with tables t0, t1 (half2 cos, sin)
+  const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
+  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&t0));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+  return second ? pack_bf16(v.x * a.x + u.x * a.y, v.y * b.x + u.y * b.y)
+                : pack_bf16(u.x * a.x - v.x * a.y, u.y * b.x - v.y * b.y);
+}
+template <int D, int NROWS, int B>
+__device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint8_t* q_tile, uint8_t* k_tile,
+                                          int half, int r0, const Blk& blk, int lane) {
+  constexpr int CPR = D / 16;    // chunks in half a row
+  constexpr int RPS = 32 / CPR;  // rows per step; B steps per batch
+  constexpr int NB = NROWS / RPS / B;
+  const int j = lane % CPR, sub = lane / CPR;
+  const int c1 = 8 * j, c2 = 8 * j + D / 2;
+  const uint32_t base[2] = {smem_u32(q_tile), smem_u32(k_tile)};
+  uint4 t[2][B][2];  // table words of two batches: [buffer][step][pairs 0-3 | 4-7]
+  auto load_tab = [&](int bi, int buf) {
+#pragma unroll
+    for (int st = 0; st < B; ++st) {
+      const int rr = r0 + (bi * B + st) * RPS + sub;
+      if (rr < blk.len) {
+        const uint4* e = reinterpret_cast<const uint4*>(tab + static_cast<size_t>(blk.pos0 + rr) * (D / 2) + c1);
+        t[buf][st][0] = __ldg(e);
+        t[buf][st][1] = __ldg(e + 1);
+      }
+    }
+  };
+  load_tab(0, 0);
+#pragma unroll
+  for (int bi = 0; bi < NB; ++bi) {
+    const int buf = bi & 1;
+    if (bi + 1 < NB) load_tab(bi + 1, buf ^ 1);
+    uint4 x[B][2], y[B][2];
+#pragma unroll
+    for (int st = 0; st < B; ++st) {
+      const int rr = r0 + (bi * B + st) * RPS + sub;
+      if (rr < blk.len) {
+        const int row = 64 * half + rr;
+#pragma unroll
+        for (int tn = 0; tn < 2; ++tn) {
+          const uint32_t a1 = base[tn] + rot_off<D>(row, c1), a2 = base[tn] + rot_off<D>(row, c2);
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[st][tn].x), "=r"(x[st][tn].y), "=r"(x[st][tn].z), "=r"(x[st][tn].w) : "r"(a1));
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(y[st][tn].x), "=r"(y[st][tn].y), "=r"(y[st][tn].z), "=r"(y[st][tn].w) : "r"(a2));
+        }
+      }
+    }
+#pragma unroll
+    for (int st = 0; st < B; ++st) {
+      const int rr = r0 + (bi * B + st) * RPS + sub;
+      if (rr < blk.len) {
+        const int row = 64 * half + rr;
+        const uint32_t tw[8] = {t[buf][st][0].x, t[buf][st][0].y, t[buf][st][0].z, t[buf][st][0].w,
+                                t[buf][st][1].x, t[buf][st][1].y, t[buf][st][1].z, t[buf][st][1].w};
+#pragma unroll
+        for (int tn = 0; tn < 2; ++tn) {
+          const uint32_t xi[4] = {x[st][tn].x, x[st][tn].y, x[st][tn].z, x[st][tn].w};
+          const uint32_t yi[4] = {y[st][tn].x, y[st][tn].y, y[st][tn].z, y[st][tn].w};
+          uint32_t xo[4], yo[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            xo[w] = rot_word(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], false);
+            yo[w] = rot_word(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], true);
+          }
+          const uint32_t a1 = base[tn] + rot_off<D>(row, c1), a2 = base[tn] + rot_off<D>(row, c2);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(xo[0]), "r"(xo[1]), "r"(xo[2]),
+                       "r"(xo[3]) : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a2), "r"(yo[0]), "r"(yo[1]), "r"(yo[2]),
+                       "r"(yo[3]) : "memory");
+        }
+      }
+    }
+  }
+}
+
+// The rotation role of the rotary backward (warps 2 and 3): every tile's Q and
+// K once their slot has landed, warp 2 the tile's first block and warp 3 its
+// second; the score GEMM waits for qk_rot.  (In the forward the tile's softmax
+// warpgroup rotates it, a quarter per warp, while it waits for its scores.)
+template <int D, int NQK, class Bars>
+__device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* smem, int tile_bytes, const Abort& ab) {
+  const int half = warp_id() - 2, lane = lane_id();
+  TileCursor cur;
+  for (int i = 0;; ++i) {
+    const int t = next_tile(cur, bars, p, ab, true);
+    if (t < 0) break;
+    const int st = i % NQK;
+    if (!mbar_wait(&bars->qk_full[st], (i / NQK) & 1, ab)) break;
+    uint8_t* q_tile = smem + st * 2 * tile_bytes;
+    rope_rows<D, 64, 4>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half), lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
+  }
+}
+
 // Operands come in two rings: Q and K of a tile together (released as soon as
 // its score GEMM has read them) and V on its own (released after the PV GEMM),
 // so more bytes are in flight from HBM than with whole Q/K/V stages.
@@ -151,6 +270,7 @@ struct FwdCfg {
 struct FwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[2], qk_empty[2], v_full[6], v_empty[6];
+  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
   uint64_t drain;
   uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
@@ -168,7 +288,7 @@ __device__ __forceinline__ void load_half(const CUtensorMap* tm, uint64_t* bar, 
   for (int c = 0; c < D / 64; ++c) tma_load_2d(tm, bar, tile + c * 16384 + half * 8192, h * D + c * 64, row0);
 }
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(384, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -188,6 +308,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
+      mbar_init(&bars->qk_rot[s], 4);  // the tile's softmax warpgroup
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -304,7 +425,7 @@ __global__ void __launch_bounds__(384, 1)
       const int t = next_tile(cur, bars, p, ab, false);
       if (t == -2) break;
       if (t >= 0) {  // S of tile i, once its operands landed (and are rotated) and its TMEM buffer is free
-        if (!mbar_wait(&bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
+        if (!mbar_wait(ROPE ? &bars->qk_rot[i % C::NQK] : &bars->qk_full[i % C::NQK], (i / C::NQK) & 1, ab)) break;
         if (!mbar_wait(&bars->t_free[i & 1], ((i >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after();
         issue_s(i);
@@ -340,6 +461,15 @@ __global__ void __launch_bounds__(384, 1)
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
       const int rr = r & 63;
+      if constexpr (ROPE) {  // this warpgroup rotates its own tile's Q and K, 32 rows per warp
+        const int st = i % C::NQK;
+        if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) goto done;
+        uint8_t* q_tile = smem + st * 2 * C::TILE;
+        rope_rows<D, 32, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 * ((warp & 3) & 1), blk, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
+      }
       if (!mbar_wait(&bars->s_full[b], (i >> 1) & 1, ab)) goto done;
       tc_fence_after();
       uint32_t sr[64];
@@ -436,6 +566,7 @@ struct BwdCfg {
 struct BwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
   uint64_t qk_full[3], qk_empty[3], vdo_full[2], vdo_empty[2];
+  uint64_t qk_rot[3];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
   uint64_t drain;
@@ -453,7 +584,7 @@ __device__ __forceinline__ void st_row_piece(uint8_t* tile, int q, int c, int j,
                : "memory");
 }
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     block_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -470,12 +601,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->sched_full[s], 1);
-      mbar_init(&bars->sched_empty[s], C::SCHED_CONSUMERS);
+      mbar_init(&bars->sched_empty[s], C::SCHED_CONSUMERS + (ROPE ? 2 : 0));
     }
     mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
+      mbar_init(&bars->qk_rot[s], 2);
     }
     for (int s = 0; s < C::NVD; ++s) {
       mbar_init(&bars->vdo_full[s], 1);
@@ -575,7 +707,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int st = i % C::NQK, sv = i % C::NVD;
       const uint32_t q = smem_u32(smem + st * 2 * C::TILE), k = q + C::TILE;
       const uint32_t v = smem_u32(smem + C::OFF_V + sv * 2 * C::TILE), dO = v + C::TILE;
-      if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
+      if (!mbar_wait(ROPE ? &bars->qk_rot[st] : &bars->qk_full[st], (i / C::NQK) & 1, ab)) break;
       // S and dP reuse their columns once the softmax warps have read the
       // previous tile's (p_full and ds_full, waited below for that tile); with
       // the accumulators in the same columns, the epilogue must also be done
@@ -626,6 +758,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint64_t tw = global_timer_ns();
     while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
     }
+  } else if (ROPE && (warp == 2 || warp == 3)) {
+    // ---------------------------------------------------------------- rotation (rotary variant)
+    rope_role<D, C::NQK>(p, bars, smem, C::TILE, ab);
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- softmax, dS (and the epilogue at D = 128)
     const int r = threadIdx.x & 127;
@@ -857,7 +992,7 @@ done:
   }
 }
 
-template <int D>
+template <int D, bool ROPE>
 int launch_fwd_impl(const BlockArgs& a) {
   using C = FwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -869,7 +1004,7 @@ int launch_fwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_fwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -890,12 +1025,13 @@ int launch_fwd_impl(const BlockArgs& a) {
   p.chunk = a.chunk;
   p.n_tiles = a.n_tiles;
   p.n_chunks = a.n_chunks;
+  p.rope_tab = a.rope_tab;
   ProfileScope prof(kKindBlockFwd, a.stream);
-  block_fwd_kernel<D><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
+  block_fwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool ROPE>
 int launch_bwd_impl(const BlockArgs& a) {
   using C = BwdCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory budget");
@@ -911,7 +1047,7 @@ int launch_bwd_impl(const BlockArgs& a) {
   if (st != JFA_OK) return st;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([]() -> int {
-    return cudaFuncSetAttribute(block_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+    return cudaFuncSetAttribute(block_bwd_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
                    cudaSuccess
                ? JFA_OK
                : JFA_ERR_CUDA;
@@ -934,8 +1070,9 @@ int launch_bwd_impl(const BlockArgs& a) {
   p.chunk = a.chunk;
   p.n_tiles = a.n_tiles;
   p.n_chunks = a.n_chunks;
+  p.rope_tab = a.rope_tab;
   ProfileScope prof(kKindBlockBwd, a.stream);
-  block_bwd_kernel<D><<<a.use_clc ? a.n_chunks : a.n_prog, C::THREADS, C::SMEM, a.stream>>>(
+  block_bwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, C::THREADS, C::SMEM, a.stream>>>(
       tq, tk, tv, tdo, tdq, tdk, tdv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -943,10 +1080,14 @@ int launch_bwd_impl(const BlockArgs& a) {
 }  // namespace blk
 
 int launch_block_fwd(const BlockArgs& a) {
-  return a.D == 128 ? blk::launch_fwd_impl<128>(a) : blk::launch_fwd_impl<64>(a);
+  if (a.rope_tab != nullptr)
+    return a.D == 128 ? blk::launch_fwd_impl<128, true>(a) : blk::launch_fwd_impl<64, true>(a);
+  return a.D == 128 ? blk::launch_fwd_impl<128, false>(a) : blk::launch_fwd_impl<64, false>(a);
 }
 int launch_block_bwd(const BlockArgs& a) {
-  return a.D == 128 ? blk::launch_bwd_impl<128>(a) : blk::launch_bwd_impl<64>(a);
+  if (a.rope_tab != nullptr)
+    return a.D == 128 ? blk::launch_bwd_impl<128, true>(a) : blk::launch_bwd_impl<64, true>(a);
+  return a.D == 128 ? blk::launch_bwd_impl<128, false>(a) : blk::launch_bwd_impl<64, false>(a);
 }
 
 }  // namespace jfa

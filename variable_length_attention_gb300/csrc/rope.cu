@@ -1,5 +1,5 @@
-// rope.cu -- rotary position embedding passes of the rotary block-diagonal
-// entry points.
+// rope.cu -- the rotary block-diagonal entry points' table packing and the
+// backward's transposed-rotation pass.
 //
 // "TLX Block Attention" (introduction) reports its block kernel 3.5x faster
 // than the unfused baseline once the rotary embedding is fused into the
@@ -13,20 +13,20 @@
 // The transposed rotation carries a gradient with respect to the rotated rows
 // back to the unrotated ones.
 //
-// One pass over whole rows rather than a rotation inside the attention kernels:
-// the block kernels are HBM-bound at ~6 TB/s, and rotating their Q/K tiles in
-// shared memory made them wait on the table reads (two warps cannot keep the
-// 64 KB of fp32 table rows a tile needs in flight; measured 2.5-2.9x slower
-// than the kernel without rotary).  A pass that streams the rows with every
-// warp of the GPU runs at the HBM copy rate; it reads and writes Q and K (and
-// dQ, dK after the backward), as many bytes as the block forward moves.
+// The block kernels rotate Q and K tiles in shared memory as they land (block.cu)
+// from a packed table: pack_kernel turns the caller's fp32 cos/sin rows into one
+// half2 (cos, sin) per pair, half the bytes the rotation has to read per tile.
+// The backward's dQ and dK, computed with respect to the rotated rows, go back
+// through the transposed rotation in one streaming pass over their rows
+// (rope_kernel, in place), at the HBM copy rate.
 //
-// Layout: rows of [rows, H, D] bf16, one warp per row at a time, each lane one
-// 16-byte chunk of the first half of a head row together with its partner chunk
-// of the second half (8 column pairs), for one or two tensors (q and k share the
-// table reads).  Each warp walks a contiguous range of rows and finds the
-// position of its first row by a binary search over the sequence offsets.
+// rope_kernel layout: rows of [rows, H, D] bf16, one warp per row at a time, each
+// lane one 16-byte chunk of the first half of a head row together with its
+// partner chunk of the second half (8 column pairs), for one or two tensors (dq
+// and dk share the table reads).  Each warp walks a contiguous range of rows and
+// finds the position of its first row by a binary search over the offsets.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "host.h"
@@ -115,7 +115,29 @@ __global__ void __launch_bounds__(256, 4) rope_kernel(const __nv_bfloat16* in0, 
   }
 }
 
+// (cos, sin) -> one half2 per pair: the block kernels' rotation reads 4 bytes
+// per pair instead of 8 (fp16 keeps 11 significant bits of values in [-1, 1],
+// finer than the bf16 rounding of the rotated rows that follows)
+__global__ void pack_kernel(const float* __restrict__ cosv, const float* __restrict__ sinv, uint32_t* __restrict__ tab,
+                            long n) {
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const __half2 h = __floats2half2_rn(cosv[i], sinv[i]);
+    tab[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
 }  // namespace rope
+
+int launch_rope_pack(const float* rope_cos, const float* rope_sin, uint32_t* tab, long positions, int half_d,
+                     cudaStream_t stream) {
+  const long n = positions * half_d;
+  if (n == 0) return JFA_OK;
+  const int grid = static_cast<int>(std::min<long>((n + 255) / 256, 4096));
+  ProfileScope prof(kKindRope, stream);
+  rope::pack_kernel<<<grid, 256, 0, stream>>>(rope_cos, rope_sin, tab, n);
+  return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
 
 int launch_rope(const RopeArgs& a, int num_sms) {
   if (a.rows == 0) return JFA_OK;
