@@ -48,9 +48,9 @@ __global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __n
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  // eight rows' loads in flight at a time (a block is up to 256 rows, so one
-  // row at a time would leave the warp waiting on memory latency)
-  constexpr int U = 8;
+  // 32 rows' loads issued per round (a block is up to 256 rows, so one row at a
+  // time would leave the warp waiting on memory latency)
+  constexpr int U = 32;
   const size_t stride = static_cast<size_t>(heads) * D;
   const __nv_bfloat16* row0 = base + (static_cast<size_t>(t.x) * heads + t.z) * D + lane * PER;
   for (int r0 = 0; r0 < t.y; r0 += U) {
