@@ -891,9 +891,10 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
   st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
                     workspace_bytes, stream, &a, &tab, &tab_rows, &num_sms);
   if (st != JFA_OK || a.n_prog == 0) return st;
-  // the packed table, the block backward rotating q and k tiles as they land
-  // (its dq and dk are with respect to the rotated rows), then dq and dk carried
-  // back in place through the transposed rotation
+  // the packed table, the block backward rotating q and k tiles as they land;
+  // its dq and dk, with respect to the rotated rows, go back through the
+  // transposed rotation in the kernel's epilogue (head_dim 128) or in a pass
+  // after it, in place (head_dim 64, whose epilogue stores rows from registers)
   st = launch_rope_pack(rope_cos, rope_sin, tab, tab_rows, head_dim / 2, stream);
   if (st != JFA_OK) return st;
   a.rope_tab = tab;
@@ -902,7 +903,7 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
   a.dk = dk;
   a.dv = dv;
   st = launch_block_bwd(a);
-  if (st != JFA_OK) return st;
+  if (st != JFA_OK || head_dim == 128) return st;  // at head_dim 128 the kernel's epilogue rotates back
   RopeArgs back{dq, dq, dk, dk, rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 1, stream};
   return launch_rope(back, num_sms);
 }

@@ -9,11 +9,13 @@
 // recomputes P from Q and K, forms Di = rowsum(P o dP) inline, and every block
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
-// Rotary variants (a template parameter): two otherwise idle warps rotate each
-// tile's Q and K in shared memory as soon as TMA has landed them, from a packed
-// fp16 (cos, sin) table the entry point builds per call (rope.cu), and the score
-// GEMM waits for them; the backward's dQ and dK go back through the transposed
-// rotation in a pass after the kernel (rope.cu).
+// Rotary variants (a template parameter): each tile's Q and K are rotated in
+// shared memory as soon as TMA has landed them (forward: by the tile's softmax
+// warpgroup; backward: by two otherwise idle warps), from a packed fp16
+// (cos, sin) table the entry point builds per call (rope.cu), and the score GEMM
+// waits for them.  The backward's dQ and dK go back through the transposed
+// rotation in the staging buffer of its epilogue at D = 128, and in a pass after
+// the kernel at D = 64 (rope.cu).
 //
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
@@ -151,16 +153,22 @@ template <int D>
 __device__ __forceinline__ uint32_t rot_off(int row, int c) {
   return (c / 64) * 16384 + row * 128 + ((((c % 64) / 8) ^ (row & 7)) << 4);
 }
+template <bool TRANSPOSED>
 __device__ __forceinline__ uint32_t rot_word(uint32_t x, uint32_t y, uint32_t t0, uint32_t t1, bool second) {
-  // element pair of word x (first half) and y (second half) with tables t0, t1 (half2 cos, sin)
+  // element pair of word x (first half) and y (second half) with tables t0, t1
+  // (half2 cos, sin); the transposed rotation turns by the opposite angle
   const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
   const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&t0));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+  float2 a = __half22float2(*reinterpret_cast<const __half2*>(&t0));
+  float2 b = __half22float2(*reinterpret_cast<const __half2*>(&t1));
+  if (TRANSPOSED) {
+    a.y = -a.y;
+    b.y = -b.y;
+  }
   return second ? pack_bf16(v.x * a.x + u.x * a.y, v.y * b.x + u.y * b.y)
                 : pack_bf16(u.x * a.x - v.x * a.y, u.y * b.x - v.y * b.y);
 }
-template <int D, int NROWS, int B>
+template <int D, int NROWS, int B, int NT = 2, bool TRANSPOSED = false>
 __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint8_t* q_tile, uint8_t* k_tile,
                                           int half, int r0, const Blk& blk, int lane) {
   constexpr int CPR = D / 16;    // chunks in half a row
@@ -168,7 +176,7 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
   constexpr int NB = NROWS / RPS / B;
   const int j = lane % CPR, sub = lane / CPR;
   const int c1 = 8 * j, c2 = 8 * j + D / 2;
-  const uint32_t base[2] = {smem_u32(q_tile), smem_u32(k_tile)};
+  const uint32_t base[2] = {smem_u32(q_tile), NT == 2 ? smem_u32(k_tile) : 0u};
   uint4 t[2][B][2];  // table words of two batches: [buffer][step][pairs 0-3 | 4-7]
   auto load_tab = [&](int bi, int buf) {
 #pragma unroll
@@ -186,14 +194,14 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
   for (int bi = 0; bi < NB; ++bi) {
     const int buf = bi & 1;
     if (bi + 1 < NB) load_tab(bi + 1, buf ^ 1);
-    uint4 x[B][2], y[B][2];
+    uint4 x[B][NT], y[B][NT];
 #pragma unroll
     for (int st = 0; st < B; ++st) {
       const int rr = r0 + (bi * B + st) * RPS + sub;
       if (rr < blk.len) {
         const int row = 64 * half + rr;
 #pragma unroll
-        for (int tn = 0; tn < 2; ++tn) {
+        for (int tn = 0; tn < NT; ++tn) {
           const uint32_t a1 = base[tn] + rot_off<D>(row, c1), a2 = base[tn] + rot_off<D>(row, c2);
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x[st][tn].x), "=r"(x[st][tn].y), "=r"(x[st][tn].z), "=r"(x[st][tn].w) : "r"(a1));
@@ -210,14 +218,14 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
         const uint32_t tw[8] = {t[buf][st][0].x, t[buf][st][0].y, t[buf][st][0].z, t[buf][st][0].w,
                                 t[buf][st][1].x, t[buf][st][1].y, t[buf][st][1].z, t[buf][st][1].w};
 #pragma unroll
-        for (int tn = 0; tn < 2; ++tn) {
+        for (int tn = 0; tn < NT; ++tn) {
           const uint32_t xi[4] = {x[st][tn].x, x[st][tn].y, x[st][tn].z, x[st][tn].w};
           const uint32_t yi[4] = {y[st][tn].x, y[st][tn].y, y[st][tn].z, y[st][tn].w};
           uint32_t xo[4], yo[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            xo[w] = rot_word(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], false);
-            yo[w] = rot_word(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], true);
+            xo[w] = rot_word<TRANSPOSED>(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], false);
+            yo[w] = rot_word<TRANSPOSED>(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], true);
           }
           const uint32_t a1 = base[tn] + rot_off<D>(row, c1), a2 = base[tn] + rot_off<D>(row, c2);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(xo[0]), "r"(xo[1]), "r"(xo[2]),
@@ -882,7 +890,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
   #pragma unroll
               for (int e = 0; e < 4; ++e) st_row_piece(sP, r, c / 64, (c % 64) / 8 + e, w + 4 * e);
-              if (valid && !full_half) {
+              if (valid && !full_half && !(ROPE && which < 2)) {
   #pragma unroll
                 for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
               }
@@ -897,6 +905,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
               for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
               put(c, f);
+            }
+            if (ROPE && which < 2) {
+              // dQ and dK of the rotated rows go back through the transposed
+              // rotation in the staging buffer: each warp its own 32 rows, staged by
+              // its own threads, then (short block) the rows leave row by row
+              __syncwarp();
+              rope_rows<D, 32, 2, 1, true>(p.rope_tab, sP, nullptr, half, 32 * ((warp & 3) & 1), blk, lane);
+              __syncwarp();
+              if (valid && !full_half) {
+#pragma unroll
+                for (int c = 0; c < D; c += 8) {
+                  const uint32_t a = smem_u32(sP + (c / 64) * 16384 + r * 128 + ((((c % 64) / 8) ^ (r & 7)) << 4));
+                  uint32_t w0, w1, w2, w3;
+                  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(a));
+                  st_global_v4(dst + c, w0, w1, w2, w3);
+                }
+              }
             }
             if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
               tc_fence_before();

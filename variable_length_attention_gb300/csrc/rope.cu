@@ -16,9 +16,10 @@
 // The block kernels rotate Q and K tiles in shared memory as they land (block.cu)
 // from a packed table: pack_kernel turns the caller's fp32 cos/sin rows into one
 // half2 (cos, sin) per pair, half the bytes the rotation has to read per tile.
-// The backward's dQ and dK, computed with respect to the rotated rows, go back
-// through the transposed rotation in one streaming pass over their rows
-// (rope_kernel, in place), at the HBM copy rate.
+// At head_dim 64 the backward's dQ and dK, computed with respect to the rotated
+// rows, go back through the transposed rotation in one streaming pass over their
+// rows (rope_kernel, in place), at the HBM copy rate; at head_dim 128 the
+// backward kernel's epilogue does it.
 //
 // rope_kernel layout: rows of [rows, H, D] bf16, one warp per row at a time, each
 // lane one 16-byte chunk of the first half of a head row together with its
