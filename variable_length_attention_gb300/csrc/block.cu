@@ -238,11 +238,12 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
   }
 }
 
-// The rotation role of the rotary backward (warps 2 and 3): every tile's Q and
-// K once their slot has landed, warp 2 the tile's first block and warp 3 its
-// second; the score GEMM waits for qk_rot.  (In the forward the tile's softmax
-// warpgroup rotates it, a quarter per warp, while it waits for its scores.)
-template <int D, int NQK, class Bars>
+// The rotation role of the rotary variants (warps 2 and 3): every tile's Q and
+// K once their slot has landed, warp 2 rows [0, NROWS) of the tile's first block
+// and warp 3 those of its second; the score GEMM waits for qk_rot.  In the
+// backward NROWS is the whole block; in the forward the tile's softmax
+// warpgroup rotates the rest while it waits for its scores.
+template <int D, int NQK, int NROWS, int B, class Bars>
 __device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* smem, int tile_bytes, const Abort& ab) {
   const int half = warp_id() - 2, lane = lane_id();
   TileCursor cur;
@@ -252,7 +253,7 @@ __device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* 
     const int st = i % NQK;
     if (!mbar_wait(&bars->qk_full[st], (i / NQK) & 1, ab)) break;
     uint8_t* q_tile = smem + st * 2 * tile_bytes;
-    rope_rows<D, 64, 4>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half), lane);
+    rope_rows<D, NROWS, B>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half), lane);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
@@ -286,7 +287,8 @@ struct FwdBars {
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr int kFwdSchedConsumers = 9;  // the MMA thread and the 8 softmax warps
+// the MMA thread and the 8 softmax warps (and the rotary variant's 2 rotation warps)
+constexpr int kFwdSchedConsumers = 9;
 
 // Loads rows [row0, row0+64) of every 64-column chunk of head h into rows
 // [64*half, 64*half+64) of a 128-row swizzled tile.
@@ -310,13 +312,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->sched_full[s], 1);
-      mbar_init(&bars->sched_empty[s], kFwdSchedConsumers);
+      mbar_init(&bars->sched_empty[s], kFwdSchedConsumers + (ROPE ? 2 : 0));
     }
     mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
-      mbar_init(&bars->qk_rot[s], 4);  // the tile's softmax warpgroup
+      mbar_init(&bars->qk_rot[s], 6);  // the 2 rotation warps and the tile's softmax warpgroup
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -451,6 +453,9 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t tw = global_timer_ns();
     while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
     }
+  } else if (ROPE && (warp == 2 || warp == 3)) {
+    // ---------------------------------------------------------------- rotation (rotary variant): rows 0-31 of each block
+    rope_role<D, C::NQK, 32, 2>(p, bars, smem, C::TILE, ab);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
     const int b = (warp - 4) >> 2;          // TMEM buffer / tile parity of this warpgroup
@@ -469,11 +474,11 @@ __global__ void __launch_bounds__(384, 1)
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
       const int rr = r & 63;
-      if constexpr (ROPE) {  // this warpgroup rotates its own tile's Q and K, 32 rows per warp
+      if constexpr (ROPE) {  // rows 32-63 of each block of its own tile, 16 per warp (the rotation warps take 0-31)
         const int st = i % C::NQK;
         if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) goto done;
         uint8_t* q_tile = smem + st * 2 * C::TILE;
-        rope_rows<D, 32, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 * ((warp & 3) & 1), blk, lane);
+        rope_rows<D, 16, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 + 16 * ((warp & 3) & 1), blk, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
@@ -768,7 +773,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (ROPE && (warp == 2 || warp == 3)) {
     // ---------------------------------------------------------------- rotation (rotary variant)
-    rope_role<D, C::NQK>(p, bars, smem, C::TILE, ab);
+    rope_role<D, C::NQK, 64, 4>(p, bars, smem, C::TILE, ab);
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- softmax, dS (and the epilogue at D = 128)
     const int r = threadIdx.x & 127;
