@@ -168,9 +168,14 @@ __device__ __forceinline__ uint32_t rot_word(uint32_t x, uint32_t y, uint32_t t0
   return second ? pack_bf16(v.x * a.x + u.x * a.y, v.y * b.x + u.y * b.y)
                 : pack_bf16(u.x * a.x - v.x * a.y, u.y * b.x - v.y * b.y);
 }
-template <int D, int NROWS, int B, int NT = 2, bool TRANSPOSED = false>
-__device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint8_t* q_tile, uint8_t* k_tile,
-                                          int half, int r0, const Blk& blk, int lane) {
+// `ready` is called once the first batch's table rows are on their way (it waits
+// for the tile to land, so the table latency overlaps that wait); false aborts.
+struct NoWait {
+  __device__ bool operator()() const { return true; }
+};
+template <int D, int NROWS, int B, int NT = 2, bool TRANSPOSED = false, class Ready = NoWait>
+__device__ __forceinline__ bool rope_rows(const uint32_t* __restrict__ tab, uint8_t* q_tile, uint8_t* k_tile,
+                                          int half, int r0, const Blk& blk, int lane, Ready ready = Ready()) {
   constexpr int CPR = D / 16;    // chunks in half a row
   constexpr int RPS = 32 / CPR;  // rows per step; B steps per batch
   constexpr int NB = NROWS / RPS / B;
@@ -190,6 +195,7 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
     }
   };
   load_tab(0, 0);
+  if (!ready()) return false;
 #pragma unroll
   for (int bi = 0; bi < NB; ++bi) {
     const int buf = bi & 1;
@@ -236,6 +242,7 @@ __device__ __forceinline__ void rope_rows(const uint32_t* __restrict__ tab, uint
       }
     }
   }
+  return true;
 }
 
 // The rotation role of the rotary variants (warps 2 and 3): every tile's Q and
@@ -251,9 +258,10 @@ __device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* 
     const int t = next_tile(cur, bars, p, ab, true);
     if (t < 0) break;
     const int st = i % NQK;
-    if (!mbar_wait(&bars->qk_full[st], (i / NQK) & 1, ab)) break;
     uint8_t* q_tile = smem + st * 2 * tile_bytes;
-    rope_rows<D, NROWS, B>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half), lane);
+    if (!rope_rows<D, NROWS, B>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half),
+                                lane, [&] { return mbar_wait(&bars->qk_full[st], (i / NQK) & 1, ab); }))
+      break;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
@@ -476,9 +484,10 @@ __global__ void __launch_bounds__(384, 1)
       const int rr = r & 63;
       if constexpr (ROPE) {  // rows 32-63 of each block of its own tile, 16 per warp (the rotation warps take 0-31)
         const int st = i % C::NQK;
-        if (!mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab)) goto done;
         uint8_t* q_tile = smem + st * 2 * C::TILE;
-        rope_rows<D, 16, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 + 16 * ((warp & 3) & 1), blk, lane);
+        if (!rope_rows<D, 16, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 + 16 * ((warp & 3) & 1), blk, lane,
+                                 [&] { return mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab); }))
+          goto done;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
