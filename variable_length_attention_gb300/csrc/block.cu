@@ -909,23 +909,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
               }
             };
+            // the result row into the staging buffer, 32 columns at a time
+            auto stage = [&]() {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_addr + col + c, v);
-              tmem_wait_ld();
-              reg_fence<32>(v);
-              float f[32];
+              for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + col + c, v);
+                tmem_wait_ld();
+                reg_fence<32>(v);
+                float f[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
-              put(c, f);
-            }
-            if (ROPE && which < 2) {
+                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
+                put(c, f);
+              }
+            };
+            if (!(ROPE && which < 2)) {
+              stage();
+            } else {
               // dQ and dK of the rotated rows go back through the transposed
               // rotation in the staging buffer: each warp its own 32 rows, staged by
-              // its own threads, then (short block) the rows leave row by row
-              __syncwarp();
-              rope_rows<D, 32, 2, 1, true>(p.rope_tab, sP, nullptr, half, 32 * ((warp & 3) & 1), blk, lane);
+              // its own threads (while the first table rows load), then (short
+              // block) the rows leave row by row
+              rope_rows<D, 32, 2, 1, true>(p.rope_tab, sP, nullptr, half, 32 * ((warp & 3) & 1), blk, lane, [&] {
+                stage();
+                __syncwarp();
+                return true;
+              });
               __syncwarp();
               if (valid && !full_half) {
 #pragma unroll
