@@ -231,9 +231,10 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
  * in shared memory, from the tables packed into the workspace as (cos, sin)
  * fp16 pairs, whose size is jfa_workspace_size(JFA_OP_BLOCK_FWD_ROPE or
  * JFA_OP_BLOCK_BWD_ROPE, ...) (the plain size plus longest sequence x
- * head_dim/2 x 4 bytes); the backward carries dq and dk back through the
- * transposed rotation in one pass after its kernel.  Errors as block_attn_*,
- * plus JFA_ERR_INVALID_ARG for missing, misaligned or too short tables.
+ * head_dim/2 x 4 bytes); the backward kernel's epilogue carries dq and dk
+ * back through the transposed rotation before it stores them.  Errors as
+ * block_attn_*, plus JFA_ERR_INVALID_ARG for missing, misaligned or too short
+ * tables.
  */
 int block_attn_fwd_rope(const void* q, const void* k, const void* v, void* o, const float* rope_cos,
                         const float* rope_sin, int rope_rows, const int32_t* offsets_dev,
@@ -392,7 +393,7 @@ int jfa_get_block_schedule(void);
  * unselected kind) and the launch count of one kernel kind: 0 forward,
  * 1 backward prepass (Di), 2 backward main, 3 dQ convert, 4 block forward,
  * 5 block backward, 6 empty-sequence fill, 7 top-k selection, 8 rotary table
- * packing and the backward's transposed-rotation pass.
+ * packing.
  */
 /*
  * Failure-path self-test (no counterpart on the pages; failure detection).

@@ -782,7 +782,7 @@ extern "C" int jfa_bwd_window(const void* q, const void* k, const void* v, const
 static int block_common(const void* q, const void* k, const void* v, const void* out0, const int32_t* offsets_dev,
                         const int32_t* offsets_host, int batch, int max_len, int num_heads, int head_dim, float scale,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream, BlockArgs* a,
-                        uint32_t** tab = nullptr, int64_t* tab_rows = nullptr, int* num_sms = nullptr) {
+                        uint32_t** tab = nullptr, int64_t* tab_rows = nullptr) {
   Common c;
   int st = validate_common(q, k, v, out0, offsets_dev, offsets_host, batch, max_len, 0, num_heads, num_heads,
                            head_dim, scale, 0, 0, &c);
@@ -799,7 +799,6 @@ static int block_common(const void* q, const void* k, const void* v, const void*
     *tab = reinterpret_cast<uint32_t*>(ws + lay.tab);
     *tab_rows = rows_tab;
   }
-  if (num_sms) *num_sms = c.dev.num_sms;
   a->q = q;
   a->k = k;
   a->v = v;
@@ -887,14 +886,12 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
   BlockArgs a{};
   uint32_t* tab = nullptr;
   int64_t tab_rows = 0;
-  int num_sms = 0;
   st = block_common(q, k, v, dq, offsets_dev, offsets_host, batch, max_len, num_heads, head_dim, scale, workspace,
-                    workspace_bytes, stream, &a, &tab, &tab_rows, &num_sms);
+                    workspace_bytes, stream, &a, &tab, &tab_rows);
   if (st != JFA_OK || a.n_prog == 0) return st;
   // the packed table, the block backward rotating q and k tiles as they land;
   // its dq and dk, with respect to the rotated rows, go back through the
-  // transposed rotation in the kernel's epilogue (head_dim 128) or in a pass
-  // after it, in place (head_dim 64, whose epilogue stores rows from registers)
+  // transposed rotation in the kernel's epilogue
   st = launch_rope_pack(rope_cos, rope_sin, tab, tab_rows, head_dim / 2, stream);
   if (st != JFA_OK) return st;
   a.rope_tab = tab;
@@ -902,10 +899,7 @@ extern "C" int block_attn_bwd_rope(const void* q, const void* k, const void* v, 
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  st = launch_block_bwd(a);
-  if (st != JFA_OK || head_dim == 128) return st;  // at head_dim 128 the kernel's epilogue rotates back
-  RopeArgs back{dq, dq, dk, dk, rope_cos, rope_sin, offsets_dev, batch, a.rows, num_heads, head_dim, 1, stream};
-  return launch_rope(back, num_sms);
+  return launch_block_bwd(a);
 }
 
 extern "C" int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, void* dq,

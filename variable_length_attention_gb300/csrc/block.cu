@@ -10,12 +10,12 @@
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
 // Rotary variants (a template parameter): each tile's Q and K are rotated in
-// shared memory as soon as TMA has landed them (forward: by the tile's softmax
-// warpgroup; backward: by two otherwise idle warps), from a packed fp16
-// (cos, sin) table the entry point builds per call (rope.cu), and the score GEMM
-// waits for them.  The backward's dQ and dK go back through the transposed
-// rotation in the staging buffer of its epilogue at D = 128, and in a pass after
-// the kernel at D = 64 (rope.cu).
+// shared memory as soon as TMA has landed them (forward: two otherwise idle
+// warps take rows 0-31 of each block and the tile's softmax warpgroup the rest;
+// backward: the two warps all of it), from a packed fp16 (cos, sin) table the
+// entry point builds per call (rope.cu), and the score GEMM waits for them.  The
+// backward's dQ and dK go back through the transposed rotation in its epilogue:
+// in the staging buffer at D = 128, on the fp32 rows in registers at D = 64.
 //
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
@@ -993,16 +993,66 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (t < 0) break;
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
+      const bool valid = rr < blk.len;
+      // rotary: the table row of this thread's token (32 pairs), loaded while
+      // the tile's GEMMs finish; dQ and dK share it
+      uint4 tab[ROPE ? D / 8 : 1];
+      if constexpr (ROPE && D == 64) {
+        if (valid) {
+          const uint4* e = reinterpret_cast<const uint4*>(p.rope_tab + static_cast<size_t>(blk.pos0 + rr) * (D / 2));
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j) tab[j] = __ldg(e + j);
+        }
+      }
       if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
       tc_fence_after();
       {
-        const bool valid = rr < blk.len;
         const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
 #pragma unroll 1
         for (int which = 0; which < 3; ++which) {
           const uint32_t col = which == 0 ? COL_DQ : (which == 1 ? COL_DK : COL_DV);
           const float mul = which == 2 ? 1.0f : p.scale;
           __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+          if constexpr (ROPE && D == 64) {
+            if (which < 2) {
+              // dQ and dK are gradients with respect to the rotated rows: the
+              // transposed rotation of the whole fp32 row, pairs (i, i + D/2),
+              // (g_i, g_i') -> (g_i c + g_i' s, g_i' c - g_i s), rounded once
+              uint32_t v[D];
+              tmem_ld32(tmem + lane_addr + col, v);
+              tmem_ld32(tmem + lane_addr + col + 32, v + 32);
+              tmem_wait_ld();
+              reg_fence<D>(v);
+              if (valid) {
+                const uint32_t tw[D / 2] = {
+#define JFA_TW(j) tab[j].x, tab[j].y, tab[j].z, tab[j].w
+                    JFA_TW(0), JFA_TW(1), JFA_TW(2), JFA_TW(3), JFA_TW(4), JFA_TW(5), JFA_TW(6), JFA_TW(7)
+#undef JFA_TW
+                };
+                uint32_t wx[D / 4], wy[D / 4];
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e) {
+                  float xo[2], yo[2];
+#pragma unroll
+                  for (int k = 0; k < 2; ++k) {
+                    const int i = 2 * e + k;
+                    const float2 cs = __half22float2(*reinterpret_cast<const __half2*>(&tw[i]));
+                    const float x = __uint_as_float(v[i]) * mul, y = __uint_as_float(v[i + D / 2]) * mul;
+                    xo[k] = x * cs.x + y * cs.y;
+                    yo[k] = y * cs.x - x * cs.y;
+                  }
+                  wx[e] = pack_bf16(xo[0], xo[1]);
+                  wy[e] = pack_bf16(yo[0], yo[1]);
+                }
+#pragma unroll
+                for (int e = 0; e < D / 16; ++e) {
+                  st_global_v4(dst + 8 * e, wx[4 * e], wx[4 * e + 1], wx[4 * e + 2], wx[4 * e + 3]);
+                  st_global_v4(dst + D / 2 + 8 * e, wy[4 * e], wy[4 * e + 1], wy[4 * e + 2], wy[4 * e + 3]);
+                }
+              }
+              continue;
+            }
+          }
           // columns c..c+31 of the result row, as fp32, stored
           auto put = [&](int c, const float* f) {
             if (!valid) return;
