@@ -12,10 +12,10 @@
 // Rotary variants (a template parameter): each tile's Q and K are rotated in
 // shared memory as soon as TMA has landed them (forward: two otherwise idle
 // warps take rows 0-31 of each block and the tile's softmax warpgroup the rest;
-// backward: the two warps all of it), from a packed fp16 (cos, sin) table the
+// backward: the two warps all of it), from a packed fp16 cos/sin table the
 // entry point builds per call (rope.cu), and the score GEMM waits for them.  The
-// backward's dQ and dK go back through the transposed rotation in its epilogue:
-// in the staging buffer at D = 128, on the fp32 rows in registers at D = 64.
+// backward's dQ and dK go back through the transposed rotation in its epilogue,
+// each thread on its own fp32 row as it comes out of TMEM, before rounding.
 //
 // Tiles: the tensor-core MMA used here has 128 rows, so a tile stacks two
 // consecutive global blocks (2p, 2p+1) of one head: rows 0-63 are block 2p,
@@ -56,7 +56,8 @@ struct Params {
   float scale, scale_log2;
   int use_clc;                // 1: one CTA per chunk of `chunk` tiles, Cluster Launch Control
   int chunk, n_tiles, n_chunks;
-  const uint32_t* rope_tab;   // rotary variant: (cos, sin) as half2, [positions, D/2]
+  const uint32_t* rope_tab;   // rotary variant: packed table, [positions, D/2] words (rope.h:
+                              // word 2m: cos of pairs 2m, 2m+1 as half2; word 2m+1: their sines)
 };
 
 // Tiles [*tb, *te) of schedule entry `ch`: chunk ch under Cluster Launch
@@ -120,24 +121,36 @@ struct Blk {
   int pos0;  // position of the block's first row inside its sequence
 };
 
-__device__ __forceinline__ Blk locate(const Params& p, int g) {
-  Blk r{0, 0, 0};
-  if (g >= p.n_blocks) return r;
-  // largest b in [0, batch) with bpb[b] <= g (branchless halving search)
-  int lo = 0, n = p.batch;
-  while (n > 1) {
-    const int half = n >> 1;
-    lo = (__ldg(p.bpb + lo + half) <= g) ? lo + half : lo;
-    n -= half;
+// Global block g -> its rows.  Each role walks the tiles in ascending block
+// order, the heads of a pair one after another and most pairs inside the
+// sequence of the previous one, so the sequence found last is kept and the
+// search (a chain of dependent loads) runs only when g leaves it.
+struct Locator {
+  int g_lo = 0, g_hi = 0;  // blocks [g_lo, g_hi) are those of the kept sequence
+  int s = 0, L = 0;        // its first row and length
+  __device__ __forceinline__ Blk operator()(const Params& p, int g) {
+    Blk r{0, 0, 0};
+    if (g >= p.n_blocks) return r;
+    if (g < g_lo || g >= g_hi) {
+      // largest b in [0, batch) with bpb[b] <= g (branchless halving search)
+      int lo = 0, n = p.batch;
+      while (n > 1) {
+        const int half = n >> 1;
+        lo = (__ldg(p.bpb + lo + half) <= g) ? lo + half : lo;
+        n -= half;
+      }
+      g_lo = __ldg(p.bpb + lo);
+      g_hi = __ldg(p.bpb + lo + 1);
+      s = __ldg(p.offsets + lo);
+      L = __ldg(p.offsets + lo + 1) - s;
+    }
+    const int j = g - g_lo;
+    r.row0 = s + kBlk * j;
+    r.len = min(kBlk, L - kBlk * j);
+    r.pos0 = kBlk * j;
+    return r;
   }
-  const int j = g - __ldg(p.bpb + lo);
-  const int s = __ldg(p.offsets + lo);
-  const int L = __ldg(p.offsets + lo + 1) - s;
-  r.row0 = s + kBlk * j;
-  r.len = min(kBlk, L - kBlk * j);
-  r.pos0 = kBlk * j;
-  return r;
-}
+};
 
 // Rotates Q and K rows [r0, r0 + NROWS) of one 64-row half of a tile pair in place, each tile
 // stored as D/64 128-byte-swizzled 64-column boxes: for i < D/2 the pair
@@ -153,36 +166,44 @@ template <int D>
 __device__ __forceinline__ uint32_t rot_off(int row, int c) {
   return (c / 64) * 16384 + row * 128 + ((((c % 64) / 8) ^ (row & 7)) << 4);
 }
+// Two column pairs of a row: u holds elements (i, i+1) of the first half, v
+// their partners (i + D/2, i + 1 + D/2), c and s the pairs' cosines and sines;
+// the rotation turns (u, v) into (u c - v s, v c + u s), its transpose into
+// (u c + v s, v c - u s), in paired fp32 arithmetic.
 template <bool TRANSPOSED>
-__device__ __forceinline__ uint32_t rot_word(uint32_t x, uint32_t y, uint32_t t0, uint32_t t1, bool second) {
-  // element pair of word x (first half) and y (second half) with tables t0, t1
-  // (half2 cos, sin); the transposed rotation turns by the opposite angle
-  const float2 u = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
-  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&y));
-  float2 a = __half22float2(*reinterpret_cast<const __half2*>(&t0));
-  float2 b = __half22float2(*reinterpret_cast<const __half2*>(&t1));
-  if (TRANSPOSED) {
-    a.y = -a.y;
-    b.y = -b.y;
-  }
-  return second ? pack_bf16(v.x * a.x + u.x * a.y, v.y * b.x + u.y * b.y)
-                : pack_bf16(u.x * a.x - v.x * a.y, u.y * b.x - v.y * b.y);
+__device__ __forceinline__ void rot2(uint64_t u, uint64_t v, uint64_t c, uint64_t s, uint64_t& uo, uint64_t& vo) {
+  const uint64_t ns = fmul2(s, f32x2(-1.0f, -1.0f));
+  uo = ffma2(v, TRANSPOSED ? s : ns, fmul2(u, c));
+  vo = ffma2(u, TRANSPOSED ? ns : s, fmul2(v, c));
+}
+__device__ __forceinline__ uint64_t h2_to_f32x2(uint32_t w) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+  return f32x2(f.x, f.y);
+}
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t r) {
+  float lo, hi;
+  f32x2_split(r, lo, hi);
+  return pack_bf16(lo, hi);
 }
 // `ready` is called once the first batch's table rows are on their way (it waits
 // for the tile to land, so the table latency overlaps that wait); false aborts.
 struct NoWait {
   __device__ bool operator()() const { return true; }
 };
-template <int D, int NROWS, int B, int NT = 2, bool TRANSPOSED = false, class Ready = NoWait>
+template <int D, int NROWS, int B, class Ready = NoWait>
 __device__ __forceinline__ bool rope_rows(const uint32_t* __restrict__ tab, uint8_t* q_tile, uint8_t* k_tile,
                                           int half, int r0, const Blk& blk, int lane, Ready ready = Ready()) {
   constexpr int CPR = D / 16;    // chunks in half a row
   constexpr int RPS = 32 / CPR;  // rows per step; B steps per batch
   constexpr int NB = NROWS / RPS / B;
+  constexpr int NT = 2;          // tensors: q and k
   const int j = lane % CPR, sub = lane / CPR;
   const int c1 = 8 * j, c2 = 8 * j + D / 2;
-  const uint32_t base[2] = {smem_u32(q_tile), NT == 2 ? smem_u32(k_tile) : 0u};
-  uint4 t[2][B][2];  // table words of two batches: [buffer][step][pairs 0-3 | 4-7]
+  const uint32_t base[2] = {smem_u32(q_tile), smem_u32(k_tile)};
+  uint4 t[2][B][2];  // table words of the chunk's 8 pairs: [buffer][step][pairs 0-3 | 4-7]
   auto load_tab = [&](int bi, int buf) {
 #pragma unroll
     for (int st = 0; st < B; ++st) {
@@ -221,8 +242,10 @@ __device__ __forceinline__ bool rope_rows(const uint32_t* __restrict__ tab, uint
       const int rr = r0 + (bi * B + st) * RPS + sub;
       if (rr < blk.len) {
         const int row = 64 * half + rr;
-        const uint32_t tw[8] = {t[buf][st][0].x, t[buf][st][0].y, t[buf][st][0].z, t[buf][st][0].w,
-                                t[buf][st][1].x, t[buf][st][1].y, t[buf][st][1].z, t[buf][st][1].w};
+        // word pairs (cos of pairs 2w, 2w+1; their sin)
+        const uint4* tt = t[buf][st];
+        const uint64_t cw[4] = {h2_to_f32x2(tt[0].x), h2_to_f32x2(tt[0].z), h2_to_f32x2(tt[1].x), h2_to_f32x2(tt[1].z)};
+        const uint64_t sw[4] = {h2_to_f32x2(tt[0].y), h2_to_f32x2(tt[0].w), h2_to_f32x2(tt[1].y), h2_to_f32x2(tt[1].w)};
 #pragma unroll
         for (int tn = 0; tn < NT; ++tn) {
           const uint32_t xi[4] = {x[st][tn].x, x[st][tn].y, x[st][tn].z, x[st][tn].w};
@@ -230,8 +253,10 @@ __device__ __forceinline__ bool rope_rows(const uint32_t* __restrict__ tab, uint
           uint32_t xo[4], yo[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            xo[w] = rot_word<TRANSPOSED>(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], false);
-            yo[w] = rot_word<TRANSPOSED>(xi[w], yi[w], tw[2 * w], tw[2 * w + 1], true);
+            uint64_t uo, vo;
+            rot2<false>(bf16x2_to_f32x2(xi[w]), bf16x2_to_f32x2(yi[w]), cw[w], sw[w], uo, vo);
+            xo[w] = f32x2_to_bf16x2(uo);
+            yo[w] = f32x2_to_bf16x2(vo);
           }
           const uint32_t a1 = base[tn] + rot_off<D>(row, c1), a2 = base[tn] + rot_off<D>(row, c2);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(xo[0]), "r"(xo[1]), "r"(xo[2]),
@@ -254,6 +279,7 @@ template <int D, int NQK, int NROWS, int B, class Bars>
 __device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* smem, int tile_bytes, const Abort& ab) {
   const int half = warp_id() - 2, lane = lane_id();
   TileCursor cur;
+  Locator locate;
   for (int i = 0;; ++i) {
     const int t = next_tile(cur, bars, p, ab, true);
     if (t < 0) break;
@@ -359,6 +385,7 @@ __global__ void __launch_bounds__(384, 1)
     // across the heads, so the block search runs once per pair, not per load.
     int cached_pair = -1;
     Blk ca{0, 0}, cb{0, 0};
+    Locator locate;
     auto rows = [&](int t, Blk& a, Blk& b, int& h) {
       const int pair = t / p.H;
       h = t % p.H;
@@ -474,6 +501,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tO = tS + 128;
     const float sl2 = p.scale_log2;
     TileCursor cur;
+    Locator locate;
     for (int i = 0;; ++i) {
       const int t = next_tile(cur, bars, p, ab, true);
       if (t == -2) goto done;
@@ -665,6 +693,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // search runs once per pair of blocks, shared by the pair's heads.
     int cached_pair = -1;
     Blk ca{0, 0}, cb{0, 0};
+    Locator locate;
     auto rows = [&](int t, Blk& a, Blk& b, int& h) {
       const int pair = t / p.H;
       h = t % p.H;
@@ -782,7 +811,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (ROPE && (warp == 2 || warp == 3)) {
     // ---------------------------------------------------------------- rotation (rotary variant)
-    rope_role<D, C::NQK, 64, 4>(p, bars, smem, C::TILE, ab);
+    rope_role<D, C::NQK, 64, D == 128 ? 4 : 2>(p, bars, smem, C::TILE, ab);
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- softmax, dS (and the epilogue at D = 128)
     const int r = threadIdx.x & 127;
@@ -794,6 +823,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
     uint32_t stg_full_ph = 0, stg_free_ph = 0;
     TileCursor cur;
+    Locator locate;
     for (int i = 0;; ++i) {
       const int t = next_tile(cur, bars, p, ab, true);
       if (t == -2) goto done;
@@ -876,6 +906,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // of the next block are touched.
         // thread 128 (row 0, block a) issues the stores; it also needs block b
         const Blk blk_a = blk, blk_b = threadIdx.x == 128 ? locate(p, 2 * pair + 1) : blk;
+        // rotary: the table row of this thread's token (64 pairs), loaded while
+        // the tile's last GEMMs run; dQ and dK share it
+        uint4 tab[ROPE ? D / 8 : 1];
+        if constexpr (ROPE) {
+          const uint4* e = reinterpret_cast<const uint4*>(p.rope_tab + static_cast<size_t>(blk.pos0 + rr) * (D / 2));
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j) tab[j] = rr < blk.len ? __ldg(e + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (!mbar_wait(&bars->acc_full, i & 1, ab)) goto done;
         tc_fence_after();
         {
@@ -896,54 +934,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
               stg_free_ph ^= 1;
             }
-            // columns c..c+31 of the result row, as fp32: staged (pieces (c%64)/8 ..
-            // (c%64)/8+3 of the 64-column box c/64) and, for a short block, stored
-            auto put = [&](int c, const float* f) {
-              uint32_t w[16];
-  #pragma unroll
-              for (int e = 0; e < 16; ++e) w[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
+            // columns c..c+31 of the result row, as bf16 pairs: staged (pieces
+            // (c%64)/8 .. (c%64)/8+3 of the 64-column box c/64) and, for a short
+            // block, stored
+            auto put = [&](int c, const uint32_t* w) {
   #pragma unroll
               for (int e = 0; e < 4; ++e) st_row_piece(sP, r, c / 64, (c % 64) / 8 + e, w + 4 * e);
-              if (valid && !full_half && !(ROPE && which < 2)) {
+              if (valid && !full_half) {
   #pragma unroll
                 for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
               }
             };
-            // the result row into the staging buffer, 32 columns at a time
-            auto stage = [&]() {
+            if (!(ROPE && which < 2)) {
+              // the result row into the staging buffer, 32 columns at a time
 #pragma unroll 1
               for (int c = 0; c < D; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_addr + col + c, v);
                 tmem_wait_ld();
                 reg_fence<32>(v);
-                float f[32];
+                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]) * mul;
-                put(c, f);
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                put(c, w);
               }
-            };
-            if (!(ROPE && which < 2)) {
-              stage();
             } else {
-              // dQ and dK of the rotated rows go back through the transposed
-              // rotation in the staging buffer: each warp its own 32 rows, staged by
-              // its own threads (while the first table rows load), then (short
-              // block) the rows leave row by row
-              rope_rows<D, 32, 2, 1, true>(p.rope_tab, sP, nullptr, half, 32 * ((warp & 3) & 1), blk, lane, [&] {
-                stage();
-                __syncwarp();
-                return true;
-              });
-              __syncwarp();
-              if (valid && !full_half) {
+              // dQ and dK are gradients with respect to the rotated rows: the
+              // transposed rotation of the fp32 row, pairs (i, i + D/2), before
+              // it is rounded and staged; 32 pairs per round
+              const uint64_t sc = f32x2(mul, mul);
+#pragma unroll 1
+              for (int r2 = 0; r2 < 2; ++r2) {
+                uint32_t vx[32], vy[32];
+                tmem_ld32(tmem + lane_addr + col + 32 * r2, vx);
+                tmem_ld32(tmem + lane_addr + col + D / 2 + 32 * r2, vy);
+                tmem_wait_ld();
+                reg_fence<32>(vx);
+                reg_fence<32>(vy);
+                uint32_t wx[16], wy[16];
 #pragma unroll
-                for (int c = 0; c < D; c += 8) {
-                  const uint32_t a = smem_u32(sP + (c / 64) * 16384 + r * 128 + ((((c % 64) / 8) ^ (r & 7)) << 4));
-                  uint32_t w0, w1, w2, w3;
-                  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(a));
-                  st_global_v4(dst + c, w0, w1, w2, w3);
+                for (int e = 0; e < 16; ++e) {
+                  // cos and sin of pairs (32 r2 + 2e, +1), times the softmax scale
+                  const uint4& tq = tab[8 * r2 + e / 2];
+                  const uint64_t c = fmul2(h2_to_f32x2(e & 1 ? tq.z : tq.x), sc);
+                  const uint64_t sn = fmul2(h2_to_f32x2(e & 1 ? tq.w : tq.y), sc);
+                  uint64_t uo, vo;
+                  rot2<true>(f32x2(__uint_as_float(vx[2 * e]), __uint_as_float(vx[2 * e + 1])),
+                             f32x2(__uint_as_float(vy[2 * e]), __uint_as_float(vy[2 * e + 1])), c, sn, uo, vo);
+                  wx[e] = f32x2_to_bf16x2(uo);
+                  wy[e] = f32x2_to_bf16x2(vo);
                 }
+                put(32 * r2, wx);
+                put(D / 2 + 32 * r2, wy);
               }
             }
             if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
@@ -987,6 +1029,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int half = r >> 6, rr = r & 63;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     TileCursor cur;
+    Locator locate;
     for (int i = 0;; ++i) {
       const int t = next_tile(cur, bars, p, ab, true);
       if (t == -2) goto done;
@@ -1018,36 +1061,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               // dQ and dK are gradients with respect to the rotated rows: the
               // transposed rotation of the whole fp32 row, pairs (i, i + D/2),
               // (g_i, g_i') -> (g_i c + g_i' s, g_i' c - g_i s), rounded once
-              uint32_t v[D];
-              tmem_ld32(tmem + lane_addr + col, v);
-              tmem_ld32(tmem + lane_addr + col + 32, v + 32);
-              tmem_wait_ld();
-              reg_fence<D>(v);
-              if (valid) {
-                const uint32_t tw[D / 2] = {
-#define JFA_TW(j) tab[j].x, tab[j].y, tab[j].z, tab[j].w
-                    JFA_TW(0), JFA_TW(1), JFA_TW(2), JFA_TW(3), JFA_TW(4), JFA_TW(5), JFA_TW(6), JFA_TW(7)
-#undef JFA_TW
-                };
-                uint32_t wx[D / 4], wy[D / 4];
+              const uint64_t sc = f32x2(mul, mul);
+#pragma unroll 1
+              for (int r2 = 0; r2 < 2; ++r2) {  // pairs [16 r2, 16 r2 + 16)
+                uint32_t vx[16], vy[16];
+                tmem_ld16(tmem + lane_addr + col + 16 * r2, vx);
+                tmem_ld16(tmem + lane_addr + col + D / 2 + 16 * r2, vy);
+                tmem_wait_ld();
+                reg_fence<16>(vx);
+                reg_fence<16>(vy);
+                if (valid) {
+                  uint32_t wx[8], wy[8];
 #pragma unroll
-                for (int e = 0; e < D / 4; ++e) {
-                  float xo[2], yo[2];
-#pragma unroll
-                  for (int k = 0; k < 2; ++k) {
-                    const int i = 2 * e + k;
-                    const float2 cs = __half22float2(*reinterpret_cast<const __half2*>(&tw[i]));
-                    const float x = __uint_as_float(v[i]) * mul, y = __uint_as_float(v[i + D / 2]) * mul;
-                    xo[k] = x * cs.x + y * cs.y;
-                    yo[k] = y * cs.x - x * cs.y;
+                  for (int e = 0; e < 8; ++e) {
+                    // cos and sin of pairs (16 r2 + 2e, +1), times the softmax scale
+                    const uint4& tq = tab[4 * r2 + e / 2];
+                    const uint64_t c = fmul2(h2_to_f32x2(e & 1 ? tq.z : tq.x), sc);
+                    const uint64_t sn = fmul2(h2_to_f32x2(e & 1 ? tq.w : tq.y), sc);
+                    uint64_t uo, vo;
+                    rot2<true>(f32x2(__uint_as_float(vx[2 * e]), __uint_as_float(vx[2 * e + 1])),
+                               f32x2(__uint_as_float(vy[2 * e]), __uint_as_float(vy[2 * e + 1])), c, sn, uo, vo);
+                    wx[e] = f32x2_to_bf16x2(uo);
+                    wy[e] = f32x2_to_bf16x2(vo);
                   }
-                  wx[e] = pack_bf16(xo[0], xo[1]);
-                  wy[e] = pack_bf16(yo[0], yo[1]);
-                }
 #pragma unroll
-                for (int e = 0; e < D / 16; ++e) {
-                  st_global_v4(dst + 8 * e, wx[4 * e], wx[4 * e + 1], wx[4 * e + 2], wx[4 * e + 3]);
-                  st_global_v4(dst + D / 2 + 8 * e, wy[4 * e], wy[4 * e + 1], wy[4 * e + 2], wy[4 * e + 3]);
+                  for (int e = 0; e < 2; ++e) {
+                    st_global_v4(dst + 16 * r2 + 8 * e, wx[4 * e], wx[4 * e + 1], wx[4 * e + 2], wx[4 * e + 3]);
+                    st_global_v4(dst + D / 2 + 16 * r2 + 8 * e, wy[4 * e], wy[4 * e + 1], wy[4 * e + 2],
+                                 wy[4 * e + 3]);
+                  }
                 }
               }
               continue;

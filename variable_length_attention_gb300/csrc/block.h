@@ -16,7 +16,7 @@ struct BlockArgs {
   int rows, batch, H, D, n_blocks, n_prog;
   int use_clc;                // 1: Cluster Launch Control over chunks of `chunk` tiles
   int chunk, n_tiles, n_chunks;
-  const uint32_t* rope_tab;   // rotary: (cos, sin) as half2 [positions, D/2] (see rope.h), or null
+  const uint32_t* rope_tab;   // rotary: packed table [positions, D/2] words (see rope.h), or null
   float scale;
   cudaStream_t stream;
 };

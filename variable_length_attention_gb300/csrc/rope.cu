@@ -15,9 +15,8 @@
 //
 // The block kernels (block.cu) rotate Q and K tiles in shared memory as they
 // land, and the backward's epilogue turns dQ and dK back by the transposed
-// rotation, from a packed table: pack_kernel turns the caller's fp32 cos/sin
-// rows into one half2 (cos, sin) per pair, half the bytes a tile's rotation has
-// to read.
+// rotation, from a packed table that pack_kernel builds from the caller's fp32
+// cos/sin rows: half the bytes, in the order the kernels' arithmetic takes them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -30,14 +29,20 @@
 namespace jfa {
 namespace rope {
 
-// (cos, sin) -> one half2 per pair: the block kernels' rotation reads 4 bytes
-// per pair instead of 8 (fp16 keeps 11 significant bits of values in [-1, 1],
-// finer than the bf16 rounding of the rotated rows that follows)
+// The packed table: for each two pairs (2m, 2m + 1) of a row, one half2 of
+// their cosines followed by one half2 of their sines, so that a kernel turns a
+// word straight into the operand pair of its paired fp32 arithmetic and reads
+// 4 bytes per pair instead of 8 (fp16 keeps 11 significant bits of values in
+// [-1, 1], finer than the bf16 rounding of the rotated rows that follows).
+// Word i of a row of half_d words: pairs 2 (i / 2) and 2 (i / 2) + 1, the sines
+// when i is odd.
 __global__ void pack_kernel(const float* __restrict__ cosv, const float* __restrict__ sinv, uint32_t* __restrict__ tab,
                             long n) {
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
-    const __half2 h = __floats2half2_rn(cosv[i], sinv[i]);
+    const float* src = (i & 1) ? sinv : cosv;
+    const long at = i & ~1L;  // row * half_d + 2 m: the first of the two pairs
+    const __half2 h = __floats2half2_rn(src[at], src[at + 1]);
     tab[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
 }
