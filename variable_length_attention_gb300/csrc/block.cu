@@ -10,9 +10,9 @@
 // owns its own dQ, dK and dV rows, so nothing is reduced across CTAs.
 //
 // Rotary variants (a template parameter): each tile's Q and K are rotated in
-// shared memory as soon as TMA has landed them (forward: two otherwise idle
-// warps take rows 0-31 of each block and the tile's softmax warpgroup the rest;
-// backward: the two warps all of it), from a packed fp16 cos/sin table the
+// shared memory as soon as TMA has landed them, by warps of their own (four
+// added to the forward's, two otherwise idle ones in the backward), from a
+// packed fp16 cos/sin table the
 // entry point builds per call (rope.cu), and the score GEMM waits for them.  The
 // backward's dQ and dK go back through the transposed rotation in its epilogue,
 // each thread on its own fp32 row as it comes out of TMEM, before rounding.
@@ -29,7 +29,8 @@
 // running and takes its chunk, so imbalance that shows only at run time is
 // absorbed ("TLX Block Attention", section 5; aixai.ru summary, "Tile balancing
 // and Cluster Launch Control").  The sequence of a global block is found by a
-// branchless binary search over the per-batch block prefix sums (section 5).
+// branchless binary search over the per-batch block prefix sums (section 5),
+// which each role runs only when its tiles leave the sequence it found last.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -270,14 +271,14 @@ __device__ __forceinline__ bool rope_rows(const uint32_t* __restrict__ tab, uint
   return true;
 }
 
-// The rotation role of the rotary variants (warps 2 and 3): every tile's Q and
-// K once their slot has landed, warp 2 rows [0, NROWS) of the tile's first block
-// and warp 3 those of its second; the score GEMM waits for qk_rot.  In the
-// backward NROWS is the whole block; in the forward the tile's softmax
-// warpgroup rotates the rest while it waits for its scores.
+// The rotation role of the rotary variants: every tile's Q and K once their
+// slot has landed, rows [r0, r0 + NROWS) of the tile's first (half 0) or second
+// (half 1) block; the score GEMM waits for qk_rot.  The forward runs four such
+// warps (32 rows each), the backward two (a whole block each).
 template <int D, int NQK, int NROWS, int B, class Bars>
-__device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* smem, int tile_bytes, const Abort& ab) {
-  const int half = warp_id() - 2, lane = lane_id();
+__device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* smem, int tile_bytes, int half, int r0,
+                                          const Abort& ab) {
+  const int lane = lane_id();
   TileCursor cur;
   Locator locate;
   for (int i = 0;; ++i) {
@@ -285,7 +286,7 @@ __device__ __forceinline__ void rope_role(const Params& p, Bars* bars, uint8_t* 
     if (t < 0) break;
     const int st = i % NQK;
     uint8_t* q_tile = smem + st * 2 * tile_bytes;
-    if (!rope_rows<D, NROWS, B>(p.rope_tab, q_tile, q_tile + tile_bytes, half, 0, locate(p, 2 * (t / p.H) + half),
+    if (!rope_rows<D, NROWS, B>(p.rope_tab, q_tile, q_tile + tile_bytes, half, r0, locate(p, 2 * (t / p.H) + half),
                                 lane, [&] { return mbar_wait(&bars->qk_full[st], (i / NQK) & 1, ab); }))
       break;
     fence_proxy_async_smem();
@@ -321,7 +322,7 @@ struct FwdBars {
   uint32_t tmem_base;
   int abort_flag;
 };
-// the MMA thread and the 8 softmax warps (and the rotary variant's 2 rotation warps)
+// the MMA thread and the 8 softmax warps (and the rotary variant's 4 rotation warps)
 constexpr int kFwdSchedConsumers = 9;
 
 // Loads rows [row0, row0+64) of every 64-column chunk of head h into rows
@@ -333,7 +334,7 @@ __device__ __forceinline__ void load_half(const CUtensorMap* tm, uint64_t* bar, 
 }
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(ROPE ? 512 : 384, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = FwdCfg<D>;
@@ -346,13 +347,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->sched_full[s], 1);
-      mbar_init(&bars->sched_empty[s], kFwdSchedConsumers + (ROPE ? 2 : 0));
+      mbar_init(&bars->sched_empty[s], kFwdSchedConsumers + (ROPE ? 4 : 0));
     }
     mbar_init(&bars->clc_bar, 1);
     for (int s = 0; s < C::NQK; ++s) {
       mbar_init(&bars->qk_full[s], 1);
       mbar_init(&bars->qk_empty[s], 1);
-      mbar_init(&bars->qk_rot[s], 6);  // the 2 rotation warps and the tile's softmax warpgroup
+      mbar_init(&bars->qk_rot[s], 4);  // the 4 rotation warps
     }
     for (int s = 0; s < C::NV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -488,9 +489,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t tw = global_timer_ns();
     while (!mbar_try_wait(&bars->drain, 0) && global_timer_ns() - tw < kWaitTimeoutNs) {
     }
-  } else if (ROPE && (warp == 2 || warp == 3)) {
-    // ---------------------------------------------------------------- rotation (rotary variant): rows 0-31 of each block
-    rope_role<D, C::NQK, 32, 2>(p, bars, smem, C::TILE, ab);
+  } else if (ROPE && warp >= 12) {
+    // ---------------------------------------------------------------- rotation (rotary variant)
+    // warps 12-15: rows 0-31 / 32-63 of the tile's first block, then its second
+    rope_role<D, C::NQK, 32, 2>(p, bars, smem, C::TILE, (warp - 12) >> 1, 32 * (warp & 1), ab);
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
     const int b = (warp - 4) >> 2;          // TMEM buffer / tile parity of this warpgroup
@@ -510,16 +512,6 @@ __global__ void __launch_bounds__(384, 1)
       const int pair = t / p.H, h = t % p.H;
       const Blk blk = locate(p, 2 * pair + half);
       const int rr = r & 63;
-      if constexpr (ROPE) {  // rows 32-63 of each block of its own tile, 16 per warp (the rotation warps take 0-31)
-        const int st = i % C::NQK;
-        uint8_t* q_tile = smem + st * 2 * C::TILE;
-        if (!rope_rows<D, 16, 2>(p.rope_tab, q_tile, q_tile + C::TILE, half, 32 + 16 * ((warp & 3) & 1), blk, lane,
-                                 [&] { return mbar_wait(&bars->qk_full[st], (i / C::NQK) & 1, ab); }))
-          goto done;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->qk_rot[st]);
-      }
       if (!mbar_wait(&bars->s_full[b], (i >> 1) & 1, ab)) goto done;
       tc_fence_after();
       uint32_t sr[64];
@@ -811,7 +803,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (ROPE && (warp == 2 || warp == 3)) {
     // ---------------------------------------------------------------- rotation (rotary variant)
-    rope_role<D, C::NQK, 64, D == 128 ? 4 : 2>(p, bars, smem, C::TILE, ab);
+    rope_role<D, C::NQK, 64, D == 128 ? 4 : 2>(p, bars, smem, C::TILE, warp - 2, 0, ab);
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- softmax, dS (and the epilogue at D = 128)
     const int r = threadIdx.x & 127;
@@ -1167,7 +1159,7 @@ int launch_fwd_impl(const BlockArgs& a) {
   p.n_chunks = a.n_chunks;
   p.rope_tab = a.rope_tab;
   ProfileScope prof(kKindBlockFwd, a.stream);
-  block_fwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
+  block_fwd_kernel<D, ROPE><<<a.use_clc ? a.n_chunks : a.n_prog, ROPE ? 512 : 384, C::SMEM, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
