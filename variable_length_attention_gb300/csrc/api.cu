@@ -482,6 +482,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   // the cleared error word, the units and the CTA starts travel in one copy
   // (they are adjacent at the head of the workspace)
   std::vector<uint8_t> blob(lay.empty - lay.err, 0);
+  units_for_device(&units, offsets_host);
   std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
   std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
   st = stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);
@@ -610,6 +611,7 @@ extern "C" int jfa_fwd_topk(const void* q, const void* k, const void* v, void* o
   // the cleared error word, units, CTA starts, empty sequences and the
   // query-block prefix in one copy
   std::vector<uint8_t> blob(lay.total - lay.err, 0);
+  units_for_device(&units, offsets_host);
   std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
   std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
   std::memcpy(blob.data() + (lay.empty - lay.err), empty.data(), empty.size() * 4);
@@ -740,6 +742,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
     // the cleared error word, the units and the CTA starts in one copy, ahead of
     // the kernels so that they follow one another directly
     std::vector<uint8_t> blob(lay.lse2 - lay.err, 0);
+    units_for_device(&units, offsets_host);
     std::memcpy(blob.data() + (lay.units - lay.err), units.data(), units.size() * 4);
     std::memcpy(blob.data() + (lay.cta - lay.err), cta_start.data(), cta_start.size() * 4);
     st = stage_to_device(ws + lay.err, blob.data(), blob.size(), stream);

@@ -127,7 +127,7 @@ __device__ __forceinline__ Unit decode(const Params& p, int idx) {
   u.m = e.z;
   u.g = u.h / (p.H / p.Hkv);
   u.kv0 = p.offsets[u.b];
-  u.L = p.offsets[u.b + 1] - u.kv0;
+  u.L = e.w;  // the sequence length (the host wrote it into the entry)
   if (p.nq > 0) {
     u.rows = p.nq;
     u.q_row0 = 2 * BM * u.m;

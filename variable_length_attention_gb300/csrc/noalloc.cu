@@ -117,6 +117,7 @@ extern "C" int jfa_fwd_noalloc(const void* q, const void* k, const void* v, void
   std::vector<int32_t> units, cta_start;
   plan_fwd(offsets_host, batch, num_heads, nq, causal, n_cta, &units, &cta_start);
   std::vector<uint8_t> blob(off_empty - off_units, 0);
+  units_for_device(&units, offsets_host);
   std::memcpy(blob.data(), units.data(), units.size() * 4);
   std::memcpy(blob.data() + (off_cta - off_units), cta_start.data(), cta_start.size() * 4);
   // pageable source: the call returns only once the bytes have been taken, so the

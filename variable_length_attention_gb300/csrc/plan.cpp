@@ -216,6 +216,13 @@ int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<i
   return static_cast<int>(P);
 }
 
+void units_for_device(std::vector<int32_t>* units, const int32_t* offsets) {
+  for (size_t e = 0; e + 3 < units->size(); e += 4) {
+    const int32_t b = (*units)[e];
+    (*units)[e + 3] = offsets[b + 1] - offsets[b];
+  }
+}
+
 }  // namespace jfa
 
 // ------------------------------------------------------------- exported test hooks

@@ -28,6 +28,10 @@ int plan_bwd_window(const int32_t* offsets, int batch, int H, int nq, int left, 
 // (min(topk, key blocks of its sequence)).
 int plan_fwd_topk(const int32_t* offsets, int batch, int H, int nq, int topk, int n_cta, std::vector<int32_t>* units,
                   std::vector<int32_t>* cta_start);
+// The device copy of a unit list: each entry's fourth field (the cost the
+// planner sorted by) replaced by the length of the entry's sequence, so that a
+// kernel decoding a unit has it without a second load that depends on the first.
+void units_for_device(std::vector<int32_t>* units, const int32_t* offsets);
 // Returns the number of programs P.
 int plan_block(const int32_t* offsets, int batch, int H, int n_sm, std::vector<int32_t>* bpb,
                std::vector<int32_t>* prog_start);
