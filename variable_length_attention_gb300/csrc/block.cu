@@ -302,9 +302,11 @@ template <int D>
 struct FwdCfg {
   static constexpr int TILE = 128 * D * 2;         // 128 rows x D, bf16
   static constexpr int CHUNK = 128 * 128;          // 64 columns x 128 rows
-  static constexpr int NQK = 2;                    // Q+K slots
-  static constexpr int NV = D == 128 ? 3 : 6;      // V slots (D=64: 160 KB in all measured
-                                                   // faster than filling the 227 KB)
+  // Q+K and V slots: at D = 128 two and three fill the 227 KB; at D = 64 four
+  // and four (192 KB) measured fastest of the splits tried (two and six, three
+  // and four, three and three, four and two)
+  static constexpr int NQK = D == 128 ? 2 : 4;
+  static constexpr int NV = D == 128 ? 3 : 4;
   static constexpr int OFF_V = NQK * 2 * TILE;
   static constexpr int OFF_BAR = OFF_V + NV * TILE;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;  // + alignment slack
@@ -313,8 +315,8 @@ struct FwdCfg {
 
 struct FwdBars {
   int4 clc_resp;  // Cluster Launch Control response (16-byte aligned)
-  uint64_t qk_full[2], qk_empty[2], v_full[6], v_empty[6];
-  uint64_t qk_rot[2];  // rotary variant: Q and K of the slot are rotated
+  uint64_t qk_full[4], qk_empty[4], v_full[4], v_empty[4];
+  uint64_t qk_rot[4];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full[2], p_full[2], o_full[2], t_free[2];
   uint64_t drain;
   uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
@@ -341,6 +343,7 @@ __global__ void __launch_bounds__(ROPE ? 512 : 384, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::OFF_BAR);
+  static_assert(C::NQK <= 4 && C::NV <= 4, "barrier arrays of the slot rings");
   static_assert(sizeof(FwdBars) <= 512, "barrier block");
   const int warp = warp_id(), lane = lane_id();
 
@@ -636,6 +639,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::OFF_BAR);
+  static_assert(C::NQK <= 3 && C::NVD <= 2, "barrier arrays of the slot rings");
   static_assert(sizeof(BwdBars) <= 512, "barrier block");
   const int warp = warp_id(), lane = lane_id();
   constexpr uint32_t COL_S = C::COL_S, COL_DP = C::COL_DP, COL_DV = C::COL_DV, COL_DK = C::COL_DK, COL_DQ = C::COL_DQ;
