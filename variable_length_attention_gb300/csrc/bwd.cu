@@ -760,8 +760,8 @@ __global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bflo
       if (pr < n_pairs) {
         const long h = pr / rows, r = pr - h * rows;
         const size_t at = (static_cast<size_t>(r) * H + h) * D + part * 8;
-        a[u] = *reinterpret_cast<const uint4*>(o + at);
-        b[u] = *reinterpret_cast<const uint4*>(dout + at);
+        a[u] = ld_stream_v4(o + at);
+        b[u] = ld_stream_v4(dout + at);
       } else {
         a[u] = make_uint4(0, 0, 0, 0);
         b[u] = make_uint4(0, 0, 0, 0);
@@ -796,7 +796,9 @@ __global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bflo
 
 __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4, float scale) {
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += static_cast<long>(gridDim.x) * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    const uint4 raw = ld_stream_v4(reinterpret_cast<const float4*>(acc) + i);
+    const float4 v = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
+                                 __uint_as_float(raw.w));
     uint2 w;
     w.x = pack_bf16(v.x * scale, v.y * scale);
     w.y = pack_bf16(v.z * scale, v.w * scale);

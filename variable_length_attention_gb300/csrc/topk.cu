@@ -49,7 +49,8 @@ __global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __n
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   // 32 rows' loads issued per round (a block is up to 256 rows, so one row at a
-  // time would leave the warp waiting on memory latency)
+  // time would leave the warp waiting on memory latency); every row is read once,
+  // so the loads bypass L1 allocation (67 -> 55 us per selection call measured)
   constexpr int U = 32;
   const size_t stride = static_cast<size_t>(heads) * D;
   const __nv_bfloat16* row0 = base + (static_cast<size_t>(t.x) * heads + t.z) * D + lane * PER;
@@ -61,9 +62,9 @@ __global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __n
       if (r0 + u < t.y) {
         const __nv_bfloat16* row = row0 + static_cast<size_t>(r0 + u) * stride;
         if constexpr (PER == 4)
-          raw[u] = *reinterpret_cast<const uint2*>(row);
+          asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(raw[u].x), "=r"(raw[u].y) : "l"(row));
         else
-          raw[u].x = *reinterpret_cast<const uint32_t*>(row);
+          asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(raw[u].x) : "l"(row));
       }
     }
 #pragma unroll
