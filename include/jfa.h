@@ -228,8 +228,9 @@ int block_attn_bwd(const void* q, const void* k, const void* v, const void* o, c
  * the backward recomputes them and returns dq and dk with respect to the
  * unrotated q and k (the transposed rotation is applied before they are
  * returned).  q and k stay unrotated in memory: the kernels rotate their tiles
- * in shared memory, from the tables packed into the workspace as (cos, sin)
- * fp16 pairs, whose size is jfa_workspace_size(JFA_OP_BLOCK_FWD_ROPE or
+ * in shared memory, from the tables packed into the workspace as fp16 words
+ * (for each two column pairs, one word of their cosines and one of their
+ * sines), whose size is jfa_workspace_size(JFA_OP_BLOCK_FWD_ROPE or
  * JFA_OP_BLOCK_BWD_ROPE, ...) (the plain size plus longest sequence x
  * head_dim/2 x 4 bytes); the backward kernel's epilogue carries dq and dk
  * back through the transposed rotation before it stores them.  Errors as
