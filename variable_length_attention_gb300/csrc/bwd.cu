@@ -788,10 +788,9 @@ __global__ void prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bflo
       }
     }
   }
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < acc4;
        i += static_cast<long>(gridDim.x) * blockDim.x)
-    acc[i] = z;
+    st_global_v4(acc + i, 0u, 0u, 0u, 0u);
 }
 
 __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4, float scale) {
@@ -799,10 +798,7 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
     const uint4 raw = ld_stream_v4(reinterpret_cast<const float4*>(acc) + i);
     const float4 v = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
                                  __uint_as_float(raw.w));
-    uint2 w;
-    w.x = pack_bf16(v.x * scale, v.y * scale);
-    w.y = pack_bf16(v.z * scale, v.w * scale);
-    reinterpret_cast<uint2*>(dq)[i] = w;
+    st_global_v2(reinterpret_cast<uint2*>(dq) + i, pack_bf16(v.x * scale, v.y * scale), pack_bf16(v.z * scale, v.w * scale));
   }
 }
 
