@@ -657,9 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_expect_tx(&bars->kv_full, 2 * C::TILE);
 #pragma unroll
+          // K and V are read by this unit only: first out of L2; the query tiles
+          // and dO are read again by the sequence's other key blocks: last out
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_2d(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n);
-            tma_load_2d(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n);
+            tma_load_2d_hint(&tm_k, &bars->kv_full, smem + C::OFF_K + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n,
+                             l2_policy_evict_first());
+            tma_load_2d_hint(&tm_v, &bars->kv_full, smem + C::OFF_V + c * C::CHUNK, u.h * D + c * 64, u.kv0 + BK * u.n,
+                             l2_policy_evict_first());
           }
         }
         for (int hg = 0; hg < p.G && ok; ++hg)
@@ -684,7 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&bars->q_full[st], C::TILE);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_load_2d(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, hq * D + c * 64, u.q_base + BQ * i);
+              tma_load_2d_hint(&tm_q, &bars->q_full[st], sQ + c * C::CHUNK, hq * D + c * 64, u.q_base + BQ * i,
+                               l2_policy_evict_last());
           } else {
             mbar_arrive(&bars->q_full[st]);
           }
@@ -697,8 +702,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&bars->do_full, C::TILE);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_load_2d(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, hq * D + c * 64,
-                          u.o_base + BQ * i);
+              tma_load_2d_hint(&tm_do, &bars->do_full, smem + C::OFF_DO + c * C::CHUNK, hq * D + c * 64,
+                               u.o_base + BQ * i, l2_policy_evict_last());
           }
         }
         if (!ok) break;
