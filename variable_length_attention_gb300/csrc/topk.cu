@@ -11,9 +11,9 @@
 // head h / (H / Hkv); the k highest scores win, ties to the lower block index.
 //
 // Kernels, in launch order:
-//   block_mean_kernel  one warp per block: the fp32 mean of its rows (query
-//                      blocks of every head, then key blocks of every key/value
-//                      head), rows read once, 16 bytes per lane
+//   block_mean_kernel  one CTA per block: the fp32 mean of its rows (query
+//                      blocks, then key blocks), each of its 8 warps loading 32
+//                      rows at once, partial sums added in shared memory
 //   select_kernel      one warp per query block: the scores against every key
 //                      block of its sequence, then k rounds of a warp arg-max;
 //                      the chosen block indices are written in ascending order,
@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "host.h"
+#include "plan.h"
 #include "profile.h"
 #include "ptx.cuh"
 #include "topk.h"
@@ -35,53 +36,63 @@ struct MeanTask {
   int row0, n, head, tensor;  // tensor 0: q, 1: k
 };
 
+// One CTA per block: warp w sums rows [32 w, 32 w + 32) of it with all 32 rows'
+// loads in flight at once (a block has at most 256 rows, so one round), and the
+// eight partial sums are added in shared memory.  Every row is read once, so
+// the loads allocate no L1 line.  (Selection call: a warp per block walking its
+// rows 32 at a time took 67 us, 55 us without L1 allocation; this, 49 us.)
+constexpr int kMeanWarps = 8;
 template <int D>
-__global__ void block_mean_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int H,
-                                  int Hkv, const int4* __restrict__ tasks, int n_tasks, float* __restrict__ out) {
+__global__ void __launch_bounds__(32 * kMeanWarps) block_mean_kernel(const __nv_bfloat16* __restrict__ q,
+                                                                      const __nv_bfloat16* __restrict__ k, int H,
+                                                                      int Hkv, const int4* __restrict__ tasks,
+                                                                      float* __restrict__ out) {
   constexpr int PER = D / 32;  // columns per lane: 4 (D = 128) or 2 (D = 64)
-  const int lane = threadIdx.x & 31;
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (w >= n_tasks) return;
-  const int4 t = tasks[w];
+  constexpr int U = 32;        // rows per warp
+  __shared__ float part[kMeanWarps][D];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int4 t = tasks[blockIdx.x];
   const __nv_bfloat16* base = t.w == 0 ? q : k;
   const int heads = t.w == 0 ? H : Hkv;
+  const size_t stride = static_cast<size_t>(heads) * D;
+  const int r0 = U * warp;
+  const __nv_bfloat16* row0 = base + (static_cast<size_t>(t.x + r0) * heads + t.z) * D + lane * PER;
+  uint2 raw[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    raw[u] = make_uint2(0u, 0u);  // bf16 zeros past the block's end
+    if (r0 + u < t.y) {
+      const __nv_bfloat16* row = row0 + static_cast<size_t>(u) * stride;
+      if constexpr (PER == 4)
+        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(raw[u].x), "=r"(raw[u].y) : "l"(row));
+      else
+        asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(raw[u].x) : "l"(row));
+    }
+  }
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  // 32 rows' loads issued per round (a block is up to 256 rows, so one row at a
-  // time would leave the warp waiting on memory latency); every row is read once,
-  // so the loads bypass L1 allocation (67 -> 55 us per selection call measured)
-  constexpr int U = 32;
-  const size_t stride = static_cast<size_t>(heads) * D;
-  const __nv_bfloat16* row0 = base + (static_cast<size_t>(t.x) * heads + t.z) * D + lane * PER;
-  for (int r0 = 0; r0 < t.y; r0 += U) {
-    uint2 raw[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      raw[u] = make_uint2(0u, 0u);  // bf16 zeros past the block's end
-      if (r0 + u < t.y) {
-        const __nv_bfloat16* row = row0 + static_cast<size_t>(r0 + u) * stride;
-        if constexpr (PER == 4)
-          asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(raw[u].x), "=r"(raw[u].y) : "l"(row));
-        else
-          asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(raw[u].x) : "l"(row));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
-      acc[0] += a.x;
-      acc[1] += a.y;
-      if constexpr (PER == 4) {
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
-        acc[2] += b.x;
-        acc[3] += b.y;
-      }
+  for (int u = 0; u < U; ++u) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
+    acc[0] += a.x;
+    acc[1] += a.y;
+    if constexpr (PER == 4) {
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
+      acc[2] += c.x;
+      acc[3] += c.y;
     }
   }
-  const float inv = t.y > 0 ? 1.0f / static_cast<float>(t.y) : 0.f;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) out[static_cast<size_t>(w) * D + lane * PER + e] = acc[e] * inv;
+  for (int e = 0; e < PER; ++e) part[warp][lane * PER + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMeanWarps; ++w) sum += part[w][threadIdx.x];
+    const float inv = t.y > 0 ? 1.0f / static_cast<float>(t.y) : 0.f;
+    out[static_cast<size_t>(blockIdx.x) * D + threadIdx.x] = sum * inv;
+  }
 }
 
 // One query block: its mean (row `qmean` of the means), the first key-block
@@ -93,7 +104,8 @@ __global__ void select_kernel(const float* __restrict__ means, const int4* __res
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (u >= n_units) return;
-  const int4 t = sel_tasks[u];  // x: row of the query mean, y: row of the first key mean, z: key blocks
+  const int4 t = sel_tasks[u];  // x: row of the query mean, y: row of key block 0's mean, z: key blocks,
+                                // w: rows between consecutive key blocks' means
   float* sc = s_scores + wib * nk_max;
   constexpr int PER = D / 32;
   float qm[PER];
@@ -162,18 +174,17 @@ __global__ void select_kernel(const float* __restrict__ means, const int4* __res
 
 int launch_topk_select(const TopkArgs& a) {
   if (a.n_tasks == 0) return JFA_OK;
-  const int threads = 256;
   {
-    const int blocks = static_cast<int>((static_cast<long>(a.n_tasks) * 32 + threads - 1) / threads);
+    static_assert(kFwdRows <= 32 * topk::kMeanWarps && kKvBlock <= 32 * topk::kMeanWarps, "one round of rows per warp");
     ProfileScope prof(kKindTopk, a.stream);
     if (a.D == 128)
-      topk::block_mean_kernel<128><<<blocks, threads, 0, a.stream>>>(
+      topk::block_mean_kernel<128><<<a.n_tasks, 32 * topk::kMeanWarps, 0, a.stream>>>(
           static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.H, a.Hkv, a.mean_tasks,
-          a.n_tasks, a.means);
+          a.means);
     else
-      topk::block_mean_kernel<64><<<blocks, threads, 0, a.stream>>>(
+      topk::block_mean_kernel<64><<<a.n_tasks, 32 * topk::kMeanWarps, 0, a.stream>>>(
           static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.H, a.Hkv, a.mean_tasks,
-          a.n_tasks, a.means);
+          a.means);
     if (cudaGetLastError() != cudaSuccess) return JFA_ERR_CUDA;
   }
   if (a.n_units == 0) return JFA_OK;
