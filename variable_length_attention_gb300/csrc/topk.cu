@@ -14,8 +14,9 @@
 //   block_mean_kernel  one CTA per block: the fp32 mean of its rows (query
 //                      blocks, then key blocks), each of its 8 warps loading 32
 //                      rows at once, partial sums added in shared memory
-//   select_kernel      one warp per query block: the scores against every key
-//                      block of its sequence, then k rounds of a warp arg-max;
+//   select_kernel      one CTA per query block: the scores against every key
+//                      block of its sequence (the warps share them), then k
+//                      rounds of a warp arg-max;
 //                      the chosen block indices are written in ascending order,
 //                      -1 after the last one
 #include <cuda_bf16.h>
@@ -95,42 +96,45 @@ __global__ void __launch_bounds__(32 * kMeanWarps) block_mean_kernel(const __nv_
   }
 }
 
-// One query block: its mean (row `qmean` of the means), the first key-block
-// mean of its sequence and key/value head, and how many key blocks there are.
+// One query block per CTA of kSelWarps warps: its mean (row x of the means),
+// the mean of its sequence's key block 0 for its key/value head (row y) and the
+// number of key blocks (z).  The warps share the dot products (block n goes to
+// warp n % kSelWarps, eight blocks' means loaded at a time), then warp 0 picks.
+constexpr int kSelWarps = 4;
 template <int D>
-__global__ void select_kernel(const float* __restrict__ means, const int4* __restrict__ sel_tasks, int n_units,
-                              int topk, int nk_max, int32_t* __restrict__ selection) {
-  extern __shared__ float s_scores[];  // [warps][nk_max]
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (u >= n_units) return;
-  const int4 t = sel_tasks[u];  // x: row of the query mean, y: row of key block 0's mean, z: key blocks,
-                                // w: rows between consecutive key blocks' means
-  float* sc = s_scores + wib * nk_max;
+__global__ void __launch_bounds__(32 * kSelWarps) select_kernel(const float* __restrict__ means,
+                                                                 const int4* __restrict__ sel_tasks, int topk,
+                                                                 int32_t* __restrict__ selection) {
+  extern __shared__ float sc[];  // [key blocks of the widest sequence]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int u = blockIdx.x;
+  const int4 t = sel_tasks[u];
   constexpr int PER = D / 32;
   float qm[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) qm[e] = means[static_cast<size_t>(t.x) * D + lane * PER + e];
-  // eight key blocks' means loaded at a time, then their dot products
   constexpr int U = 8;
-  for (int n0 = 0; n0 < t.z; n0 += U) {
+  for (int n0 = warp; n0 < t.z; n0 += U * kSelWarps) {
     float km[U][PER];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int v = 0; v < U; ++v) {
+      const int n = n0 + v * kSelWarps;
 #pragma unroll
-      for (int e = 0; e < PER; ++e)
-        km[u][e] = n0 + u < t.z ? means[static_cast<size_t>(t.y + n0 + u) * D + lane * PER + e] : 0.f;
+      for (int e = 0; e < PER; ++e) km[v][e] = n < t.z ? means[static_cast<size_t>(t.y + n) * D + lane * PER + e] : 0.f;
+    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int v = 0; v < U; ++v) {
+      const int n = n0 + v * kSelWarps;
       float d = 0.f;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) d = fmaf(qm[e], km[u][e], d);
+      for (int e = 0; e < PER; ++e) d = fmaf(qm[e], km[v][e], d);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-      if (lane == 0 && n0 + u < t.z) sc[n0 + u] = d;
+      if (lane == 0 && n < t.z) sc[n] = d;
     }
   }
-  __syncwarp();
+  __syncthreads();
+  if (warp != 0) return;
   // k rounds of arg-max (ties to the lower index); chosen blocks are marked
   // with -inf, and a score is never -inf otherwise (finite inputs)
   const int cnt = min(topk, t.z);
@@ -188,16 +192,21 @@ int launch_topk_select(const TopkArgs& a) {
     if (cudaGetLastError() != cudaSuccess) return JFA_ERR_CUDA;
   }
   if (a.n_units == 0) return JFA_OK;
-  const int sel_threads = 128;  // 4 warps, nk_max scores each
-  const size_t smem = static_cast<size_t>(sel_threads / 32) * a.nk_max * sizeof(float);
-  const int blocks = static_cast<int>((static_cast<long>(a.n_units) * 32 + sel_threads - 1) / sel_threads);
+  const size_t smem = static_cast<size_t>(a.nk_max) * sizeof(float);  // one score per key block
+  if (smem > 48 * 1024) {  // a sequence of more than 12,288 key blocks: opt in to more shared memory
+    const cudaError_t e = a.D == 128 ? cudaFuncSetAttribute(topk::select_kernel<128>,
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                                     : cudaFuncSetAttribute(topk::select_kernel<64>,
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return JFA_ERR_UNSUPPORTED;  // beyond the device's shared memory per block
+  }
   ProfileScope prof(kKindTopk, a.stream);
   if (a.D == 128)
-    topk::select_kernel<128><<<blocks, sel_threads, smem, a.stream>>>(a.means, a.sel_tasks, a.n_units, a.topk,
-                                                                     a.nk_max, a.selection);
+    topk::select_kernel<128><<<a.n_units, 32 * topk::kSelWarps, smem, a.stream>>>(a.means, a.sel_tasks, a.topk,
+                                                                                 a.selection);
   else
-    topk::select_kernel<64><<<blocks, sel_threads, smem, a.stream>>>(a.means, a.sel_tasks, a.n_units, a.topk,
-                                                                    a.nk_max, a.selection);
+    topk::select_kernel<64><<<a.n_units, 32 * topk::kSelWarps, smem, a.stream>>>(a.means, a.sel_tasks, a.topk,
+                                                                                a.selection);
   return cudaGetLastError() == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
