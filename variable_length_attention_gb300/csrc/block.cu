@@ -614,6 +614,7 @@ struct BwdBars {
   uint64_t qk_rot[3];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
   uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
+  uint64_t box_full[2], box_free[2];  // the same per 64-column box (D = 128, no rotary: pipelined)
   uint64_t drain;
   uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
   int sched_unit[4];
@@ -664,6 +665,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars->p_used, 1);
     mbar_init(&bars->stg_full, 128);
     mbar_init(&bars->stg_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->box_full[b], 128);
+      mbar_init(&bars->box_free[b], 1);
+    }
     mbar_init(&bars->p_full, 4);
     mbar_init(&bars->ds_full, 4);
     mbar_init(&bars->acc_full, 1);
@@ -818,6 +823,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float sl2 = p.scale_log2;
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
     uint32_t stg_full_ph = 0, stg_free_ph = 0;
+    uint32_t box_full_ph[2] = {0, 0}, box_free_ph[2] = {0, 0};
     TileCursor cur;
     Locator locate;
     for (int i = 0;; ++i) {
@@ -916,6 +922,63 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const bool valid = rr < blk.len;
           const bool full_half = blk.len == kBlk;
           const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
+          if constexpr (!ROPE) {
+            // dQ, dK, dV one 64-column box at a time through the two halves of
+            // the staging buffer: the rows of one box are written while TMA still
+            // reads the other
+  #pragma unroll 1
+            for (int s = 0; s < 6; ++s) {
+              const int which = s >> 1, box = s & 1;
+              const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
+              const float mul = which == 2 ? 1.0f : p.scale;
+              const CUtensorMap* tm_out = which == 0 ? &tm_dq : (which == 1 ? &tm_dk : &tm_dv);
+              __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+              if (s >= 2) {  // the box's previous rows (two stages back) have been read out
+                if (threadIdx.x == 128) {
+                  bulk_wait_read_all_but_newest();
+                  mbar_arrive(&bars->box_free[box]);
+                }
+                if (!mbar_wait(&bars->box_free[box], box_free_ph[box], ab)) goto done;
+                box_free_ph[box] ^= 1;
+              }
+  #pragma unroll 1
+              for (int c = 64 * box; c < 64 * box + 64; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + col + c, v);
+                tmem_wait_ld();
+                reg_fence<32>(v);
+                uint32_t w[16];
+  #pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) st_row_piece(sP, r, box, (c % 64) / 8 + e, w + 4 * e);
+                if (valid && !full_half) {
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+              }
+              if (s == 5) {  // every accumulator has been read: TMEM is free
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->t_free);
+              }
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->box_full[box]);
+              if (!mbar_wait(&bars->box_full[box], box_full_ph[box], ab)) goto done;
+              box_full_ph[box] ^= 1;
+              if (threadIdx.x == 128) {
+  #pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                  const Blk bk = hf == 0 ? blk_a : blk_b;
+                  if (bk.len == kBlk)
+                    tma_store_2d(tm_out, smem + C::OFF_PDS + box * 16384 + hf * 8192, h * D + 64 * box, bk.row0);
+                }
+                bulk_commit_group();
+              }
+            }
+          } else
   #pragma unroll 1
           for (int which = 0; which < 3; ++which) {
             const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
