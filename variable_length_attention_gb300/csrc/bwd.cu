@@ -191,7 +191,8 @@ struct Bars {
 
 constexpr int kSchedConsumers = 13;  // 8 P/dS warps + 4 drain warps + the MMA thread
 
-template <int D, int MASK>
+// FINE: the broadcast-Q instantiation, whose dK/dV epilogue is pipelined per box
+template <int D, int MASK, bool FINE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -406,9 +407,132 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool key_ok = BK * u.n + r < u.L;
           const size_t row = (static_cast<size_t>(u.kv0 + BK * u.n + r) * p.Hkv + u.h) * D;
           const uint32_t stage32 = smem_u32(smem + C::OFF_STG);
+          // broadcast-Q (two query tiles per unit): the drain is mostly this
+          // epilogue, so dV, then dK go one 64-column box per stage through the
+          // two 16 KB slots in turn, the rows of one stage written while TMA still
+          // reads the previous one (backward call 487 -> 455 us); self-attention
+          // units keep one hand-off per tensor, as the finer one measured slower
+          // there (jagged 648 -> 653 us; with both paths in one kernel, 661 us)
+          const bool fine = FINE && full_blk;
+          if (fine) {
+            constexpr int NBOX = D / 64;
 #pragma unroll 1
-          for (int which = 0; which < 2; ++which) {
-            if (full_blk) {  // the buffer holds nothing TMA still reads
+            for (int s = 0; s < 2 * NBOX; ++s) {
+              const int which = s / NBOX, box = s % NBOX, slot = s & 1;
+              if (s == 0 || s >= 2) {  // the slot's last reader (the dQ reduction, or stage s-2) is done
+                if (threadIdx.x == 256) {
+                  if (s == 0)
+                    bulk_wait_read_all();
+                  else
+                    bulk_wait_read_all_but_newest();
+                  mbar_arrive(&bars->kvst_free);
+                }
+                if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
+                kvst_free_ph ^= 1;
+              }
+              const uint32_t tAcc = tmem + lane_addr + (which == 0 ? C::COL_DV : C::COL_DK);
+              const float mul = which == 0 ? 1.0f : p.scale;
+#pragma unroll 1
+              for (int c = 64 * box; c < 64 * box + 64; c += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tAcc + c, ov);
+                tmem_wait_ld();
+                reg_fence<32>(ov);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
+                // row r of the slot's 64-column box, 16-byte pieces (c%64)/8 .. +3, 128-byte swizzle
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t addr = stage32 + slot * 16384 + r * 128 + ((((c % 64) / 8 + e) ^ (r & 7)) << 4);
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * e]),
+                               "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
+                               : "memory");
+                }
+              }
+              if (s == 2 * NBOX - 1) {  // dV and dK are out of TMEM: the next unit's MMAs may start
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->dkv_empty);
+              }
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->kvst_full);
+              if (!mbar_wait(&bars->kvst_full, kvst_full_ph, ab)) goto done;
+              kvst_full_ph ^= 1;
+              if (threadIdx.x == 256) {
+                tma_store_2d(which == 0 ? &tm_dv : &tm_dk, smem + C::OFF_STG + slot * 16384, u.h * D + 64 * box,
+                             u.kv0 + BK * u.n);
+                bulk_commit_group();
+              }
+            }
+            // hand the buffer back to the dQ reduction
+            if (threadIdx.x == 256) {
+              bulk_wait_read_all();
+              mbar_arrive(&bars->kvst_free);
+            }
+            if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
+            kvst_free_ph ^= 1;
+          } else {
+  #pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+              if (full_blk) {  // the buffer holds nothing TMA still reads
+                if (threadIdx.x == 256) {
+                  bulk_wait_read_all();
+                  mbar_arrive(&bars->kvst_free);
+                }
+                if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
+                kvst_free_ph ^= 1;
+              }
+              const uint32_t tAcc = tmem + lane_addr + (which == 0 ? C::COL_DV : C::COL_DK);
+              const float mul = which == 0 ? 1.0f : p.scale;
+              __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row;
+  #pragma unroll 1
+              for (int c = 0; c < D; c += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tAcc + c, ov);
+                tmem_wait_ld();
+                reg_fence<32>(ov);
+                uint32_t pk[16];
+  #pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
+                if (full_blk) {
+                  // row r of 64-column box c/64, 16-byte pieces (c%64)/8 .. +3, 128-byte swizzle
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint32_t addr =
+                        stage32 + (c / 64) * 16384 + r * 128 + ((((c % 64) / 8 + e) ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * e]),
+                                 "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
+                                 : "memory");
+                  }
+                } else if (key_ok) {
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+              }
+              if (which == 1) {  // dV and dK are out of TMEM: the next unit's MMAs may start
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->dkv_empty);
+              }
+              if (full_blk) {
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->kvst_full);
+                if (!mbar_wait(&bars->kvst_full, kvst_full_ph, ab)) goto done;
+                kvst_full_ph ^= 1;
+                if (threadIdx.x == 256) {
+  #pragma unroll
+                  for (int b2 = 0; b2 < D / 64; ++b2)
+                    tma_store_2d(which == 0 ? &tm_dv : &tm_dk, smem + C::OFF_STG + b2 * 16384, u.h * D + 64 * b2,
+                                 u.kv0 + BK * u.n);
+                  bulk_commit_group();
+                }
+              }
+            }
+            if (full_blk) {  // hand the buffer back to the dQ reduction
               if (threadIdx.x == 256) {
                 bulk_wait_read_all();
                 mbar_arrive(&bars->kvst_free);
@@ -416,61 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
               kvst_free_ph ^= 1;
             }
-            const uint32_t tAcc = tmem + lane_addr + (which == 0 ? C::COL_DV : C::COL_DK);
-            const float mul = which == 0 ? 1.0f : p.scale;
-            __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row;
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t ov[32];
-              tmem_ld32(tAcc + c, ov);
-              tmem_wait_ld();
-              reg_fence<32>(ov);
-              uint32_t pk[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * mul, __uint_as_float(ov[2 * e + 1]) * mul);
-              if (full_blk) {
-                // row r of 64-column box c/64, 16-byte pieces (c%64)/8 .. +3, 128-byte swizzle
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const uint32_t addr =
-                      stage32 + (c / 64) * 16384 + r * 128 + ((((c % 64) / 8 + e) ^ (r & 7)) << 4);
-                  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * e]),
-                               "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
-                               : "memory");
-                }
-              } else if (key_ok) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  st_global_v4(dst + c + 8 * e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-              }
-            }
-            if (which == 1) {  // dV and dK are out of TMEM: the next unit's MMAs may start
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->dkv_empty);
-            }
-            if (full_blk) {
-              fence_proxy_async_smem();
-              mbar_arrive(&bars->kvst_full);
-              if (!mbar_wait(&bars->kvst_full, kvst_full_ph, ab)) goto done;
-              kvst_full_ph ^= 1;
-              if (threadIdx.x == 256) {
-#pragma unroll
-                for (int b2 = 0; b2 < D / 64; ++b2)
-                  tma_store_2d(which == 0 ? &tm_dv : &tm_dk, smem + C::OFF_STG + b2 * 16384, u.h * D + 64 * b2,
-                               u.kv0 + BK * u.n);
-                bulk_commit_group();
-              }
-            }
-          }
-          if (full_blk) {  // hand the buffer back to the dQ reduction
-            if (threadIdx.x == 256) {
-              bulk_wait_read_all();
-              mbar_arrive(&bars->kvst_free);
-            }
-            if (!mbar_wait(&bars->kvst_free, kvst_free_ph, ab)) goto done;
-            kvst_free_ph ^= 1;
           }
         }
         if (!mbar_wait(&bars->dq_full, ph, ab)) goto done;
@@ -807,7 +876,7 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* 
   }
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool FINE = false>
 int launch_main(const BwdArgs& a) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv, tdo;
@@ -821,7 +890,7 @@ int launch_main(const BwdArgs& a) {
   if (st == JFA_OK) st = make_map_2d(&tdk, a.dk, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st == JFA_OK) st = make_map_2d(&tdv, a.dv, static_cast<uint64_t>(a.Hkv) * D, a.kv_rows, 64, BK);
   if (st != JFA_OK) return st;
-  auto kern = bwd_kernel<D, MASK>;
+  auto kern = bwd_kernel<D, MASK, FINE>;
   static PerDeviceOnce setup;  // per instantiation
   st = setup.run([&]() -> int {
     cudaFuncAttributes fa;
@@ -886,10 +955,12 @@ int launch_bwd_prep(const BwdArgs& a, int num_sms) {
 int launch_bwd_main(const BwdArgs& a) {
   if (a.D == 128) {
     if (a.mask == kMaskWindow) return bwd::launch_main<128, kMaskWindow>(a);
-    return a.mask == kMaskCausal ? bwd::launch_main<128, kMaskCausal>(a) : bwd::launch_main<128, kMaskNone>(a);
+    if (a.mask == kMaskCausal) return bwd::launch_main<128, kMaskCausal>(a);
+    return a.nq > 0 ? bwd::launch_main<128, kMaskNone, true>(a) : bwd::launch_main<128, kMaskNone>(a);
   }
   if (a.mask == kMaskWindow) return bwd::launch_main<64, kMaskWindow>(a);
-  return a.mask == kMaskCausal ? bwd::launch_main<64, kMaskCausal>(a) : bwd::launch_main<64, kMaskNone>(a);
+  if (a.mask == kMaskCausal) return bwd::launch_main<64, kMaskCausal>(a);
+  return a.nq > 0 ? bwd::launch_main<64, kMaskNone, true>(a) : bwd::launch_main<64, kMaskNone>(a);
 }
 
 int launch_dq_convert(const BwdArgs& a, int num_sms) {
