@@ -175,7 +175,7 @@ int jfa_bwd_window(const void* q, const void* k, const void* v, const void* o, c
  *   block indices (0-based, within the sequence) in ascending order, then -1
  *   where the sequence has fewer than topk blocks.  Workspace:
  *   jfa_workspace_size(JFA_OP_TOPK_SELECT, ...).  Sequences of more than
- *   393,216 keys return JFA_ERR_UNSUPPORTED.
+ *   1,572,864 keys return JFA_ERR_UNSUPPORTED.
  * jfa_fwd_topk: second stage, o and lse as jfa_fwd, with the selection of
  *   jfa_topk_select (or any selection of ascending, in-range block indices,
  *   min(topk, blocks) of them per row).  Workspace:

@@ -100,3 +100,28 @@ def test_topk_covering_every_block_is_full_attention():
     torch.cuda.synchronize()
     assert (o1.float() - o2.float()).abs().max().item() < 1e-2
     assert (l1 - l2).abs().max().item() < 1e-3
+
+
+def test_topk_longest_sequence_limit():
+    """The selection keeps one score per key block of the longest sequence in
+    shared memory (48 KB): a sequence of 12,288 key blocks (1,572,864 keys) runs,
+    one key more is refused before any work.  The inputs make the answer exact:
+    every query row is the same vector u, every key row zero except in four key
+    blocks, whose rows are c u with distinct c > 0, so every query block picks
+    those four blocks (bf16-exact values, no near-ties)."""
+    n_blk, D, topk = 12288, 64, 4
+    T = n_blk * 128
+    u = torch.full((D,), 0.125, dtype=torch.bfloat16, device="cuda")
+    q = u.expand(T + 1, 1, D).contiguous()
+    k = torch.zeros((T + 1, 1, D), dtype=torch.bfloat16, device="cuda")
+    chosen = [5, 100, 7777, n_blk - 1]
+    for blk, c in zip(chosen, [1.0, 0.875, 0.75, 0.625]):
+        k[128 * blk:128 * (blk + 1), 0] = (u.float() * c).to(torch.bfloat16)
+    offs_h = np.array([0, T], dtype=np.int32)
+    sel = V.jfa_topk_select(q[:T], k[:T], torch.from_numpy(offs_h).cuda(), offs_h, topk=topk)
+    torch.cuda.synchronize()
+    assert sel.shape == (T // 256, topk)
+    assert torch.equal(sel.cpu(), torch.tensor(chosen, dtype=torch.int32).expand(T // 256, topk))
+    offs_h1 = np.array([0, T + 1], dtype=np.int32)
+    with pytest.raises(V.jfa.JfaError, match="UNSUPPORTED"):
+        V.jfa_topk_select(q, k, torch.from_numpy(offs_h1).cuda(), offs_h1, topk=topk)

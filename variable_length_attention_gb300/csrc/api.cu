@@ -548,7 +548,9 @@ extern "C" int jfa_topk_select(const void* q, const void* k, const int32_t* offs
   int nk_max = 0;
   const int n_units = topk_tasks(offsets_host, batch, nq, num_heads, num_kv_heads, &mt, &stasks, &nk_max);
   if (n_units > 0 && selection == nullptr) return JFA_ERR_INVALID_ARG;
-  if (static_cast<size_t>(nk_max) * 4 * sizeof(float) > 48 * 1024) return JFA_ERR_UNSUPPORTED;  // > 393,216 keys
+  // the selection kernel keeps one score per key block of the longest sequence
+  // in shared memory (48 KB: 12,288 blocks, 1,572,864 keys)
+  if (static_cast<size_t>(nk_max) * sizeof(float) > 48 * 1024) return JFA_ERR_UNSUPPORTED;
   const TopkLayout lay = topk_layout(static_cast<int>(mt.size()), n_units, head_dim);
   if (workspace == nullptr || workspace_bytes < lay.total) return JFA_ERR_WORKSPACE_TOO_SMALL;
   st = current_device(&c.dev);

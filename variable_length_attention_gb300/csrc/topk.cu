@@ -193,13 +193,7 @@ int launch_topk_select(const TopkArgs& a) {
   }
   if (a.n_units == 0) return JFA_OK;
   const size_t smem = static_cast<size_t>(a.nk_max) * sizeof(float);  // one score per key block
-  if (smem > 48 * 1024) {  // a sequence of more than 12,288 key blocks: opt in to more shared memory
-    const cudaError_t e = a.D == 128 ? cudaFuncSetAttribute(topk::select_kernel<128>,
-                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                                     : cudaFuncSetAttribute(topk::select_kernel<64>,
-                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return JFA_ERR_UNSUPPORTED;  // beyond the device's shared memory per block
-  }
+  if (smem > 48 * 1024) return JFA_ERR_UNSUPPORTED;  // the entry point rejects such sequences first
   ProfileScope prof(kKindTopk, a.stream);
   if (a.D == 128)
     topk::select_kernel<128><<<a.n_units, 32 * topk::kSelWarps, smem, a.stream>>>(a.means, a.sel_tasks, a.topk,
