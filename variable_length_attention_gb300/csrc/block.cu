@@ -922,17 +922,50 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const bool valid = rr < blk.len;
           const bool full_half = blk.len == kBlk;
           const size_t row = (static_cast<size_t>(blk.row0 + rr) * p.H + h) * D;
-          if constexpr (!ROPE) {
+          {
             // dQ, dK, dV one 64-column box at a time through the two halves of
             // the staging buffer: the rows of one box are written while TMA still
-            // reads the other
+            // reads the other.  Rotary: dQ and dK are gradients with respect to
+            // the rotated rows, so the whole fp32 row goes back through the
+            // transposed rotation (pairs (i, i + D/2)) into registers first, then
+            // its two boxes are staged in turn.
+            uint32_t wrow[ROPE ? D / 2 : 1];  // rotary: the row's bf16 pairs
   #pragma unroll 1
-            for (int s = 0; s < 6; ++s) {
-              const int which = s >> 1, box = s & 1;
+            for (int which = 0; which < 3; ++which) {
               const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
               const float mul = which == 2 ? 1.0f : p.scale;
               const CUtensorMap* tm_out = which == 0 ? &tm_dq : (which == 1 ? &tm_dk : &tm_dv);
               __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
+              const bool rotated = ROPE && which < 2;
+              if constexpr (ROPE) {
+                if (rotated) {
+                  const uint64_t sc = f32x2(mul, mul);
+  #pragma unroll
+                  for (int r2 = 0; r2 < 2; ++r2) {
+                    uint32_t vx[32], vy[32];
+                    tmem_ld32(tmem + lane_addr + col + 32 * r2, vx);
+                    tmem_ld32(tmem + lane_addr + col + D / 2 + 32 * r2, vy);
+                    tmem_wait_ld();
+                    reg_fence<32>(vx);
+                    reg_fence<32>(vy);
+  #pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                      // cos and sin of pairs (32 r2 + 2e, +1), times the softmax scale
+                      const uint4& tq = tab[8 * r2 + e / 2];
+                      const uint64_t c = fmul2(h2_to_f32x2(e & 1 ? tq.z : tq.x), sc);
+                      const uint64_t sn = fmul2(h2_to_f32x2(e & 1 ? tq.w : tq.y), sc);
+                      uint64_t uo, vo;
+                      rot2<true>(f32x2(__uint_as_float(vx[2 * e]), __uint_as_float(vx[2 * e + 1])),
+                                 f32x2(__uint_as_float(vy[2 * e]), __uint_as_float(vy[2 * e + 1])), c, sn, uo, vo);
+                      wrow[16 * r2 + e] = f32x2_to_bf16x2(uo);
+                      wrow[D / 4 + 16 * r2 + e] = f32x2_to_bf16x2(vo);
+                    }
+                  }
+                }
+              }
+  #pragma unroll
+              for (int box = 0; box < 2; ++box) {
+              const int s = 2 * which + box;
               if (s >= 2) {  // the box's previous rows (two stages back) have been read out
                 if (threadIdx.x == 128) {
                   bulk_wait_read_all_but_newest();
@@ -941,16 +974,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 if (!mbar_wait(&bars->box_free[box], box_free_ph[box], ab)) goto done;
                 box_free_ph[box] ^= 1;
               }
-  #pragma unroll 1
-              for (int c = 64 * box; c < 64 * box + 64; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + col + c, v);
-                tmem_wait_ld();
-                reg_fence<32>(v);
-                uint32_t w[16];
   #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                  w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+              for (int c = 64 * box; c < 64 * box + 64; c += 32) {
+                uint32_t w[16];
+                if (rotated) {
+  #pragma unroll
+                  for (int e = 0; e < 16; ++e) w[e] = wrow[(ROPE ? c / 2 : 0) + e];
+                } else {
+                  uint32_t v[32];
+                  tmem_ld32(tmem + lane_addr + col + c, v);
+                  tmem_wait_ld();
+                  reg_fence<32>(v);
+  #pragma unroll
+                  for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                }
   #pragma unroll
                 for (int e = 0; e < 4; ++e) st_row_piece(sP, r, box, (c % 64) / 8 + e, w + 4 * e);
                 if (valid && !full_half) {
@@ -977,95 +1015,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 }
                 bulk_commit_group();
               }
-            }
-          } else
-  #pragma unroll 1
-          for (int which = 0; which < 3; ++which) {
-            const uint32_t col = which == 0 ? COL_S : (which == 1 ? COL_DP : COL_DV);
-            const float mul = which == 2 ? 1.0f : p.scale;
-            const CUtensorMap* tm_out = which == 0 ? &tm_dq : (which == 1 ? &tm_dk : &tm_dv);
-            __nv_bfloat16* dst = (which == 0 ? p.dq : (which == 1 ? p.dk : p.dv)) + row;
-            if (which > 0) {  // the previous result's boxes must have been read out
-              if (threadIdx.x == 128) {
-                bulk_wait_read_all();
-                mbar_arrive(&bars->stg_free);
               }
-              if (!mbar_wait(&bars->stg_free, stg_free_ph, ab)) goto done;
-              stg_free_ph ^= 1;
-            }
-            // columns c..c+31 of the result row, as bf16 pairs: staged (pieces
-            // (c%64)/8 .. (c%64)/8+3 of the 64-column box c/64) and, for a short
-            // block, stored
-            auto put = [&](int c, const uint32_t* w) {
-  #pragma unroll
-              for (int e = 0; e < 4; ++e) st_row_piece(sP, r, c / 64, (c % 64) / 8 + e, w + 4 * e);
-              if (valid && !full_half) {
-  #pragma unroll
-                for (int e = 0; e < 4; ++e) st_global_v4(dst + c + 8 * e, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-              }
-            };
-            if (!(ROPE && which < 2)) {
-              // the result row into the staging buffer, 32 columns at a time
-#pragma unroll 1
-              for (int c = 0; c < D; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + col + c, v);
-                tmem_wait_ld();
-                reg_fence<32>(v);
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-                put(c, w);
-              }
-            } else {
-              // dQ and dK are gradients with respect to the rotated rows: the
-              // transposed rotation of the fp32 row, pairs (i, i + D/2), before
-              // it is rounded and staged; 32 pairs per round
-              const uint64_t sc = f32x2(mul, mul);
-#pragma unroll 1
-              for (int r2 = 0; r2 < 2; ++r2) {
-                uint32_t vx[32], vy[32];
-                tmem_ld32(tmem + lane_addr + col + 32 * r2, vx);
-                tmem_ld32(tmem + lane_addr + col + D / 2 + 32 * r2, vy);
-                tmem_wait_ld();
-                reg_fence<32>(vx);
-                reg_fence<32>(vy);
-                uint32_t wx[16], wy[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  // cos and sin of pairs (32 r2 + 2e, +1), times the softmax scale
-                  const uint4& tq = tab[8 * r2 + e / 2];
-                  const uint64_t c = fmul2(h2_to_f32x2(e & 1 ? tq.z : tq.x), sc);
-                  const uint64_t sn = fmul2(h2_to_f32x2(e & 1 ? tq.w : tq.y), sc);
-                  uint64_t uo, vo;
-                  rot2<true>(f32x2(__uint_as_float(vx[2 * e]), __uint_as_float(vx[2 * e + 1])),
-                             f32x2(__uint_as_float(vy[2 * e]), __uint_as_float(vy[2 * e + 1])), c, sn, uo, vo);
-                  wx[e] = f32x2_to_bf16x2(uo);
-                  wy[e] = f32x2_to_bf16x2(vo);
-                }
-                put(32 * r2, wx);
-                put(D / 2 + 32 * r2, wy);
-              }
-            }
-            if (which == 2) {  // every accumulator is in registers or staged: TMEM is free
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars->t_free);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->stg_full);
-            if (!mbar_wait(&bars->stg_full, stg_full_ph, ab)) goto done;
-            stg_full_ph ^= 1;
-            if (threadIdx.x == 128) {
-  #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const Blk bk = hf == 0 ? blk_a : blk_b;
-                if (bk.len != kBlk) continue;
-  #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc)
-                  tma_store_2d(tm_out, smem + C::OFF_PDS + cc * 16384 + hf * 8192, h * D + 64 * cc, bk.row0);
-              }
-              bulk_commit_group();
             }
           }
           // the next tile's P goes into the same buffer: wait for the last boxes
@@ -1121,7 +1071,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               // transposed rotation of the whole fp32 row, pairs (i, i + D/2),
               // (g_i, g_i') -> (g_i c + g_i' s, g_i' c - g_i s), rounded once
               const uint64_t sc = f32x2(mul, mul);
-#pragma unroll 1
+#pragma unroll
               for (int r2 = 0; r2 < 2; ++r2) {  // pairs [16 r2, 16 r2 + 16)
                 uint32_t vx[16], vy[16];
                 tmem_ld16(tmem + lane_addr + col + 16 * r2, vx);
