@@ -613,8 +613,8 @@ struct BwdBars {
   uint64_t qk_full[3], qk_empty[3], vdo_full[2], vdo_empty[2];
   uint64_t qk_rot[3];  // rotary variant: Q and K of the slot are rotated
   uint64_t s_full, dp_full, p_full, p_used, ds_full, acc_full, t_free;
-  uint64_t stg_full, stg_free;  // epilogue staging in the P/dS buffer: rows written / read out by TMA
-  uint64_t box_full[2], box_free[2];  // the same per 64-column box (D = 128, no rotary: pipelined)
+  uint64_t stg_free;  // D = 128 epilogue: every staged box read out by TMA (the next P may go in)
+  uint64_t box_full[2], box_free[2];  // the same buffer per 64-column box: rows written / read out
   uint64_t drain;
   uint64_t sched_full[4], sched_empty[4], clc_bar;  // schedule ring (chunks), see publish()
   int sched_unit[4];
@@ -663,7 +663,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_used, 1);
-    mbar_init(&bars->stg_full, 128);
     mbar_init(&bars->stg_free, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->box_full[b], 128);
@@ -822,7 +821,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     uint8_t* sDS = sP;  // the same buffer: dS goes in once the dV GEMM has read P
     const float sl2 = p.scale_log2;
     const uint32_t zero[4] = {0u, 0u, 0u, 0u};
-    uint32_t stg_full_ph = 0, stg_free_ph = 0;
+    uint32_t stg_free_ph = 0;
     uint32_t box_full_ph[2] = {0, 0}, box_free_ph[2] = {0, 0};
     TileCursor cur;
     Locator locate;
