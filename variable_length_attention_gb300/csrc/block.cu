@@ -153,16 +153,7 @@ struct Locator {
   }
 };
 
-// Rotates Q and K rows [r0, r0 + NROWS) of one 64-row half of a tile pair in place, each tile
-// stored as D/64 128-byte-swizzled 64-column boxes: for i < D/2 the pair
-// (x_i, x_{i+D/2}) becomes (x_i c_i - x_{i+D/2} s_i, x_{i+D/2} c_i + x_i s_i), c and
-// s from the packed table row of the row's position.  One warp: each lane takes
-// a 16-byte chunk of the first half of a row (columns 8j..8j+7) and its partner
-// chunk of the second half, 4 rows per step at D = 128 (8 at D = 64).  Steps go
-// in batches of B: the batch's shared-memory loads are all issued before its
-// stores, and the next batch's table rows load while this one is rotated, so
-// neither the shared-memory nor the table latency is paid per row.  Rows past
-// the block's end are left alone (their scores are masked).
+// Byte offset of column c of row `row` in a tile of 128-byte-swizzled 64-column boxes.
 template <int D>
 __device__ __forceinline__ uint32_t rot_off(int row, int c) {
   return (c / 64) * 16384 + row * 128 + ((((c % 64) / 8) ^ (row & 7)) << 4);
@@ -189,6 +180,16 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t r) {
   f32x2_split(r, lo, hi);
   return pack_bf16(lo, hi);
 }
+// Rotates Q and K rows [r0, r0 + NROWS) of one 64-row half of a tile pair in place, each tile
+// stored as D/64 128-byte-swizzled 64-column boxes: for i < D/2 the pair
+// (x_i, x_{i+D/2}) becomes (x_i c_i - x_{i+D/2} s_i, x_{i+D/2} c_i + x_i s_i), c and
+// s from the packed table row of the row's position.  One warp: each lane takes
+// a 16-byte chunk of the first half of a row (columns 8j..8j+7) and its partner
+// chunk of the second half, 4 rows per step at D = 128 (8 at D = 64).  Steps go
+// in batches of B: the batch's shared-memory loads are all issued before its
+// stores, and the next batch's table rows load while this one is rotated, so
+// neither the shared-memory nor the table latency is paid per row.  Rows past
+// the block's end are left alone (their scores are masked).
 // `ready` is called once the first batch's table rows are on their way (it waits
 // for the tile to land, so the table latency overlaps that wait); false aborts.
 struct NoWait {
